@@ -1,0 +1,161 @@
+"""fp64 CPU oracle for the FlashAttention forward (materialises S and P).
+
+TEST INFRASTRUCTURE.  Only tests/, __graft_entry__.smoke() and bench.py's
+cpu_baseline / reference arm may import or run anything in this package; the
+product path (attention_forward_fa_gb300) never does, and nothing here imports
+the product path.
+
+What it computes is the plain definition of attention, written out:
+
+  S[i, j] = scale * sum_d Q[i, d] K[j, d]
+  P[i, j] = exp(S[i, j] - m_i) / sum_j' exp(S[i, j'] - m_i),  m_i = max_j S[i, j]
+  O[i]    = sum_j P[i, j] V[j]
+  LSE[i]  = m_i + ln sum_j exp(S[i, j] - m_i)
+
+  * the three-line definition of standard attention and the numerically stable
+    softmax of FlashAttention correctness verification (ai6s.net), sections
+    "Standard Attention vs FlashAttention: mathematical equivalence" and
+    "Layered test framework" (standard_attention);
+  * scale and masking as in the FlashAttentionScore operator doc (gitcode
+    ops-transformer), section "Function description", forward formula;
+  * LSE as the natural log of the row sum over scaled scores, the quantity the
+    backward re-uses as P = exp(scale*S - LSE) (BSA PyPTO implementation notes,
+    section 3.2 "Core design strategies", recomputation strategy).
+
+The valid key set J(i) of each query row is where the variants differ:
+  * dense: every key j < kv_len;
+  * causal (mask_mode 1): keys j > i are masked (top-left aligned);
+  * per-batch lengths: keys j >= seqlens[b] are masked; query rows
+    i >= seqlens[b] are padding (BSA notes, section 3.2, per-batch boundary mask);
+  * block-sparse: the keys of the KV blocks listed for the row's 128-row Q block
+    (Mask2Idx compact lists, BSA notes section 1); a slot < 0 or >= #blocks is
+    invalid and contributes nothing; mask_mode 2 applies j > i only inside the
+    diagonal block;
+  * top-k (sparse MLA): the keys listed for the row's token, shared by all heads
+    (sparse-MLA exact-max page, section "Background: sparse MLA and top-k
+    gathered KV"); a slot < 0 or >= kv_len is invalid.
+A key listed by two valid slots contributes twice (slot semantics).
+
+Readings where the pages are silent: a row with no valid key, and a padded row
+i >= seqlens[b], gets O = 0 and LSE = +inf (so that a backward's
+exp(scale*S - LSE) is 0 there).  The lazy-rescale threshold does not change
+this result: every threshold reaches the same exact value.
+
+Everything is float64 from the exact bf16/fp16 input values; numpy's matmul is
+the only library step.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+
+BLOCK = 128
+MASK_NONE, MASK_CAUSAL, MASK_CAUSAL_DIAG_BLOCK = 0, 1, 2
+
+
+def _softmax_rows(s: np.ndarray, w: np.ndarray):
+    """Masked softmax over the last axis.
+
+    s: scaled scores (float64); w: non-negative integer multiplicity of each
+    column (0 = masked).  Returns (P, LSE) with P rows of empty sets = 0 and
+    LSE = +inf for them.
+    """
+    valid = w > 0
+    neg = np.where(valid, s, -np.inf)
+    m = neg.max(axis=-1, keepdims=True)
+    empty = ~np.isfinite(m)
+    m_safe = np.where(empty, 0.0, m)
+    e = np.exp(np.where(valid, s - m_safe, -np.inf)) * w
+    l = e.sum(axis=-1, keepdims=True)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        p = np.where(empty, 0.0, e / np.where(empty, 1.0, l))
+        lse = np.where(empty, np.inf, m_safe + np.log(np.where(empty, 1.0, l)))
+    return p, lse[..., 0]
+
+
+def attention_fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
+                  mask: int = MASK_NONE, seqlens: Optional[np.ndarray] = None,
+                  kv_block_idx: Optional[np.ndarray] = None,
+                  topk_idx: Optional[np.ndarray] = None,
+                  block: int = BLOCK, rows: Optional[np.ndarray] = None,
+                  heads: Optional[np.ndarray] = None, batches: Optional[np.ndarray] = None,
+                  return_p: bool = False):
+    """Reference forward.
+
+    q [B,Hq,Sq,D], k [B,Hkv,Skv,D], v [B,Hkv,Skv,Dv] (float64 values).
+    kv_block_idx [B, Hq or 1, ceil(Sq/block), max_sel]; topk_idx [B, Sq, W].
+    ``rows``/``heads``/``batches`` optionally restrict which outputs are
+    computed (for sampling large problems); skipped outputs stay NaN.
+    Returns O [B,Hq,Sq,Dv] and LSE [B,Hq,Sq] (float64); with return_p also a
+    dict (b, h) -> (P over the full key axis with multiplicity folded in).
+    """
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Skv, _ = k.shape
+    Dv = v.shape[-1]
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    G = Hq // Hkv
+    O = np.full((B, Hq, Sq, Dv), np.nan)
+    LSE = np.full((B, Hq, Sq), np.nan)
+    Ps = {}
+    row_set = np.arange(Sq) if rows is None else np.asarray(rows)
+    head_set = np.arange(Hq) if heads is None else np.asarray(heads)
+    batch_set = np.arange(B) if batches is None else np.asarray(batches)
+    nkb = (Skv + block - 1) // block
+    for b in batch_set:
+        qlen = Sq if seqlens is None else int(seqlens[b])
+        kvlen = Skv if seqlens is None else int(seqlens[b])
+        for h in head_set:
+            kh = h // G
+            for r0 in range(0, row_set.size, 256):
+                ri = row_set[r0:r0 + 256]
+                w = _multiplicity(ri, b, h, qlen, kvlen, Skv, nkb, block, mask,
+                                  kv_block_idx, topk_idx)
+                s = scale * (q[b, h, ri, :] @ k[b, kh].T)
+                p, lse = _softmax_rows(s, w)
+                O[b, h, ri, :] = p @ v[b, kh]
+                LSE[b, h, ri] = lse
+                if return_p:
+                    Ps[(int(b), int(h), int(r0))] = p
+    if return_p:
+        return O, LSE, Ps
+    return O, LSE
+
+
+def _multiplicity(ri, b, h, qlen, kvlen, Skv, nkb, block, mask, kv_block_idx, topk_idx):
+    """Integer weight of every (row, key) pair: how many valid slots list the
+    key for the row (1 for dense), 0 where masked."""
+    n = ri.size
+    j = np.arange(Skv)
+    w = np.zeros((n, Skv), dtype=np.float64)
+    if topk_idx is not None:
+        for t, i in enumerate(ri):
+            sl = topk_idx[b, i]
+            sl = sl[(sl >= 0) & (sl < kvlen)]
+            np.add.at(w[t], sl, 1.0)
+    elif kv_block_idx is not None:
+        hl = h if kv_block_idx.shape[1] > 1 else 0
+        for t, i in enumerate(ri):
+            qb = i // block
+            for s in kv_block_idx[b, hl, qb]:
+                if s < 0 or s >= nkb:
+                    continue
+                lo, hi = s * block, min((s + 1) * block, Skv)
+                if mask == MASK_CAUSAL_DIAG_BLOCK and s == qb:
+                    hi = min(hi, i + 1)
+                w[t, lo:hi] += 1.0
+    else:
+        w[:, :] = 1.0
+    w[:, j >= kvlen] = 0.0
+    if mask == MASK_CAUSAL:
+        w[j[None, :] > ri[:, None]] = 0.0
+    w[ri >= qlen, :] = 0.0
+    return w
+
+
+def attention_problem(p, **kw):
+    """Run the oracle on a workloads.Problem-like object (duck-typed: needs
+    q()/k()/v(), scale, mask, seqlens, kv_block_idx, topk_idx)."""
+    return attention_fwd(p.q(), p.k(), p.v(), p.scale, mask=p.mask, seqlens=p.seqlens,
+                         kv_block_idx=p.kv_block_idx, topk_idx=p.topk_idx, **kw)
