@@ -1,0 +1,13 @@
+"""GB300 (sm_103a) tiled FlashAttention forward.
+
+The computation runs in hand-written CUDA kernels behind the C ABI of
+libfa_fwd.so (include/fa_fwd.h).  This package is the Python binding: the
+same entry points, argument marshalling only (torch tensors -> device
+pointers, the current torch stream).  There is no fallback: without the
+library every call raises.
+"""
+from ._binding import (  # noqa: F401
+    FA_DTYPE_FP16, FA_MASK_CAUSAL, FA_MASK_CAUSAL_DIAG_BLOCK, FA_MASK_NONE, FA_V_FROM_K,
+    FaError, fa_check_status, fa_fwd, fa_set_wait_timeout_ns, fa_strerror, flash_attention_forward,
+    library, library_path,
+)

@@ -1,0 +1,172 @@
+"""ctypes binding of libfa_fwd.so (see include/fa_fwd.h for the contract)."""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(PKG, "libfa_fwd.so")
+
+FA_MASK_NONE = 0
+FA_MASK_CAUSAL = 1
+FA_MASK_CAUSAL_DIAG_BLOCK = 2
+FA_DTYPE_FP16 = 0x100
+FA_V_FROM_K = 0x200
+
+FA_OK = 0
+
+
+class FaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"fa_fwd error {code}: {msg}")
+        self.code = code
+
+
+class fa_block_sparse_t(ctypes.Structure):
+    _fields_ = [("idx", ctypes.c_void_p), ("max_sel", ctypes.c_int32), ("block", ctypes.c_int32),
+                ("stride_b", ctypes.c_int64), ("stride_h", ctypes.c_int64)]
+
+
+class fa_topk_t(ctypes.Structure):
+    _fields_ = [("idx", ctypes.c_void_p), ("topk", ctypes.c_int32), ("stride_b", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def library() -> ctypes.CDLL:
+    """Load libfa_fwd.so (raises OSError if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise OSError(f"{_LIB_PATH} is missing: build it with "
+                          "`python -m attention_forward_fa_gb300.build`")
+        lib = ctypes.CDLL(_LIB_PATH)
+        lib.fa_fwd.restype = ctypes.c_int
+        lib.fa_fwd.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 7 + [
+            ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(fa_block_sparse_t),
+            ctypes.POINTER(fa_topk_t), ctypes.c_float, ctypes.c_void_p]
+        lib.fa_check_status.restype = ctypes.c_int
+        lib.fa_check_status.argtypes = [ctypes.c_void_p]
+        lib.fa_set_wait_timeout_ns.restype = None
+        lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_int64]
+        lib.fa_strerror.restype = ctypes.c_char_p
+        lib.fa_strerror.argtypes = [ctypes.c_int]
+        lib.fa_last_cuda_error.restype = ctypes.c_int
+        lib.fa_last_cuda_error_string.restype = ctypes.c_char_p
+        _lib = lib
+    return _lib
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def fa_strerror(code: int) -> str:
+    return library().fa_strerror(code).decode()
+
+
+def fa_fwd(q, k, v, o, lse, B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int, Dv: int,
+           scale: float, mask_mode: int, seqlens=None, kv_block_idx=None, topk_idx=None,
+           rescale_threshold: float = 0.0, stream=None) -> int:
+    """Direct call of the C entry point.  Tensors (or raw device pointers) for
+    q, k, v, o, lse, seqlens; kv_block_idx = (idx, max_sel, block, stride_b,
+    stride_h) and topk_idx = (idx, topk, stride_b) with device index arrays.
+    Returns the FA_* code."""
+    lib = library()
+    bs = None
+    if kv_block_idx is not None:
+        idx, max_sel, block, sb, sh = kv_block_idx
+        bs = ctypes.pointer(fa_block_sparse_t(_ptr(idx), max_sel, block, sb, sh))
+    tk = None
+    if topk_idx is not None:
+        idx, topk, sb = topk_idx
+        tk = ctypes.pointer(fa_topk_t(_ptr(idx), topk, sb))
+    return lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, D, Dv,
+                      float(scale), int(mask_mode), _ptr(seqlens), bs, tk,
+                      float(rescale_threshold), _stream(stream))
+
+
+def fa_check_status(stream=None) -> int:
+    return library().fa_check_status(_stream(stream))
+
+
+def fa_set_wait_timeout_ns(ns: int) -> None:
+    library().fa_set_wait_timeout_ns(int(ns))
+
+
+def _raise(code: int):
+    if code != FA_OK:
+        lib = library()
+        msg = lib.fa_strerror(code).decode()
+        if code == -6:
+            msg += f" ({lib.fa_last_cuda_error_string().decode()})"
+        raise FaError(code, msg)
+
+
+def flash_attention_forward(q, k, v=None, *, scale: Optional[float] = None, causal: bool = False,
+                            mask_mode: Optional[int] = None, seqlens=None, block_idx=None,
+                            topk_idx=None, rescale_threshold: float = 0.0, out=None, lse=None,
+                            stream=None):
+    """Allocating convenience wrapper over fa_fwd.
+
+    q [B,Hq,Sq,D], k [B,Hkv,Skv,D], v [B,Hkv,Skv,Dv] (or None with top-k and a
+    shared latent), bf16 or fp16 CUDA tensors.  block_idx: int32 tensor
+    [B, Hq or 1, ceil(Sq/128), max_sel]; topk_idx: int32 [B, Sq, W].
+    Returns (o, lse)."""
+    import torch
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("q, k, v must be bf16 or fp16")
+    for t in (q, k, v):
+        if t is not None and (not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype):
+            raise ValueError("q, k, v must be contiguous CUDA tensors of one dtype")
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Skv, _ = k.shape
+    v_from_k = v is None
+    Dv = v.shape[-1] if v is not None else 512
+    if mask_mode is None:
+        mask_mode = FA_MASK_CAUSAL if causal else FA_MASK_NONE
+    if q.dtype == torch.float16:
+        mask_mode |= FA_DTYPE_FP16
+    if v_from_k:
+        mask_mode |= FA_V_FROM_K
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, Sq, Dv), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    bs = None
+    if block_idx is not None:
+        assert block_idx.dtype == torch.int32 and block_idx.is_contiguous()
+        nb, hh, nqb, ms = block_idx.shape
+        bs = (block_idx, ms, 128, hh * nqb * ms, nqb * ms if hh > 1 else 0)
+    tk = None
+    if topk_idx is not None:
+        assert topk_idx.dtype == torch.int32 and topk_idx.is_contiguous()
+        tk = (topk_idx, topk_idx.shape[-1], topk_idx.shape[-2] * topk_idx.shape[-1])
+    if seqlens is not None:
+        assert seqlens.dtype == torch.int32 and seqlens.is_cuda
+    code = fa_fwd(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens, bs, tk,
+                  rescale_threshold, stream)
+    _raise(code)
+    return out, lse

@@ -1,0 +1,227 @@
+// Host side of libfa_fwd.so: argument validation, TMA descriptors, variant
+// selection and launch.  The C ABI is declared in include/fa_fwd.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa_fwd.h"
+#include "fa_tiled.cuh"
+
+namespace {
+
+// Device status word of this module (one per device the library runs on):
+// bit 0 = a bounded wait expired, bit 1 = a bf16 V value overflowed fp16.
+__device__ int g_fa_status;
+
+std::atomic<int> g_last_cuda{0};
+std::atomic<long long> g_timeout_ns{2000000000LL};
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda.store((int)e);
+  return FA_ERR_CUDA;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 3-D view (cols, rows, planes) of a contiguous [planes, rows, cols] 16-bit
+// tensor, tiled in boxes of 64 columns x box_rows rows with 128-byte swizzle.
+bool encode_3d(CUtensorMap* tm, const void* base, bool fp16, uint64_t cols, uint64_t rows,
+               uint64_t planes, uint32_t box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {cols, rows, planes};
+  cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(tm, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int* status_ptr() {
+  // the symbol's device address for the current device
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_fa_status) != cudaSuccess) return nullptr;
+  return static_cast<int*>(ptr);
+}
+
+template <int D, bool BF16, int NS>
+int launch_tiled(const fa::TiledParams& prm, int units, cudaStream_t st) {
+  auto kern = fa::fa_fwd_tiled_kernel<D, BF16, NS>;
+  constexpr int smem = fa::TiledSmem<D, NS>::kAlloc;
+  static std::once_flag once[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaError_t attr_err = cudaSuccess;
+  std::call_once(once[dev & 63], [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  if (attr_err != cudaSuccess) return cuda_fail(attr_err);
+  kern<<<units, fa::kTiledThreads, smem, st>>>(prm);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+           int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
+           const int32_t* seqlens, const fa_block_sparse_t* kv_block_idx,
+           const fa_topk_t* topk_idx, float rescale_threshold, void* stream) {
+  const int mask = mask_mode & 0xF;
+  const bool fp16 = (mask_mode & FA_DTYPE_FP16) != 0;
+  const bool v_from_k = (mask_mode & FA_V_FROM_K) != 0;
+  if (mask_mode & ~(0xF | FA_DTYPE_FP16 | FA_V_FROM_K)) return FA_ERR_SHAPE;
+  // ---- pointers
+  if (!q || !k || !o || !lse || (!v && !v_from_k)) return FA_ERR_NULL;
+  if (kv_block_idx && !kv_block_idx->idx) return FA_ERR_NULL;
+  if (topk_idx && !topk_idx->idx) return FA_ERR_NULL;
+  // ---- shapes
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || D <= 0 || Dv <= 0)
+    return FA_ERR_SHAPE;
+  if (Hq % Hkv) return FA_ERR_SHAPE;
+  if (kv_block_idx && topk_idx) return FA_ERR_SHAPE;
+  if (mask > FA_MASK_CAUSAL_DIAG_BLOCK) return FA_ERR_SHAPE;
+  if (mask == FA_MASK_CAUSAL_DIAG_BLOCK && !kv_block_idx) return FA_ERR_SHAPE;
+  if (kv_block_idx) {
+    if (kv_block_idx->block != 128) return FA_ERR_SHAPE;
+    if (kv_block_idx->max_sel <= 0 || kv_block_idx->max_sel > fa::kMaxSel) return FA_ERR_SHAPE;
+    if (kv_block_idx->stride_b < 0 || kv_block_idx->stride_h < 0) return FA_ERR_SHAPE;
+  }
+  if (topk_idx && (topk_idx->topk <= 0 || topk_idx->stride_b < 0)) return FA_ERR_SHAPE;
+  if (!std::isfinite(scale)) return FA_ERR_SHAPE;
+  if (!(rescale_threshold >= 0.f && rescale_threshold <= 15.f)) return FA_ERR_THRESHOLD;
+  if ((long long)B * Hq > (1LL << 30) || (long long)Sq * 128 > (1LL << 31) ||
+      (long long)Skv * 128 > (1LL << 31))
+    return FA_ERR_SHAPE;
+  // ---- supported variants
+  const bool tiled = !topk_idx && !v_from_k && D == Dv && (D == 64 || D == 128);
+  if (!tiled) return FA_ERR_UNSUPPORTED;
+  // ---- alignment (TMA: 16-byte bases; vector stores of O)
+  if (!aligned(q, 16) || !aligned(k, 16) || (v && !aligned(v, 16)) || !aligned(o, 16) ||
+      !aligned(lse, 4))
+    return FA_ERR_ALIGN;
+  if (seqlens && !aligned(seqlens, 4)) return FA_ERR_ALIGN;
+  if (kv_block_idx && !aligned(kv_block_idx->idx, 4)) return FA_ERR_ALIGN;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* status = status_ptr();
+  if (!status) return cuda_fail(cudaGetLastError());
+
+  fa::TiledParams prm;
+  std::memset(&prm, 0, sizeof(prm));
+  if (!encode_3d(&prm.tm_q, q, fp16, D, Sq, (uint64_t)B * Hq, fa::kBM) ||
+      !encode_3d(&prm.tm_k, k, fp16, D, Skv, (uint64_t)B * Hkv, fa::kBN) ||
+      !encode_3d(&prm.tm_v, v, fp16, Dv, Skv, (uint64_t)B * Hkv, fa::kBN))
+    return cuda_fail(cudaErrorInvalidValue);
+  prm.o = o;
+  prm.lse = lse;
+  prm.seqlens = seqlens;
+  if (kv_block_idx) {
+    prm.blk_idx = kv_block_idx->idx;
+    prm.blk_stride_b = kv_block_idx->stride_b;
+    prm.blk_stride_h = kv_block_idx->stride_h;
+    prm.max_sel = kv_block_idx->max_sel;
+  }
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.Sq = Sq;
+  prm.Skv = Skv;
+  prm.G = Hq / Hkv;
+  prm.mask = mask;
+  prm.n_qt = (Sq + fa::kBM - 1) / fa::kBM;
+  // Slot pairing: two heads of one GQA group at the same query tile when the
+  // group size is even (identical KV sequence), else two consecutive query
+  // tiles of one head.  Block lists that differ per head or per query block
+  // simply give the two slots independent KV sequences.
+  const bool head_pairs = (prm.G % 2 == 0);
+  prm.pair_mode = head_pairs ? 1 : 0;
+  if (head_pairs) {
+    prm.units_per_q = B * (Hq / 2);
+    prm.n_qpos = prm.n_qt;
+  } else {
+    prm.units_per_q = B * Hq;
+    prm.n_qpos = (prm.n_qt + 1) / 2;
+  }
+  prm.scale = scale;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.threshold = rescale_threshold;
+  prm.timeout_ns = g_timeout_ns.load();
+  prm.status = status;
+  const long long units = (long long)prm.units_per_q * prm.n_qpos;
+  if (units > 0x7FFFFFFF) return FA_ERR_SHAPE;
+
+  if (D == 128) {
+    return fp16 ? launch_tiled<128, false, 4>(prm, (int)units, st)
+                : launch_tiled<128, true, 4>(prm, (int)units, st);
+  }
+  return fp16 ? launch_tiled<64, false, 6>(prm, (int)units, st)
+              : launch_tiled<64, true, 6>(prm, (int)units, st);
+}
+
+int fa_check_status(void* stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int h = 0;
+  e = cudaMemcpyFromSymbol(&h, g_fa_status, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (h) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_fa_status, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  if (h & fa::kStatusTimeout) return FA_ERR_DEVICE_TIMEOUT;
+  if (h & fa::kStatusRange) return FA_ERR_RANGE;
+  return FA_OK;
+}
+
+void fa_set_wait_timeout_ns(int64_t ns) { g_timeout_ns.store(ns > 0 ? ns : 2000000000LL); }
+
+const char* fa_strerror(int code) {
+  switch (code) {
+    case FA_OK: return "ok";
+    case FA_ERR_NULL: return "a required pointer is NULL";
+    case FA_ERR_SHAPE: return "invalid sizes or descriptor fields";
+    case FA_ERR_UNSUPPORTED: return "unsupported head dimension / mode combination";
+    case FA_ERR_ALIGN: return "tensor base address not aligned";
+    case FA_ERR_THRESHOLD: return "rescale_threshold outside [0, 15]";
+    case FA_ERR_CUDA: return "CUDA call failed";
+    case FA_ERR_DEVICE_TIMEOUT: return "bounded on-chip wait expired";
+    case FA_ERR_RANGE: return "bf16 V value outside the fp16 range";
+    default: return "unknown error code";
+  }
+}
+
+int fa_last_cuda_error(void) { return g_last_cuda.load(); }
+const char* fa_last_cuda_error_string(void) {
+  return cudaGetErrorName(static_cast<cudaError_t>(g_last_cuda.load()));
+}
+
+}  // extern "C"

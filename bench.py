@@ -1,0 +1,393 @@
+"""Benchmark of the tiled FlashAttention forward on GB300.
+
+Workload (one "step" = one forward over one batch): dense causal attention,
+B=2, H=16, Sq=Skv=2048, D=Dv=128, bf16 Q/K/V drawn N(0,1), scale 1/sqrt(128),
+fp32 LSE output.  Metric: algorithmic TFLOP/s = 2 (D + Dv) x unmasked
+(query, key) pairs / time, also reported as ms per call and as a fraction of
+the measured dense bf16 tensor peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs one process per GPU (torchrun); every rank runs its own replica of
+the workload (the forward shards over (b, h) with no exchange), so the
+scaling is weak and the whole-job value is the sum over ranks.
+The reference arm times the fp64 CPU oracle on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s on 1 GB300 and % of dense BF16 tensor peak; ms/call"
+L2_BYTES = 129 * 2 ** 20
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_forward_fa_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d, "measured"
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+            "sm_max_mhz": 2070.0}, "fallback"
+
+
+def dram_traffic(workload: str):
+    """ncu DRAM bytes per launch for the current kernel sources, else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path))
+    e = d.get(workload)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons, pw = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+                pw.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        load = [s for s in sm] or [None]
+        return {"sm_mhz": statistics.median(load) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(pw) if pw else None}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def workload_problem():
+    from attention_forward_fa_gb300 import workloads as W
+    return W.config(2)
+
+
+def workload_desc(p):
+    return {"workload": "dense causal attention forward, B=2 H=16 Sq=Skv=2048 D=Dv=128, bf16 "
+                        "Q/K/V ~ N(0,1), scale 1/sqrt(128), fp32 LSE",
+            "B": p.B, "H": p.Hq, "Sq": p.Sq, "Skv": p.Skv, "D": p.D, "Dv": p.Dv,
+            "mask": "causal", "rescale_threshold": 0.0}
+
+
+def oracle_rows(p, q, k, v, b, h, rows):
+    """Time the fp64 oracle on `rows` of head (b, h); returns (algorithmic
+    flops of those rows, seconds)."""
+    from oracle import attention as A
+    t0 = time.perf_counter()
+    A.attention_fwd(q, k, v, p.scale, mask=p.mask, seqlens=p.seqlens, rows=rows,
+                    heads=np.array([h]), batches=np.array([b]))
+    el = time.perf_counter() - t0
+    kv = p.Skv if p.seqlens is None else int(p.seqlens[b])
+    keys = np.minimum(rows + 1, kv) if p.mask == 1 else np.full(rows.size, kv)
+    return 2.0 * (p.D + p.Dv) * float(keys.sum()), el
+
+
+def row_sample(p, n_rows, step_index):
+    """n_rows rows spread evenly over [0, Sq) (so the causal work per row
+    matches the whole workload), shifted per step; head and batch rotate."""
+    stride = max(1, p.Sq // n_rows)
+    off = step_index % stride
+    rows = np.arange(off, p.Sq, stride)[:n_rows]
+    bh = step_index % (p.B * p.Hq)
+    return rows, bh // p.Hq, bh % p.Hq
+
+
+def oracle_timed(p, seconds):
+    """Oracle throughput on a bounded sample: consecutive row samples until
+    `seconds` of CPU work have passed.  Returns (flops, seconds, rows)."""
+    q, k, v = p.q(), p.k(), p.v()
+    f_tot = t_tot = 0.0
+    n = 0
+    i = 0
+    while t_tot < seconds:
+        rows, b, h = row_sample(p, 256, i)
+        f, t = oracle_rows(p, q, k, v, b, h, rows)
+        f_tot += f
+        t_tot += t
+        n += rows.size
+        i += 1
+    return f_tot, t_tot, n
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    p = workload_problem()
+    from attention_forward_fa_gb300 import workloads as W
+    q, k, v = p.q(), p.k(), p.v()
+    # size each step so that warm-up + K steps take about a minute
+    rows0, b0, h0 = row_sample(p, 64, 0)
+    _, t64 = oracle_rows(p, q, k, v, b0, h0, rows0)
+    per_row = max(t64 / 64, 1e-6)
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    n_rows = int(min(p.Sq, max(1, budget / per_row)))
+    for i in range(args.warmup):
+        rows, b, h = row_sample(p, n_rows, i)
+        oracle_rows(p, q, k, v, b, h, rows)
+    t_tot = f_tot = 0.0
+    for i in range(args.steps):
+        rows, b, h = row_sample(p, n_rows, args.warmup + i)
+        f, t = oracle_rows(p, q, k, v, b, h, rows)
+        f_tot += f
+        t_tot += t
+    value = f_tot / t_tot / 1e12
+    sample = (f"each step = {n_rows} query rows (spread over the sequence) of one (b, h) head "
+              f"of the workload, fp64 numpy oracle materialising S and P; the full workload is "
+              f"{W.algorithmic_flops(p) / 1e9:.2f} GFLOP")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * t_tot / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_desc(p),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import attention_forward_fa_gb300 as fa
+    from attention_forward_fa_gb300 import build as fa_build
+    from attention_forward_fa_gb300 import workloads as W
+
+    if rank == 0 or world == 1:
+        fa_build.build()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if rank != 0:
+            fa_build.build()  # no-op once rank 0 built it (mtime check)
+        dist.barrier()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    p = workload_problem()
+    flops = W.algorithmic_flops(p)
+    dt = torch.bfloat16
+
+    def up(bits):
+        return torch.from_numpy(bits.view(np.int16).copy()).to(dev).view(dt)
+
+    q0, k0, v0 = up(p.q_bits), up(p.k_bits), up(p.v_bits)
+    per_set = 2 * (q0.numel() + k0.numel() + v0.numel() + q0.numel()) + 4 * p.B * p.Hq * p.Sq
+    n_sets = max(2, int(np.ceil(2.5 * L2_BYTES / per_set)))
+    sets = []
+    for i in range(n_sets):
+        o = torch.empty((p.B, p.Hq, p.Sq, p.Dv), dtype=dt, device=dev)
+        lse = torch.empty((p.B, p.Hq, p.Sq), dtype=torch.float32, device=dev)
+        sets.append((q0.clone(), k0.clone(), v0.clone(), o, lse))
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    def step(i):
+        q, k, v, o, lse = sets[i % n_sets]
+        code = fa.fa_fwd(q, k, v, o, lse, p.B, p.Hq, p.Hkv, p.Sq, p.Skv, p.D, p.Dv, p.scale,
+                         p.mask, None, None, None, 0.0, sp)
+        if code != 0:
+            raise RuntimeError(fa.fa_strerror(code))
+
+    # warm-up, then an untimed soak so that clocks are sampled under load
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else local)
+    sampler.start()
+    t_soak = time.perf_counter()
+    i = 0
+    while time.perf_counter() - t_soak < args.soak:
+        for _ in range(200):
+            step(i)
+            i += 1
+        torch.cuda.synchronize()
+    # timed region: exactly K steps, one event pair per launch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    t_all0.record(stream)
+    for s in range(args.steps):
+        starts[s].record(stream)
+        step(s)
+        ends[s].record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    status = fa.fa_check_status()
+    if status != 0:
+        raise RuntimeError("device status after timed region: " + fa.fa_strerror(status))
+    total_ms = t_all0.elapsed_time(t_all1)
+    kern_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    kern_avg_ms = sum(kern_ms) / len(kern_ms)
+    if dist:
+        t = torch.tensor([total_ms, kern_avg_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, kern_avg_ms = float(t[0]), float(t[1])
+    ms_per_step = total_ms / args.steps
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+
+    # end to end through the public entry point with host buffers
+    pin = lambda x: x.cpu().pin_memory()  # noqa: E731
+    hq, hk, hv = pin(q0), pin(k0), pin(v0)
+    ho = torch.empty((p.B, p.Hq, p.Sq, p.Dv), dtype=dt).pin_memory()
+    hl = torch.empty((p.B, p.Hq, p.Sq), dtype=torch.float32).pin_memory()
+    dq, dk, dv, do, dl = sets[0]
+    h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2
+    d2h = ho.numel() * 2 + hl.numel() * 4
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        code = fa.fa_fwd(dq, dk, dv, do, dl, p.B, p.Hq, p.Hkv, p.Sq, p.Skv, p.D, p.Dv, p.scale,
+                         p.mask, None, None, None, 0.0, sp)
+        if code != 0:
+            raise RuntimeError(fa.fa_strerror(code))
+        ho.copy_(do, non_blocking=True)
+        hl.copy_(dl, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    n_e2e = max(3, min(args.steps, 50))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = flops / (kern_avg_ms * 1e-3) / 1e12
+    cfg = workload_desc(p)
+    cfg.update({"parallelism": f"replicas x{world} (no exchange)",
+                "l2": f"{n_sets} rotating input/output sets of {per_set / 2**20:.0f} MiB "
+                      f"(> 2 x 129 MiB L2), no flush",
+                "algorithmic_gflop_per_step": flops / 1e9})
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": cfg,
+            "pct_of_bf16_peak": 100.0 * achieved / peak,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_source": f"{peak_src} bf16_tflops (burst); P.V runs as fp16 at "
+                                        f"the same nominal rate",
+                         "traffic": dram_traffic("c2_causal"),
+                         "kernel": "fa_fwd_tiled_kernel<128,bf16,4>",
+                         "kernel_avg_ms": kern_avg_ms},
+            "clocks": clocks,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps}
+    if world == 1 and not args.no_cpu_baseline:
+        f, t, n = oracle_timed(p, args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": f / t / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} query rows of the same workload (256-row samples spread over the "
+                      f"sequence, rotating heads), fp64 numpy oracle materialising S and P, "
+                      f"{t:.1f} s; algorithmic flops of those rows / time"}
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed load before timing")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,161 @@
+/*
+ * fa_fwd.h -- C ABI of the GB300 (sm_103a) tiled FlashAttention forward.
+ *
+ * One operation: O = softmax(scale * Q K^T + mask) V for every query row,
+ * computed tile by tile with a per-row online softmax (running max m, running
+ * sum l, rescale of the O accumulator), never materialising S or P, plus the
+ * per-row log-sum-exp LSE = scale * m + ln(l) for a backward pass.
+ *
+ * Where the operation is defined:
+ *   - attention itself and its blockwise / online-softmax form:
+ *     "FlashAttention correctness verification" (ai6s.net), sections
+ *     "Standard Attention vs FlashAttention: mathematical equivalence" and
+ *     "Formal verification outline" (loop invariant, inductive step
+ *     L_{i+1} = L_i exp(m_i - m_{i+1}) + l_{i+1});
+ *   - scale, mask and the softmax max / sum outputs kept for the backward:
+ *     "FlashAttentionScore" operator doc (gitcode ops-transformer), sections
+ *     "Function description" (forward formula) and "Parameter description"
+ *     (softmaxMaxOut / softmaxSumOut);
+ *   - BNSD layout, GQA (Hq % Hkv == 0), per-batch actual sequence lengths,
+ *     compact per-Q-block KV-block lists with invalid slots, LSE semantics
+ *     P = exp(scale*S - LSE): "BSA (Block Sparse Attention) PyPTO
+ *     implementation notes", sections 1 "Overview", 3.2 "Core design
+ *     strategies" and 3.3 "Data layout and tiling";
+ *   - top-k gathered keys shared by all heads (sparse MLA, MQA) and the
+ *     exact-running-max versus lazy-rescale switch (threshold in log2 units):
+ *     "Sparse-MLA training forward: exact running max vs lazy rescale"
+ *     (cf-1.com), sections "Background: sparse MLA and top-k gathered KV" and
+ *     "Verifying the threshold branch from source".
+ *
+ * Conventions for every entry point below:
+ *   - All tensor pointers are caller-owned DEVICE memory on the current
+ *     device, contiguous, and must stay valid until the work on `stream` has
+ *     finished.  The library keeps no pointer after a call returns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream).  Argument errors are returned
+ *     synchronously and nothing is launched.  Device-side errors are
+ *     reported later through fa_check_status().
+ *   - The library allocates no device memory per call.
+ */
+#ifndef FA_FWD_H_
+#define FA_FWD_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ------------------------------------------------------ */
+#define FA_OK                   0
+#define FA_ERR_NULL            -1  /* a required pointer is NULL                      */
+#define FA_ERR_SHAPE           -2  /* a size <= 0, Hq % Hkv != 0, both sparse modes,  */
+                                   /* block != 128, max_sel / topk out of range, ...  */
+#define FA_ERR_UNSUPPORTED     -3  /* (D, Dv, dtype, mode) combination not built      */
+#define FA_ERR_ALIGN           -4  /* tensor base not 16-byte aligned (lse: 4 bytes)  */
+#define FA_ERR_THRESHOLD       -5  /* rescale_threshold outside [0, 15] or not finite */
+#define FA_ERR_CUDA            -6  /* a CUDA call failed; see fa_last_cuda_error()    */
+#define FA_ERR_DEVICE_TIMEOUT  -7  /* a bounded on-chip wait expired (kernel bailed)  */
+#define FA_ERR_RANGE           -8  /* a bf16 V value outside the fp16 range (|v| >    */
+                                   /* 65504) met the fp16 P.V product                 */
+
+/* ---- mask_mode flag word ----------------------------------------------- */
+/* bits 0-3: mask */
+#define FA_MASK_NONE             0  /* every key j < kv_len is visible                */
+#define FA_MASK_CAUSAL           1  /* key j masked for query i when j > i (top-left) */
+#define FA_MASK_CAUSAL_DIAG_BLOCK 2 /* block-sparse only: j > i masked only inside    */
+                                    /* the diagonal block (key block == query block)  */
+/* element type of q, k, v and o (default bf16) */
+#define FA_DTYPE_FP16        0x100
+/* top-k only: V is the first Dv columns of every K row (shared MLA latent);   */
+/* `v` may then be NULL */
+#define FA_V_FROM_K          0x200
+
+/* ---- sparse descriptors ------------------------------------------------ */
+
+/* Compact per-Q-block KV-block lists ("Mask2Idx", BSA notes section 1).
+ * The entry for batch b, query head h, query block qb, slot s is
+ *   idx[b*stride_b + h*stride_h + qb*max_sel + s]   (device int32)
+ * Query block qb covers rows [qb*block, qb*block + block); a valid entry e
+ * names keys [e*block, e*block + block).  An entry < 0 or >= ceil(Skv/block)
+ * is an invalid slot and contributes nothing.  stride_h = 0 shares one list
+ * among all heads.  Each valid slot counts once (a block listed twice counts
+ * twice).  Slots are visited in list order.  block must be 128, 1 <= max_sel
+ * <= 512. */
+typedef struct {
+  const int32_t* idx;
+  int32_t max_sel;
+  int32_t block;
+  int64_t stride_b;
+  int64_t stride_h;
+} fa_block_sparse_t;
+
+/* Top-k gathered keys, shared by all query heads (sparse MLA / MQA).
+ * The entry for batch b, query row i, slot w is idx[b*stride_b + i*topk + w]
+ * (device int32); an entry < 0 or >= kv_len is an invalid slot. */
+typedef struct {
+  const int32_t* idx;
+  int32_t topk;
+  int64_t stride_b;
+} fa_topk_t;
+
+/* ---- the forward ------------------------------------------------------- */
+/*
+ * fa_fwd -- attention forward with online softmax and LSE output.
+ *
+ *   q    [B, Hq,  Sq,  D ]  bf16 or fp16 (FA_DTYPE_FP16), contiguous BNSD
+ *   k    [B, Hkv, Skv, D ]  same type
+ *   v    [B, Hkv, Skv, Dv]  same type (NULL with FA_V_FROM_K)
+ *   o    [B, Hq,  Sq,  Dv]  same type, written in full (padding rows too)
+ *   lse  [B, Hq,  Sq]       fp32, natural log over scaled scores,
+ *                           +inf for a row with no valid key or a padding row
+ *   query head h reads KV head h / (Hq / Hkv).
+ *   scale          multiplies Q K^T before the softmax (typically 1/sqrt(D)).
+ *   mask_mode      FA_MASK_* | FA_DTYPE_FP16 | FA_V_FROM_K.
+ *   seqlens        NULL, or device int32[B]: actual length of batch b, applied
+ *                  to queries and keys alike; rows i >= seqlens[b] are padding
+ *                  (O = 0, LSE = +inf) and keys j >= seqlens[b] are masked.
+ *                  Padding rows of k and v must hold finite values.
+ *   kv_block_idx   NULL, or host pointer to a block-sparse descriptor (its
+ *                  idx array is device memory).
+ *   topk_idx       NULL, or host pointer to a top-k descriptor.  At most one
+ *                  of kv_block_idx / topk_idx may be set.
+ *   rescale_threshold  0 = exact running max (O and l are rescaled whenever a
+ *                  row max grows); t > 0 = lazy rescale: the running max is
+ *                  kept until a block's max exceeds it by more than t in
+ *                  log2 units of scaled scores (t = 8 is the usual lazy
+ *                  setting).  Range [0, 15] so that p <= 2^t fits the fp16 P
+ *                  operand.  Every setting targets the same exact result.
+ *   stream         cudaStream_t, as void*.
+ *
+ * Supported (D, Dv): dense / causal / ragged / GQA / block-sparse: D = Dv in
+ * {64, 128}; top-k: D = 576, Dv = 512 with FA_V_FROM_K.
+ * Returns FA_OK or a negative FA_ERR_* code (nothing launched on error).
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int Hq, int Hkv, int Sq, int Skv, int D, int Dv, float scale,
+           int mask_mode, const int32_t* seqlens,
+           const fa_block_sparse_t* kv_block_idx, const fa_topk_t* topk_idx,
+           float rescale_threshold, void* stream);
+
+/* Synchronises `stream`, then returns and clears the device status word of
+ * the current device: FA_OK, FA_ERR_DEVICE_TIMEOUT or FA_ERR_RANGE (the first
+ * error seen since the last call), or FA_ERR_CUDA if the synchronisation
+ * itself failed. */
+int fa_check_status(void* stream);
+
+/* Sets the limit of every bounded on-chip wait (nanoseconds, default 2e9);
+ * values <= 0 restore the default.  Affects launches made after the call. */
+void fa_set_wait_timeout_ns(int64_t ns);
+
+/* Static string for a return code. */
+const char* fa_strerror(int code);
+
+/* The cudaError_t of the last FA_ERR_CUDA (0 if none), and its name. */
+int fa_last_cuda_error(void);
+const char* fa_last_cuda_error_string(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FA_FWD_H_ */

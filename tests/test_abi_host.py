@@ -1,0 +1,77 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds for
+sm_103a, loads, exports every function include/fa_fwd.h declares, and rejects
+bad arguments synchronously with the documented codes."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_forward_fa_gb300 import _binding as B
+from attention_forward_fa_gb300 import build as BUILD
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa_fwd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    BUILD.build()
+    return B.library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fa_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_check_status", "fa_strerror", "fa_set_wait_timeout_ns",
+              "fa_last_cuda_error", "fa_last_cuda_error_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_error_strings(lib):
+    for code in range(-8, 1):
+        assert B.fa_strerror(code)
+    assert "unknown" in B.fa_strerror(-99)
+
+
+P = 0x10000  # a 16-byte aligned stand-in address; validation fails before any use
+
+
+def call(lib, **kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=P, B=1, Hq=2, Hkv=2, Sq=128, Skv=128, D=128, Dv=128,
+             scale=0.1, mask_mode=0, seqlens=None, kv_block_idx=None, topk_idx=None,
+             rescale_threshold=0.0, stream=0)
+    a.update(kw)
+    return B.fa_fwd(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), -1), (dict(k=None), -1), (dict(o=None), -1), (dict(lse=None), -1),
+    (dict(v=None), -1),
+    (dict(B=0), -2), (dict(Hq=3, Hkv=2), -2), (dict(Sq=-1), -2), (dict(D=0), -2),
+    (dict(mask_mode=3), -2), (dict(mask_mode=2), -2), (dict(mask_mode=0x400), -2),
+    (dict(kv_block_idx=(P, 17, 64, 0, 0)), -2), (dict(kv_block_idx=(P, 0, 128, 0, 0)), -2),
+    (dict(kv_block_idx=(P, 513, 128, 0, 0)), -2),
+    (dict(kv_block_idx=(P, 4, 128, 0, 0), topk_idx=(P, 8, 0)), -2),
+    (dict(rescale_threshold=-1.0), -5), (dict(rescale_threshold=16.0), -5),
+    (dict(rescale_threshold=float("nan")), -5), (dict(scale=float("inf")), -2),
+    (dict(D=96, Dv=96), -3), (dict(D=128, Dv=64), -3), (dict(D=256, Dv=256), -3),
+    (dict(q=P + 8), -4), (dict(o=P + 2), -4), (dict(lse=P + 2), -4),
+])
+def test_argument_errors_are_synchronous(lib, kw, code):
+    assert call(lib, **kw) == code
+
+
+def test_timeout_setter(lib):
+    B.fa_set_wait_timeout_ns(5_000_000)
+    B.fa_set_wait_timeout_ns(0)   # back to the default

@@ -1,0 +1,143 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle, element
+by element, on the same seeded inputs (dense, causal, ragged, GQA,
+block-sparse, both rescale thresholds, bf16 and fp16, D = 64 and 128), plus
+sampled rows of the full-size workloads in the launch configuration the
+benchmark times."""
+import numpy as np
+import pytest
+
+from attention_forward_fa_gb300 import workloads as W
+from oracle import attention as A
+
+from tests.parity import compare, run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from attention_forward_fa_gb300 import build
+    build.build()
+
+
+def full_check(p, threshold=0.0):
+    O, L = run_gpu(p, threshold)
+    Or, Lr = A.attention_problem(p)
+    return compare(O, L, Or, Lr, where=p.name)
+
+
+# ------------------------------------------------------------ small, full outputs
+
+def test_config1_dense_tiny():
+    full_check(W.config(1))
+
+
+@pytest.mark.parametrize("threshold", [0.0, 8.0])
+@pytest.mark.parametrize("S", [640, 700, 129])
+def test_causal_mha_ragged_tail(S, threshold):
+    # odd head count -> consecutive query tiles share a CTA; S % 128 != 0 -> ragged tail
+    full_check(W.dense(name=f"causal_S{S}", B=1, Hq=3, Sq=S, D=128, mask=W.MASK_CAUSAL,
+                       seed=11 + S), threshold)
+
+
+def test_noncausal_cross_lengths_fp16():
+    full_check(W.dense(name="cross_fp16", B=2, Hq=2, Sq=200, Skv=333, D=128, dtype="fp16",
+                       mask=W.MASK_NONE, seed=12))
+
+
+def test_causal_cross_lengths():
+    full_check(W.dense(name="causal_cross", B=1, Hq=2, Sq=300, Skv=520, D=128,
+                       mask=W.MASK_CAUSAL, seed=13))
+
+
+@pytest.mark.parametrize("threshold", [0.0, 8.0])
+def test_gqa_ragged_even_group(threshold):
+    # G = 4 -> head pairs share K/V tiles; lengths cover full, ragged, 1 and 0
+    full_check(W.dense(name="gqa_ragged", B=4, Hq=8, Hkv=2, Sq=700, D=128, mask=W.MASK_CAUSAL,
+                       seqlens=[700, 129, 1, 0], seed=14), threshold)
+
+
+def test_gqa_odd_group():
+    full_check(W.dense(name="gqa_odd", B=1, Hq=6, Hkv=2, Sq=384, D=128, mask=W.MASK_CAUSAL,
+                       seed=15))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("mask", [W.MASK_NONE, W.MASK_CAUSAL])
+def test_head_dim_64(dtype, mask):
+    full_check(W.dense(name="d64", B=2, Hq=2, Sq=300, D=64, dtype=dtype, mask=mask, seed=16))
+
+
+def test_single_key_and_single_row():
+    full_check(W.dense(name="one", B=1, Hq=2, Sq=1, Skv=1, D=128, seed=17))
+
+
+@pytest.mark.parametrize("mask", [W.MASK_CAUSAL_DIAG_BLOCK, W.MASK_NONE, W.MASK_CAUSAL])
+@pytest.mark.parametrize("threshold", [0.0, 8.0])
+def test_block_sparse_small(mask, threshold):
+    full_check(W.block_sparse(name="bs_small", B=1, H=4, S=1024, D=128, dtype="fp16",
+                              n_random=3, mask=mask, seed=18), threshold)
+
+
+def test_block_sparse_shared_lists_gqa_bf16_ragged():
+    p = W.block_sparse(name="bs_shared", B=2, H=4, S=640, D=128, dtype="bf16", n_random=2,
+                       seed=19, per_head=False)
+    p.Hkv = 2
+    p.k_bits = np.ascontiguousarray(p.k_bits[:, :2])
+    p.v_bits = np.ascontiguousarray(p.v_bits[:, :2])
+    p.seqlens = np.array([640, 333], dtype=np.int32)
+    full_check(p)
+
+
+def test_block_sparse_invalid_and_duplicate_slots():
+    p = W.block_sparse(name="bs_dup", B=1, H=2, S=512, D=64, dtype="fp16", n_random=1,
+                       pad_slots=2, seed=20)
+    idx = p.kv_block_idx
+    idx[0, 0, 1] = [1, 1, -1, 7]          # duplicate slot counts twice; 7 is out of range
+    idx[0, 1, 2] = [-1, -1, -1, -1]       # nothing valid: O = 0, LSE = +inf
+    idx[0, 1, 3] = [-5, 3, 0, 2]
+    full_check(p)
+
+
+def test_extreme_values_are_finite():
+    """All-equal large scores (q = k = const) must not overflow."""
+    p = W.dense(name="const", B=1, Hq=2, Sq=256, D=128, mask=W.MASK_CAUSAL, seed=21)
+    p.q_bits[:] = W.round_to_bf16_bits(np.full(p.q_bits.shape, 3.0, np.float32))
+    p.k_bits[:] = W.round_to_bf16_bits(np.full(p.k_bits.shape, 3.0, np.float32))
+    full_check(p)
+
+
+def test_repeated_calls_are_deterministic():
+    p = W.dense(name="det", B=1, Hq=4, Sq=512, D=128, mask=W.MASK_CAUSAL, seed=22)
+    d = to_device(p)
+    O1, L1 = run_gpu(p, 0.0, d)
+    O2, L2 = run_gpu(p, 0.0, d)
+    assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
+
+
+# ------------------------------------------------------------ full-size workloads, sampled rows
+
+def sampled_check(p, rows, heads, batches, threshold=0.0):
+    O, L = run_gpu(p, threshold)
+    Or, Lr = A.attention_problem(p, rows=np.asarray(rows), heads=np.asarray(heads),
+                                 batches=np.asarray(batches))
+    return compare(O, L, Or, Lr, where=p.name + " (sampled)")
+
+
+@pytest.mark.parametrize("threshold", [0.0, 8.0])
+def test_config2_full_size_sampled(threshold):
+    p = W.config(2)
+    rows = np.r_[0:3, 127:130, 1000:1003, 2045:2048]
+    sampled_check(p, rows, [0, 7, 15], [0, 1], threshold)
+
+
+def test_config3_full_size_sampled():
+    p = W.config(3)
+    rows = np.r_[0:2, 13:16, 516:519, 3000:3003, 4094:4096]
+    sampled_check(p, rows, [0, 5, 31], [0, 1, 2, 3])
+
+
+def test_config4_full_size_sampled():
+    p = W.config(4)
+    rows = np.r_[0:2, 127:129, 8000:8002, 16382:16384]
+    sampled_check(p, rows, [0, 9, 15], [0])
