@@ -20,6 +20,9 @@ namespace {
 __device__ int g_fa_status;
 
 std::atomic<int> g_last_cuda{0};
+#ifdef FA_TRACE
+unsigned long long* g_trace = nullptr;
+#endif
 std::atomic<long long> g_timeout_ns{2000000000LL};
 
 int cuda_fail(cudaError_t e) {
@@ -73,10 +76,18 @@ int launch_tiled(const fa::TiledParams& prm, int units, cudaStream_t st) {
   int dev = 0;
   cudaGetDevice(&dev);
   cudaError_t attr_err = cudaSuccess;
+  static int regs_ok[64];
   std::call_once(once[dev & 63], [&] {
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // The warpgroups re-split the register file with setmaxnreg; that only
+    // works if every thread was launched with at least the average of the
+    // split (an unmet setmaxnreg.inc would wait forever).
+    cudaFuncAttributes fattr;
+    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fattr, kern);
+    if (attr_err == cudaSuccess) regs_ok[dev & 63] = fattr.numRegs >= fa::kRegsNeeded ? 1 : -1;
   });
   if (attr_err != cudaSuccess) return cuda_fail(attr_err);
+  if (regs_ok[dev & 63] != 1) return cuda_fail(cudaErrorInvalidConfiguration);
   kern<<<units, fa::kTiledThreads, smem, st>>>(prm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
@@ -174,6 +185,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   prm.threshold = rescale_threshold;
   prm.timeout_ns = g_timeout_ns.load();
   prm.status = status;
+#ifdef FA_TRACE
+  prm.trace = g_trace;
+#endif
   const long long units = (long long)prm.units_per_q * prm.n_qpos;
   if (units > 0x7FFFFFFF) return FA_ERR_SHAPE;
 
@@ -220,6 +234,12 @@ const char* fa_strerror(int code) {
 }
 
 int fa_last_cuda_error(void) { return g_last_cuda.load(); }
+
+#ifdef FA_TRACE
+// Profiling builds only: device buffer of kTraceCtas x kTraceCap u64 (zeroed
+// by the caller) that receives the cycle-stamped events of the first CTAs.
+void fa_debug_set_trace(void* buf) { g_trace = static_cast<unsigned long long*>(buf); }
+#endif
 const char* fa_last_cuda_error_string(void) {
   return cudaGetErrorName(static_cast<cudaError_t>(g_last_cuda.load()));
 }

@@ -3,12 +3,16 @@
 //
 // One CTA owns up to two 128-row query tiles ("slots") that are processed in
 // ping-pong so that the softmax of one overlaps the tensor-core work of the
-// other.  Work split inside the CTA (384 threads):
-//   warps 0-3   softmax + epilogue of slot 0 (one thread per query row)
-//   warps 4-7   softmax + epilogue of slot 1
-//   warp  8     TMA producer: Q tiles, then K / V tiles into a ring of stages
-//   warp  9     TMEM allocator and tcgen05.mma issuer
-//   warps 10-11 bf16 -> fp16 conversion of V tiles in shared memory (bf16 I/O)
+// other.  Work split inside the CTA (512 threads, four warpgroups):
+//   warps 0-3   softmax of slot 0 (one thread per query row), including the
+//               correction O *= exp2(m_old - m_new) of its rows when the max moves
+//   warps 4-7   softmax of slot 1
+//   warps 8-11  bf16 -> fp16 conversion of V tiles in shared memory (bf16 I/O)
+//               and the epilogue (O / l, LSE) of both slots
+//   warp  12    TMA producer: Q tiles, then K / V tiles into a ring of stages
+//   warp  13    TMEM allocator and tcgen05.mma issuer
+// The softmax warpgroups raise their register budget with setmaxnreg; the
+// other two lower theirs.
 //
 // TMEM (512 columns): S_t / P_t of slot t at column 128 t, O_t at 256 + 128 t.
 // P is written over S as fp16 (64 columns); rows that see few keys also get a
@@ -28,9 +32,20 @@ namespace fa {
 
 constexpr int kBM = 128;          // query rows per tile
 constexpr int kBN = 128;          // keys per KV tile
-constexpr int kTiledThreads = 384;
+constexpr int kTiledThreads = 512;
+// setmaxnreg budgets per warpgroup (two softmax, correction, producer/MMA/converter);
+// their sum over the four warpgroups must not exceed 4 x the launch budget of
+// 128 registers per thread (the host checks the compiled count before launch)
+constexpr int kSoftmaxRegs = 200;
+constexpr int kCorrRegs = 56;
+constexpr int kOtherRegs = 56;
+constexpr int kRegsNeeded = (2 * kSoftmaxRegs + kCorrRegs + kOtherRegs + 3) / 4;
+static_assert(kSoftmaxRegs % 8 == 0 && kCorrRegs % 8 == 0 && kOtherRegs % 8 == 0,
+              "setmaxnreg takes multiples of 8");
+static_assert(kRegsNeeded <= 65536 / kTiledThreads, "register split exceeds the register file");
 constexpr int kMaxSel = 512;      // longest block list a CTA stages in smem
 constexpr int kHiLoKeys = 256;    // rows with fewer valid keys use the hi+lo P split
+constexpr int kL2Ahead = 8;       // KV tiles prefetched into L2 ahead of the smem ring
 
 enum : int { kStatusTimeout = 1, kStatusRange = 2 };
 
@@ -52,7 +67,39 @@ struct TiledParams {
   float scale, scale_log2, threshold;
   long long timeout_ns;
   int* status;
+  unsigned long long* trace;   // cycle-stamped events of the first CTAs (trace builds only)
 };
+
+// Trace points: compiled only with -DFA_TRACE (a profiling build); otherwise
+// they expand to nothing.  Every tracing thread owns one region of the buffer
+// (no atomics): region = CTA * kTraceRoles + role, slot 0 of a region holds
+// its count.  Each record is clock64 << 24 | tag << 16 | slot << 15 | j.
+constexpr int kTraceCtas = 8;
+constexpr int kTraceRoles = 8;
+constexpr int kTraceCap = 1024;
+#ifdef FA_TRACE
+__device__ __forceinline__ void fa_trace(const TiledParams& p, int role, int& n, int tag, int t,
+                                         int j) {
+  if (p.trace == nullptr || blockIdx.x >= kTraceCtas) return;
+  unsigned long long* buf = p.trace + ((size_t)blockIdx.x * kTraceRoles + role) * kTraceCap;
+  ++n;
+  if (n < kTraceCap)
+    buf[n] = ((unsigned long long)clock64() << 24) | ((unsigned long long)tag << 16) |
+             ((unsigned long long)(t & 1) << 15) | (unsigned long long)(j & 0x7FFF);
+  buf[0] = (unsigned long long)n;
+}
+#define FA_TR_ROLE(r) \
+  int tr_n = 0;       \
+  const int tr_role = (r)
+#define FA_TR(tag, t, j) fa_trace(p, tr_role, tr_n, tag, t, j)
+#else
+#define FA_TR_ROLE(r) ((void)0)
+#define FA_TR(tag, t, j) ((void)0)
+#endif
+// tags: 1 S ready (softmax), 2 P written (softmax), 3 smdone seen (correction),
+// 4 rescale done / p_full arrive (correction), 5 stage filled (producer issue),
+// 6 QK issued, 7 PV issued, 8 V converted, 9 P ready seen (MMA), 10 epilogue start,
+// 11 epilogue end, 12 kernel start, 13 kernel end, 14 stage ready (MMA)
 
 // Shared-memory plan (offsets from a 1024-byte aligned base).
 template <int D, int NS>
@@ -62,10 +109,11 @@ struct TiledSmem {
   static constexpr int kQOff = 0;
   static constexpr int kStageOff = 2 * kQBytes;
   static constexpr int kListOff = kStageOff + NS * kStageBytes;
-  static constexpr int kBarOff = kListOff + 2 * kMaxSel * 4;
+  static constexpr int kRowOff = kListOff + 2 * kMaxSel * 4;   // alpha[2][128], m[2][128], l[2][128]
+  static constexpr int kBarOff = kRowOff + 3 * 2 * kBM * 4;
   // barriers: q_full[2], full[NS], empty[NS], vready[NS], s_full[2], p_full[2],
-  // o_ready[2], drain
-  static constexpr int kNumBars = 2 + 3 * NS + 6 + 1;
+  // o_ready[2], drain, sm_done[2]
+  static constexpr int kNumBars = 2 + 3 * NS + 6 + 1 + 2;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;   // tmem base, abort flag, slot info
   static constexpr int kBytes = kMiscOff + 64;
   static constexpr int kAlloc = kBytes + 1024;              // slack for 1024-byte alignment
@@ -79,12 +127,13 @@ struct WaitCtx {
 
 // Bounded wait on an mbarrier phase.  Returns false (and stops every other
 // wait of the CTA) once the limit passes or another thread gave up.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtx& c) {
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, WaitCtx c) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
+    // suspended in hardware until the phase completes (or ~20 us pass)
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*c.abort) return false;
-    if (mbar_try_wait(bar, parity)) return true;
     if ((long long)(globaltimer_ns() - t0) > c.timeout) {
       *c.abort = 1;
       atomicOr(c.status, kStatusTimeout);
@@ -100,28 +149,37 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, long lo
   }
 }
 
-// The order in which the MMA warp consumes K / V tiles.  f(is_pv, slot, j,
-// load, release) is called per MMA group; `load` marks the first use of a
-// tile (a new ring stage), `release` the last.  With `shared`, slot 1 reads the
-// tiles slot 0 loaded (same KV head and KV tile sequence, n0 <= n1).
-template <class F>
-__device__ __forceinline__ void for_each_event(int n0, int n1, bool shared, F&& f) {
-  auto ev = [&](bool pv, int t, int j) -> bool {
-    const int nt = t ? n1 : n0;
-    if (j >= nt) return true;
-    const bool load = shared ? (t == 0 || j >= n0) : true;
-    const bool rel = shared ? (t == 1) : true;
-    return f(pv, t, j, load, rel);
-  };
-  if (!ev(false, 0, 0)) return;
-  if (!ev(false, 1, 0)) return;
+// The order in which the MMA warp consumes K / V tiles, as a numbered event
+// list: 0 = QK(0,0), 1 = QK(1,0), then per iteration j four events PV(0,j),
+// QK(0,j+1), PV(1,j), QK(1,j+1).  `load` marks the first use of a tile (a
+// new ring stage), `rel` the last.  With `shared`, slot 1 reads the tiles slot
+// 0 loaded (same KV head and KV tile sequence, n0 <= n1).
+struct Event {
+  bool valid, pv, load, rel;
+  int t, j;
+};
+__device__ __forceinline__ int num_events(int n0, int n1) {
   const int n = n0 > n1 ? n0 : n1;
-  for (int j = 0; j < n; ++j) {
-    if (!ev(true, 0, j)) return;
-    if (!ev(false, 0, j + 1)) return;
-    if (!ev(true, 1, j)) return;
-    if (!ev(false, 1, j + 1)) return;
+  return n > 0 ? 2 + 4 * n : 0;
+}
+__device__ __forceinline__ Event event_at(int e, int n0, int n1, bool shared) {
+  Event ev;
+  if (e < 2) {
+    ev.pv = false;
+    ev.t = e;
+    ev.j = 0;
+  } else {
+    const int r = (e - 2) & 3;
+    const int j = (e - 2) >> 2;
+    ev.pv = (r & 1) == 0;
+    ev.t = r >> 1;
+    ev.j = ev.pv ? j : j + 1;
   }
+  const int nt = ev.t ? n1 : n0;
+  ev.valid = ev.j < nt;
+  ev.load = shared ? (ev.t == 0 || ev.j >= n0) : true;
+  ev.rel = shared ? (ev.t == 1) : true;
+  return ev;
 }
 
 template <int D, bool kBF16, int NS>
@@ -141,15 +199,19 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   const uint32_t sQ = sbase + SM::kQOff;
   const uint32_t sStage = sbase + SM::kStageOff;
   int* s_list = reinterpret_cast<int*>(smem + SM::kListOff);
+  float* s_alpha = reinterpret_cast<float*>(smem + SM::kRowOff);   // [2][128]
+  float* s_m = s_alpha + 2 * kBM;                                    // [2][128]
+  float* s_l = s_m + 2 * kBM;                                        // [2][128]
   const uint32_t bar0 = sbase + SM::kBarOff;
-  auto BAR_QFULL = [&](int t) { return bar0 + 8u * t; };
-  auto BAR_FULL = [&](int s) { return bar0 + 8u * (2 + s); };
-  auto BAR_EMPTY = [&](int s) { return bar0 + 8u * (2 + NS + s); };
-  auto BAR_VREADY = [&](int s) { return bar0 + 8u * (2 + 2 * NS + s); };
-  auto BAR_SFULL = [&](int t) { return bar0 + 8u * (2 + 3 * NS + t); };
-  auto BAR_PFULL = [&](int t) { return bar0 + 8u * (4 + 3 * NS + t); };
-  auto BAR_OREADY = [&](int t) { return bar0 + 8u * (6 + 3 * NS + t); };
+  auto BAR_QFULL = [=](int t) { return bar0 + 8u * t; };
+  auto BAR_FULL = [=](int s) { return bar0 + 8u * (2 + s); };
+  auto BAR_EMPTY = [=](int s) { return bar0 + 8u * (2 + NS + s); };
+  auto BAR_VREADY = [=](int s) { return bar0 + 8u * (2 + 2 * NS + s); };
+  auto BAR_SFULL = [=](int t) { return bar0 + 8u * (2 + 3 * NS + t); };
+  auto BAR_PFULL = [=](int t) { return bar0 + 8u * (4 + 3 * NS + t); };
+  auto BAR_OREADY = [=](int t) { return bar0 + 8u * (6 + 3 * NS + t); };
   const uint32_t BAR_DRAIN = bar0 + 8u * (8 + 3 * NS);
+  auto BAR_SMDONE = [=](int t) { return bar0 + 8u * (9 + 3 * NS + t); };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + SM::kMiscOff);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + SM::kMiscOff + 4);
   int* s_slot = reinterpret_cast<int*>(smem + SM::kMiscOff + 8);   // [2] n, [2] hilo
@@ -162,43 +224,48 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   const int u = blockIdx.x;
   const int qpos = p.n_qpos - 1 - u / p.units_per_q;   // heaviest query positions first
   const int bh = u % p.units_per_q;
-  int b, h_s[2], qt_s[2];
+  int b, h0, h1, qt0, qt1;
   if (p.pair_mode == 0) {
     b = bh / p.Hq;
-    h_s[0] = h_s[1] = bh % p.Hq;
-    qt_s[0] = 2 * qpos;
-    qt_s[1] = 2 * qpos + 1;
+    h0 = h1 = bh % p.Hq;
+    qt0 = 2 * qpos;
+    qt1 = 2 * qpos + 1;
   } else {
     const int hpairs = p.Hq / 2;
     b = bh / hpairs;
-    h_s[0] = 2 * (bh % hpairs);
-    h_s[1] = h_s[0] + 1;
-    qt_s[0] = qt_s[1] = qpos;
+    h0 = 2 * (bh % hpairs);
+    h1 = h0 + 1;
+    qt0 = qt1 = qpos;
   }
-  const int kvh = h_s[0] / p.G;   // both slots share it (GQA pairs never straddle a group)
+  const int kvh = h0 / p.G;   // both slots share it (GQA pairs never straddle a group)
   const int q_len = p.seqlens ? min(p.seqlens[b], p.Sq) : p.Sq;
   const int kv_len = p.seqlens ? min(p.seqlens[b], p.Skv) : p.Skv;
   const int nkb = (p.Skv + kBN - 1) / kBN;
   const bool sparse = p.blk_idx != nullptr;
 
   // ---------------------------------------------------------------- setup
+  {
+    FA_TR_ROLE(6);
+    if (tid == 0) FA_TR(12, 0, 0);
+  }
   if (tid == 0) {
     for (int t = 0; t < 2; ++t) {
       mbar_init(BAR_QFULL(t), 1);
       mbar_init(BAR_SFULL(t), 1);
-      mbar_init(BAR_PFULL(t), kBM);      // every softmax thread of the slot arrives
+      mbar_init(BAR_SMDONE(t), kBM);     // softmax threads, once, after their last tile
+      mbar_init(BAR_PFULL(t), kBM);      // softmax threads, per tile
       mbar_init(BAR_OREADY(t), 1);
     }
     for (int s = 0; s < NS; ++s) {
       mbar_init(BAR_FULL(s), 1);
       mbar_init(BAR_EMPTY(s), 1);
-      mbar_init(BAR_VREADY(s), 64);     // every converter thread arrives
+      mbar_init(BAR_VREADY(s), kBM);    // every correction thread arrives
     }
     mbar_init(BAR_DRAIN, 1);
     *s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(smem_u32(s_tmem), 512);
     tmem_relinquish();
   }
@@ -207,7 +274,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   // slots of its query block (order kept) into s_list[t].
   if (warp < 2) {
     const int t = warp;
-    const int qt = qt_s[t];
+    const int qt = t ? qt1 : qt0;
     const int q0 = qt * kBM;
     int n = 0, hilo = 0;
     const bool live = qt < p.n_qt && q0 < q_len && kv_len > 0;
@@ -222,7 +289,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       hilo = min_keys < kHiLoKeys;
     } else if (live && sparse) {
       const int* lst = p.blk_idx + (long long)b * p.blk_stride_b +
-                       (long long)h_s[t] * p.blk_stride_h + (long long)qt * p.max_sel;
+                       (long long)(t ? h1 : h0) * p.blk_stride_h + (long long)qt * p.max_sel;
       int keys_lb = 0;
       for (int base = 0; base < p.max_sel; base += 32) {
         const int s = base + lane;
@@ -256,187 +323,54 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   const int n0 = s_slot[0], n1 = s_slot[1];
   const bool shared_kv = !sparse ? (n0 >= 1 && n0 <= n1) : false;
   const WaitCtx wc{s_abort, p.status, p.timeout_ns};
-  auto kv_tile = [&](int t, int j) -> int { return sparse ? s_list[t * kMaxSel + j] : j; };
+  auto kv_tile = [=](int t, int j) -> int { return sparse ? s_list[t * kMaxSel + j] : j; };
 
-  if (warp == 8) {
-    // ============================================================ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&p.tm_q);
-      tma_prefetch_desc(&p.tm_k);
-      tma_prefetch_desc(&p.tm_v);
-      for (int t = 0; t < 2; ++t) {
-        if ((t ? n1 : n0) == 0) continue;
-        mbar_arrive_expect_tx(BAR_QFULL(t), SM::kQBytes);
-        for (int bx = 0; bx < kBoxes; ++bx)
-          tma_load_3d(sQ + t * SM::kQBytes + bx * (kBM * 128), &p.tm_q, BAR_QFULL(t), 64 * bx,
-                      qt_s[t] * kBM, b * p.Hq + h_s[t]);
-      }
-      int ld = 0;
-      for_each_event(n0, n1, shared_kv, [&](bool pv, int t, int j, bool load, bool) -> bool {
-        if (!load) return true;
-        const int s = ld % NS;
-        const uint32_t f = ld / NS;
-        ++ld;
-        if (!wait_bar(BAR_EMPTY(s), (f & 1) ^ 1, wc)) return false;
-        const int kvt = kv_tile(t, j);
-        mbar_arrive_expect_tx(BAR_FULL(s), SM::kStageBytes);
-        const CUtensorMap* tm = pv ? &p.tm_v : &p.tm_k;
-        for (int bx = 0; bx < kBoxes; ++bx)
-          tma_load_3d(sStage + s * SM::kStageBytes + bx * (kBN * 128), tm, BAR_FULL(s), 64 * bx,
-                      kvt * kBN, b * p.Hkv + kvh);
-        return true;
-      });
-      if (*s_abort) {
-        // let every copy in flight land before the CTA's shared memory goes away
-        for (int i = (ld > NS ? ld - NS : 0); i < ld; ++i)
-          drain_bar(BAR_FULL(i % NS), (i / NS) & 1, wc.timeout);
-        for (int t = 0; t < 2; ++t)
-          if ((t ? n1 : n0) > 0) drain_bar(BAR_QFULL(t), 0, wc.timeout);
-      }
-    }
-  } else if (warp == 9) {
-    // ============================================================ MMA issuer
-    if (lane == 0) {
-      int ld = 0, vc = 0;
-      uint32_t stK = 0, stV = 0;
-      const int hilo0 = s_slot[2], hilo1 = s_slot[3];
-      for_each_event(n0, n1, shared_kv, [&](bool pv, int t, int j, bool load, bool rel) -> bool {
-        uint32_t s;
-        if (load) {
-          s = ld % NS;
-          const uint32_t f = ld / NS;
-          ++ld;
-          if (pv && kBF16) {
-            if (!wait_bar(BAR_VREADY(vc % NS), (vc / NS) & 1, wc)) return false;
-            ++vc;
-          } else {
-            if (!wait_bar(BAR_FULL(s), f & 1, wc)) return false;
-          }
-          if (pv) stV = s; else stK = s;
-        } else {
-          s = pv ? stV : stK;
-        }
-        const uint32_t tS = tmem + 128u * t;
-        const uint32_t tO = tmem + 256u + 128u * t;
-        if (!pv) {
-          if (j == 0 && !wait_bar(BAR_QFULL(t), 0, wc)) return false;
-          tc_fence_after();
-          const uint32_t qa = sQ + t * SM::kQBytes;
-          const uint32_t ka = sStage + s * SM::kStageBytes;
-#pragma unroll
-          for (int kk = 0; kk < kKSteps; ++kk) {
-            const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-            mma_ss(tS, sw128_desc(qa + off, 16, 1024), sw128_desc(ka + off, 16, 1024), kIdescQK,
-                   kk > 0);
-          }
-          mma_commit(BAR_SFULL(t));
-        } else {
-          if (!wait_bar(BAR_PFULL(t), j & 1, wc)) return false;
-          tc_fence_after();
-          const uint32_t va = sStage + s * SM::kStageBytes;
-#pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            mma_ts(tO, tS + 8 * kk, sw128_desc(va + kk * 2048, kBN * 128, 1024), kIdescPV,
-                   (j > 0 || kk > 0) ? 1u : 0u);
-          if (t ? hilo1 : hilo0) {
-#pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
-              mma_ts(tO, tS + 64 + 8 * kk, sw128_desc(va + kk * 2048, kBN * 128, 1024), kIdescPV,
-                     1u);
-          }
-          mma_commit(BAR_OREADY(t));
-        }
-        if (rel) mma_commit(BAR_EMPTY(s));
-        return true;
-      });
-      // every MMA has finished before TMEM is released
-      if (n0 + n1 > 0) {
-        mma_commit(BAR_DRAIN);
-        drain_bar(BAR_DRAIN, 0, wc.timeout);
-      }
-    }
-    __syncwarp();
-  } else if (warp >= 10) {
-    // ============================================================ V converter
-    if (kBF16) {
-      const int ct = tid - 320;   // 0..63
-      int ld = 0, vc = 0;
-      float amax = 0.f;
-      for_each_event(n0, n1, shared_kv, [&](bool pv, int, int, bool load, bool) -> bool {
-        if (!load) return true;
-        const int s = ld % NS;
-        const uint32_t f = ld / NS;
-        ++ld;
-        if (!pv) return true;
-        if (!wait_bar(BAR_FULL(s), f & 1, wc)) return false;
-        uint4* base = reinterpret_cast<uint4*>(smem + SM::kStageOff + s * SM::kStageBytes);
-#pragma unroll 4
-        for (int i = ct; i < SM::kStageBytes / 16; i += 64) {
-          uint4 w = base[i];
-          uint32_t* ww = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float lo = __uint_as_float(ww[e] << 16);
-            const float hi = __uint_as_float(ww[e] & 0xFFFF0000u);
-            amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
-            ww[e] = pack_f16x2(lo, hi);
-          }
-          base[i] = w;
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(BAR_VREADY(vc % NS));
-        ++vc;
-        return true;
-      });
-      if (amax > 65504.f) atomicOr(p.status, kStatusRange);
-    }
-  } else {
-    // ============================================================ softmax + epilogue
+  if (warp < 8) {
+    // ============================================================ softmax
+    regs_inc<kSoftmaxRegs>();
+    FA_TR_ROLE(warp >> 2);
     const int t = warp >> 2;
     const int nt = t ? n1 : n0;
     const int hilo = s_slot[2 + t];
-    const int qt = qt_s[t];
-    const int h = h_s[t];
+    const int qt = t ? qt1 : qt0;
     const int row = (warp & 3) * 32 + lane;
     const int q0 = qt * kBM;
     const int qi = q0 + row;
     const bool row_valid = qi < q_len;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + 128u * t + lane_off;
-    const uint32_t tO = tmem + 256u + 128u * t + lane_off;
     const float c = p.scale_log2;
     float m = -INFINITY, l = 0.f;
-    bool ok = true;   // warp-uniform
     for (int j = 0; j < nt; ++j) {
-      ok = __all_sync(0xffffffffu, wait_bar(BAR_SFULL(t), j & 1, wc));
-      if (!ok) break;
+      if (!__all_sync(0xffffffffu, wait_bar(BAR_SFULL(t), j & 1, wc))) break;
+      if (row == 0) FA_TR(1, t, j);
       tc_fence_after();
-      uint32_t su[kBN];
-#pragma unroll
-      for (int cc = 0; cc < kBN / 32; ++cc)
-        tmem_ld32(tS + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(&su[32 * cc]));
-      tmem_wait_ld();
-      float s[kBN];
-#pragma unroll
-      for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(su[i]);
       const int kvt = kv_tile(t, j);
       const int kbase = kvt * kBN;
       const bool causal_here = (p.mask == 1) || (p.mask == 2 && kvt == qt);
       const bool need_mask =
           !row_valid || kbase + kBN > kv_len || (causal_here && kbase + kBN - 1 > q0);
+      // keys at column >= lim are masked (only consulted when need_mask)
+      const int lim = !row_valid ? 0 : min(kv_len - kbase, causal_here ? qi - kbase + 1 : kBN);
+      // the whole S row of this thread in registers (4 loads in flight)
+      uint32_t su[kBN];
+#pragma unroll
+      for (int cc = 0; cc < kBN / 32; ++cc)
+        tmem_ld32(tS + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(&su[32 * cc]));
+      tmem_wait_ld();
+      float sv[kBN];
+#pragma unroll
+      for (int i = 0; i < kBN; ++i) sv[i] = __uint_as_float(su[i]);
       if (need_mask) {
-        const int lim_kv = kv_len - kbase;                        // keys >= lim_kv masked
-        const int lim_c = causal_here ? qi - kbase + 1 : kBN;     // keys >= lim_c masked
-        const int lim = row_valid ? min(lim_kv, lim_c) : 0;
 #pragma unroll
         for (int i = 0; i < kBN; ++i)
-          if (i >= lim) s[i] = -INFINITY;
+          if (i >= lim) sv[i] = -INFINITY;
       }
       float mx[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+      for (int i = 0; i < 8; ++i) mx[i] = sv[i];
 #pragma unroll
-      for (int i = 8; i < kBN; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+      for (int i = 8; i < kBN; ++i) mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
       const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float m_new = fmaxf(m, mb);
@@ -450,68 +384,130 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         }
       }
       const float neg = (m_use == -INFINITY) ? 0.f : -m_use * c;
-      float sm[8];
+      // p = exp2(s c - m c); P (fp16) written over S (all of S is already in
+      // registers), with the hi+lo split (second fp16 term p - fp16(p) in
+      // columns 64..127) for rows that see few keys
+      float sm[4] = {0.f, 0.f, 0.f, 0.f};
+      if (!hilo) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sm[i] = 0.f;
+        for (int cc = 0; cc < kBN / 32; ++cc) {
+          uint32_t ph[16];
 #pragma unroll
-      for (int i = 0; i < kBN; ++i) {
-        s[i] = ex2_approx(fmaf(s[i], c, neg));
-        sm[i & 7] += s[i];
+          for (int i = 0; i < 16; ++i) {
+            const float a0 = ex2_approx(fmaf(sv[32 * cc + 2 * i], c, neg));
+            const float a1 = ex2_approx(fmaf(sv[32 * cc + 2 * i + 1], c, neg));
+            sm[i & 3] += a0 + a1;
+            ph[i] = pack_f16x2(a0, a1);
+          }
+          tmem_st16(tS + 16 * cc, ph);
+        }
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < kBN / 32; ++cc) {
+          uint32_t ph[16], pl[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float a0 = ex2_approx(fmaf(sv[32 * cc + 2 * i], c, neg));
+            const float a1 = ex2_approx(fmaf(sv[32 * cc + 2 * i + 1], c, neg));
+            sm[i & 3] += a0 + a1;
+            ph[i] = pack_f16x2(a0, a1);
+            pl[i] = pack_f16x2(a0 - f16_lo_to_f32(ph[i]), a1 - f16_hi_to_f32(ph[i]));
+          }
+          tmem_st16(tS + 16 * cc, ph);
+          tmem_st16(tS + 64 + 16 * cc, pl);
+        }
       }
-      const float rs = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+      const float rs = (sm[0] + sm[1]) + (sm[2] + sm[3]);
       l = alpha * l + rs;
       m = m_use;
-      // rescale O_t; the previous P.V product into O_t must have landed first
+      // O_t *= alpha for the rows whose max moved.  The previous P.V product
+      // into O_t has landed (Q.K^T of this tile was issued after it and the
+      // tensor pipe completes in order); the wait only confirms it.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        ok = __all_sync(0xffffffffu, wait_bar(BAR_OREADY(t), (j - 1) & 1, wc));
-        if (!ok) break;
+        if (!__all_sync(0xffffffffu, wait_bar(BAR_OREADY(t), (j - 1) & 1, wc))) break;
         tc_fence_after();
+        const uint32_t tO = tmem + 256u + 128u * t + lane_off;
 #pragma unroll
-        for (int cc = 0; cc < Dv / 32; ++cc) {
-          uint32_t r[32];
-          tmem_ld32(tO + 32 * cc, r);
+        for (int cc = 0; cc < Dv / 16; ++cc) {
+          uint32_t r[16];
+          tmem_ld16(tO + 16 * cc, r);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          tmem_st32(tO + 32 * cc, r);
-        }
-      }
-      // P (fp16) over S; hi+lo split for rows that see few keys
-      {
-        uint32_t r[32];
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = pack_f16x2(s[64 * cc + 2 * i], s[64 * cc + 2 * i + 1]);
-          tmem_st32(tS + 32 * cc, r);
-        }
-        if (hilo) {
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float a0 = s[64 * cc + 2 * i], a1 = s[64 * cc + 2 * i + 1];
-              const uint32_t hi2 = pack_f16x2(a0, a1);
-              r[i] = pack_f16x2(a0 - f16_lo_to_f32(hi2), a1 - f16_hi_to_f32(hi2));
-            }
-            tmem_st32(tS + 64 + 32 * cc, r);
-          }
+          for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tmem_st16(tO + 16 * cc, r);
         }
       }
       tmem_wait_st();
       tc_fence_before();
+      if (row == 0) FA_TR(2, t, j);
       mbar_arrive(BAR_PFULL(t));
     }
-    // ---------------------------------------------------------- epilogue
-    if (qt < p.n_qt && ok) {
+    // final row statistics for the epilogue warpgroup
+    s_m[t * kBM + row] = m;
+    s_l[t * kBM + row] = l;
+    mbar_arrive(BAR_SMDONE(t));
+  } else if (warp < 12) {
+    // ============================================================ correction + epilogue
+    regs_dec<kCorrRegs>();
+    FA_TR_ROLE(2);
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    bool ok = true;   // warp-uniform
+    int ld = 0, vc = 0;
+    uint32_t vmax = 0;   // largest |bf16 V| bit pattern seen (per 16-bit half)
+    const int ne = num_events(n0, n1);
+    for (int e = 0; e < ne && kBF16; ++e) {
+      const Event ev = event_at(e, n0, n1, shared_kv);
+      if (!ev.valid || !ev.load) continue;
+      const int s = ld % NS;
+      const uint32_t f = ld / NS;
+      ++ld;
+      if (!ev.pv) continue;
+      // bf16 -> fp16 in place as soon as the tile lands, so that P (fp16) and
+      // V share a type
+      ok = __all_sync(0xffffffffu, wait_bar(BAR_FULL(s), f & 1, wc));
+      if (!ok) break;
+      uint4* base = reinterpret_cast<uint4*>(smem + SM::kStageOff + s * SM::kStageBytes);
+#pragma unroll 4
+      for (int i = row; i < SM::kStageBytes / 16; i += kBM) {
+        uint4 w = base[i];
+        uint32_t* ww = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          vmax = max_u16x2(vmax, ww[q] & 0x7FFF7FFFu);
+          ww[q] = pack_f16x2(__uint_as_float(ww[q] << 16), __uint_as_float(ww[q] & 0xFFFF0000u));
+        }
+        base[i] = w;
+      }
+      fence_proxy_async_smem();
+      if (row == 0) FA_TR(8, ev.t, ev.j);
+      mbar_arrive(BAR_VREADY(vc % NS));
+      ++vc;
+    }
+    if (kBF16 && ((vmax & 0xFFFFu) > 0x477Fu || (vmax >> 16) > 0x477Fu))
+      atomicOr(p.status, kStatusRange);   // |v| >= 65536 became inf in fp16
+    // epilogue: O / l and LSE of both slots
+#pragma unroll 1
+    for (int t = 0; t < 2 && ok; ++t) {
+      const int qt = t ? qt1 : qt0;
+      if (qt >= p.n_qt) continue;
+      const int nt = t ? n1 : n0;
+      const int h = t ? h1 : h0;
+      const int qi = qt * kBM + row;
       bool acc = false;
       if (nt > 0) {
-        acc = __all_sync(0xffffffffu, wait_bar(BAR_OREADY(t), (nt - 1) & 1, wc));
+        acc = __all_sync(0xffffffffu, wait_bar(BAR_SMDONE(t), 0, wc)) &&
+              __all_sync(0xffffffffu, wait_bar(BAR_OREADY(t), (nt - 1) & 1, wc));
+        if (!acc) break;
         tc_fence_after();
       }
-      const bool write = qi < p.Sq && (nt == 0 || acc);
+      if (row == 0) FA_TR(10, t, 0);
+      const float l = acc ? s_l[t * kBM + row] : 0.f;
+      const float m = acc ? s_m[t * kBM + row] : 0.f;
+      const bool write = qi < p.Sq;
       uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + ((size_t)(b * p.Hq + h) * p.Sq + qi) * Dv;
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      const uint32_t tO = tmem + 256u + 128u * t + lane_off;
 #pragma unroll
       for (int cc = 0; cc < Dv / 32; ++cc) {
         uint32_t r[32];
@@ -522,31 +518,181 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[i] = 0;
         }
-        uint32_t w[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float a0 = __uint_as_float(r[2 * i]) * inv_l;
-          const float a1 = __uint_as_float(r[2 * i + 1]) * inv_l;
-          w[i] = kBF16 ? pack_bf16x2(a0, a1) : pack_f16x2(a0, a1);
-        }
         if (write) {
           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cc);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          for (int i = 0; i < 4; ++i) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float a0 = __uint_as_float(r[8 * i + 2 * e]) * inv_l;
+              const float a1 = __uint_as_float(r[8 * i + 2 * e + 1]) * inv_l;
+              w[e] = kBF16 ? pack_bf16x2(a0, a1) : pack_f16x2(a0, a1);
+            }
+            dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
         }
       }
       if (write)
         p.lse[(size_t)(b * p.Hq + h) * p.Sq + qi] = (l > 0.f) ? m * p.scale + __logf(l) : INFINITY;
+      if (row == 0) FA_TR(11, t, 0);
     }
+  } else if (warp == 12) {
+    // ============================================================ producer
+    regs_dec<kOtherRegs>();
+    FA_TR_ROLE(3);
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      for (int t = 0; t < 2; ++t) {
+        if ((t ? n1 : n0) == 0) continue;
+        mbar_arrive_expect_tx(BAR_QFULL(t), SM::kQBytes);
+        for (int bx = 0; bx < kBoxes; ++bx)
+          tma_load_3d(sQ + t * SM::kQBytes + bx * (kBM * 128), &p.tm_q, BAR_QFULL(t), 64 * bx,
+                      (t ? qt1 : qt0) * kBM, b * p.Hq + (t ? h1 : h0));
+      }
+      // L2 prefetch of K and V tiles kL2Ahead iterations ahead of their use, so
+      // that the ring's TMA loads hit L2 instead of waiting on HBM
+      int pf0 = 0, pf1 = 0;
+      const CUtensorMap* tmk = &p.tm_k;
+      const CUtensorMap* tmv = &p.tm_v;
+      const int plane = b * p.Hkv + kvh;
+      auto prefetch_kv = [=](int t, int jj) {
+        const int kvt = sparse ? s_list[t * kMaxSel + jj] : jj;
+        for (int bx = 0; bx < kBoxes; ++bx) {
+          tma_prefetch_l2_3d(tmk, 64 * bx, kvt * kBN, plane);
+          tma_prefetch_l2_3d(tmv, 64 * bx, kvt * kBN, plane);
+        }
+      };
+      int ld = 0;
+      const int ne = num_events(n0, n1);
+      for (int e = 0; e < ne; ++e) {
+        const Event ev = event_at(e, n0, n1, shared_kv);
+        if (!ev.valid || !ev.load) continue;
+        if (ev.t == 0 || shared_kv) {
+          const int lim = min(ev.j + kL2Ahead, shared_kv ? n1 : n0);
+          for (; pf0 < lim; ++pf0) prefetch_kv(shared_kv ? 1 : 0, pf0);
+        } else {
+          const int lim = min(ev.j + kL2Ahead, n1);
+          for (; pf1 < lim; ++pf1) prefetch_kv(1, pf1);
+        }
+        const int s = ld % NS;
+        const uint32_t f = ld / NS;
+        ++ld;
+        if (!wait_bar(BAR_EMPTY(s), (f & 1) ^ 1, wc)) break;
+        const int kvt = kv_tile(ev.t, ev.j);
+        FA_TR(5, ev.t, ev.j);
+        mbar_arrive_expect_tx(BAR_FULL(s), SM::kStageBytes);
+        const CUtensorMap* tm = ev.pv ? &p.tm_v : &p.tm_k;
+        for (int bx = 0; bx < kBoxes; ++bx)
+          tma_load_3d(sStage + s * SM::kStageBytes + bx * (kBN * 128), tm, BAR_FULL(s), 64 * bx,
+                      kvt * kBN, b * p.Hkv + kvh);
+      }
+      if (*s_abort) {
+        // let every copy in flight land before the CTA's shared memory goes away
+        for (int i = (ld > NS ? ld - NS : 0); i < ld; ++i)
+          drain_bar(BAR_FULL(i % NS), (i / NS) & 1, wc.timeout);
+        for (int t = 0; t < 2; ++t)
+          if ((t ? n1 : n0) > 0) drain_bar(BAR_QFULL(t), 0, wc.timeout);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 13) {
+    // ============================================================ MMA issuer
+    regs_dec<kOtherRegs>();
+    FA_TR_ROLE(4);
+    if (lane == 0) {
+      int ld = 0, vc = 0;
+      uint32_t stK = 0, stV = 0;
+      const int hilo0 = s_slot[2], hilo1 = s_slot[3];
+      const uint64_t q_desc0 = sw128_desc(sQ, 16, 1024);               // K-major Q
+      const uint64_t k_desc0 = sw128_desc(sStage, 16, 1024);           // K-major K
+      const uint64_t v_desc0 = sw128_desc(sStage, kBN * 128, 1024);    // MN-major V
+      const int ne = num_events(n0, n1);
+      for (int e = 0; e < ne; ++e) {
+        const Event ev = event_at(e, n0, n1, shared_kv);
+        if (!ev.valid) continue;
+        const int t = ev.t, j = ev.j;
+        uint32_t s;
+        if (ev.load) {
+          s = ld % NS;
+          const uint32_t f = ld / NS;
+          ++ld;
+          if (ev.pv && kBF16) {
+            if (!wait_bar(BAR_VREADY(vc % NS), (vc / NS) & 1, wc)) break;
+            ++vc;
+          } else {
+            if (!wait_bar(BAR_FULL(s), f & 1, wc)) break;
+          }
+          FA_TR(14, t, j);
+          if (ev.pv) stV = s; else stK = s;
+        } else {
+          s = ev.pv ? stV : stK;
+        }
+        const uint32_t tS = tmem + 128u * t;
+        const uint32_t tO = tmem + 256u + 128u * t;
+        // descriptors: the start-address field is the low 14 bits (address >> 4)
+        // and never carries, so offsets are added to a base descriptor
+        const uint32_t stage16 = (s * SM::kStageBytes) >> 4;
+        if (!ev.pv) {
+          // S_t is free: the softmax read it before arriving on PFULL, which
+          // this thread waited on (with a fence) before the previous P.V
+          if (j == 0 && !wait_bar(BAR_QFULL(t), 0, wc)) break;
+          const uint64_t qd = q_desc0 + ((t * SM::kQBytes) >> 4);
+          const uint64_t kd = k_desc0 + stage16;
+#pragma unroll
+          for (int kk = 0; kk < kKSteps; ++kk) {
+            const uint32_t off16 = ((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4;
+            mma_ss(tS, qd + off16, kd + off16, kIdescQK, kk > 0);
+          }
+          mma_commit(BAR_SFULL(t));
+          FA_TR(6, t, j);
+        } else {
+          FA_TR(20, t, j);
+          if (!wait_bar(BAR_PFULL(t), j & 1, wc)) break;
+          FA_TR(9, t, j);
+          tc_fence_after();
+          FA_TR(21, t, j);
+          const uint64_t vd = v_desc0 + stage16;
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            mma_ts(tO, tS + 8 * kk, vd + (kk * 2048 >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+            if (kk == 0) FA_TR(22, t, j);
+          }
+          FA_TR(23, t, j);
+          if (t ? hilo1 : hilo0) {
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              mma_ts(tO, tS + 64 + 8 * kk, vd + (kk * 2048 >> 4), kIdescPV, 1u);
+          }
+          mma_commit(BAR_OREADY(t));
+          FA_TR(7, t, j);
+        }
+        if (ev.rel) mma_commit(BAR_EMPTY(s));
+      }
+      // every MMA has finished before TMEM is released
+      if (n0 + n1 > 0) {
+        mma_commit(BAR_DRAIN);
+        drain_bar(BAR_DRAIN, 0, wc.timeout);
+      }
+    }
+    __syncwarp();
+  } else {
+    // warps 14-15: no role (they complete the fourth warpgroup)
+    regs_dec<kOtherRegs>();
   }
 
   // ---------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  }
+  {
+    FA_TR_ROLE(7);
+    if (tid == 0) FA_TR(13, 0, 0);
   }
 }
 
