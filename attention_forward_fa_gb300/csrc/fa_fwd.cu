@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/fa_fwd.h"
@@ -66,6 +67,54 @@ int* status_ptr() {
   void* ptr = nullptr;
   if (cudaGetSymbolAddress(&ptr, g_fa_status) != cudaSuccess) return nullptr;
   return static_cast<int*>(ptr);
+}
+
+// bf16 -> fp16 copy of V (the P.V product runs on fp16 operands; fp16 keeps
+// three more mantissa bits of P than bf16).  bf16 -> fp16 is exact for
+// 2^-14 <= |v| <= 65504; larger magnitudes become inf and set status bit 1.
+__global__ void fa_convert_v_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
+                                    size_t n16, int* status) {
+  uint32_t vmax = 0;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16;
+       i += (size_t)gridDim.x * blockDim.x) {
+    uint4 w = in[i];
+    uint32_t* ww = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      vmax = fa::max_u16x2(vmax, ww[q] & 0x7FFF7FFFu);
+      ww[q] = fa::pack_f16x2(__uint_as_float(ww[q] << 16), __uint_as_float(ww[q] & 0xFFFF0000u));
+    }
+    out[i] = w;
+  }
+  if ((vmax & 0xFFFFu) > 0x477Fu || (vmax >> 16) > 0x477Fu) atomicOr(status, fa::kStatusRange);
+}
+
+int convert_v(const void* v, void* vh, size_t n_elems, int* status, cudaStream_t st) {
+  const size_t n16 = n_elems / 8;
+  int blocks = (int)std::min<size_t>((n16 + 255) / 256, 152 * 8);
+  if (blocks < 1) blocks = 1;
+  fa_convert_v_kernel<<<blocks, 256, 0, st>>>(static_cast<const uint4*>(v), static_cast<uint4*>(vh),
+                                              n16, status);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+// Stream-ordered scratch from the device's default memory pool, which is
+// told once to keep freed blocks cached (no release at synchronisation).
+void* scratch_alloc(size_t bytes, cudaStream_t st) {
+  static std::once_flag once[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::call_once(once[dev & 63], [dev] {
+    cudaMemPool_t pool;
+    if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
+      uint64_t thr = ~0ull;
+      cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &thr);
+    }
+  });
+  void* ptr = nullptr;
+  if (cudaMallocAsync(&ptr, bytes, st) != cudaSuccess) return nullptr;
+  return ptr;
 }
 
 template <int D, bool BF16, int NS>
@@ -144,11 +193,31 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   int* status = status_ptr();
   if (!status) return cuda_fail(cudaGetLastError());
 
+  // bf16 V: an fp16 copy in stream-ordered scratch, freed on the same stream
+  const size_t nv = (size_t)B * Hkv * Skv * Dv;
+  void* v16 = const_cast<void*>(v);
+  if (!fp16) {
+    v16 = scratch_alloc(nv * 2, st);
+    if (!v16) return cuda_fail(cudaGetLastError());
+    const int rc = convert_v(v, v16, nv, status, st);
+    if (rc != FA_OK) {
+      cudaFreeAsync(v16, st);
+      return rc;
+    }
+  }
+  struct ScratchGuard {
+    void* ptr;
+    cudaStream_t st;
+    ~ScratchGuard() {
+      if (ptr) cudaFreeAsync(ptr, st);
+    }
+  } guard{fp16 ? nullptr : v16, st};
+
   fa::TiledParams prm;
   std::memset(&prm, 0, sizeof(prm));
   if (!encode_3d(&prm.tm_q, q, fp16, D, Sq, (uint64_t)B * Hq, fa::kBM) ||
       !encode_3d(&prm.tm_k, k, fp16, D, Skv, (uint64_t)B * Hkv, fa::kBN) ||
-      !encode_3d(&prm.tm_v, v, fp16, Dv, Skv, (uint64_t)B * Hkv, fa::kBN))
+      !encode_3d(&prm.tm_v, v16, /*fp16=*/true, Dv, Skv, (uint64_t)B * Hkv, fa::kBN))
     return cuda_fail(cudaErrorInvalidValue);
   prm.o = o;
   prm.lse = lse;

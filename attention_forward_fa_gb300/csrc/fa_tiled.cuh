@@ -7,10 +7,14 @@
 //   warps 0-3   softmax of slot 0 (one thread per query row), including the
 //               correction O *= exp2(m_old - m_new) of its rows when the max moves
 //   warps 4-7   softmax of slot 1
-//   warps 8-11  bf16 -> fp16 conversion of V tiles in shared memory (bf16 I/O)
-//               and the epilogue (O / l, LSE) of both slots
+//   warps 8-11  epilogue (O / l, LSE) of both slots
 //   warp  12    TMA producer: Q tiles, then K / V tiles into a ring of stages
 //   warp  13    TMEM allocator and tcgen05.mma issuer
+//   warp  14    MMA scheduler: waits on the mbarriers of the next MMA groups and
+//               releases them to warp 13 through named barriers
+// Q and K are bf16 or fp16; V is always fp16 here (bf16 V is converted to fp16
+// once per call by fa_convert_v_kernel), so that P and V share the fp16 type of
+// the P.V product.
 // The softmax warpgroups raise their register budget with setmaxnreg; the
 // other two lower theirs.
 //
@@ -45,7 +49,9 @@ static_assert(kSoftmaxRegs % 8 == 0 && kCorrRegs % 8 == 0 && kOtherRegs % 8 == 0
 static_assert(kRegsNeeded <= 65536 / kTiledThreads, "register split exceeds the register file");
 constexpr int kMaxSel = 512;      // longest block list a CTA stages in smem
 constexpr int kHiLoKeys = 256;    // rows with fewer valid keys use the hi+lo P split
-constexpr int kL2Ahead = 8;       // KV tiles prefetched into L2 ahead of the smem ring
+// hardware named barriers (0 is __syncthreads): 1-2 scheduler -> issuer release,
+// 3-4 issuer -> scheduler consumed, 5-6 softmax slot t -> issuer "P ready"
+constexpr int kBarPReady = 5;
 
 enum : int { kStatusTimeout = 1, kStatusRange = 2 };
 
@@ -96,10 +102,9 @@ __device__ __forceinline__ void fa_trace(const TiledParams& p, int role, int& n,
 #define FA_TR_ROLE(r) ((void)0)
 #define FA_TR(tag, t, j) ((void)0)
 #endif
-// tags: 1 S ready (softmax), 2 P written (softmax), 3 smdone seen (correction),
-// 4 rescale done / p_full arrive (correction), 5 stage filled (producer issue),
-// 6 QK issued, 7 PV issued, 8 V converted, 9 P ready seen (MMA), 10 epilogue start,
-// 11 epilogue end, 12 kernel start, 13 kernel end, 14 stage ready (MMA)
+// tags: 1 S ready (softmax), 2 P written (softmax), 5 stage load issued
+// (producer), 6 QK issued, 7 PV issued, 9 dependencies met (MMA), 10 epilogue
+// start, 11 epilogue end, 12 kernel start, 13 kernel end
 
 // Shared-memory plan (offsets from a 1024-byte aligned base).
 template <int D, int NS>
@@ -109,11 +114,11 @@ struct TiledSmem {
   static constexpr int kQOff = 0;
   static constexpr int kStageOff = 2 * kQBytes;
   static constexpr int kListOff = kStageOff + NS * kStageBytes;
-  static constexpr int kRowOff = kListOff + 2 * kMaxSel * 4;   // alpha[2][128], m[2][128], l[2][128]
-  static constexpr int kBarOff = kRowOff + 3 * 2 * kBM * 4;
-  // barriers: q_full[2], full[NS], empty[NS], vready[NS], s_full[2], p_full[2],
-  // o_ready[2], drain, sm_done[2]
-  static constexpr int kNumBars = 2 + 3 * NS + 6 + 1 + 2;
+  static constexpr int kRowOff = kListOff + 2 * kMaxSel * 4;   // m[2][128], l[2][128]
+  static constexpr int kBarOff = kRowOff + 2 * 2 * kBM * 4;
+  // barriers: q_full[2], full[NS], empty[NS], s_full[2], p_full[2], o_ready[2],
+  // drain, sm_done[2]
+  static constexpr int kNumBars = 2 + 2 * NS + 6 + 1 + 2;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;   // tmem base, abort flag, slot info
   static constexpr int kBytes = kMiscOff + 64;
   static constexpr int kAlloc = kBytes + 1024;              // slack for 1024-byte alignment
@@ -199,19 +204,17 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   const uint32_t sQ = sbase + SM::kQOff;
   const uint32_t sStage = sbase + SM::kStageOff;
   int* s_list = reinterpret_cast<int*>(smem + SM::kListOff);
-  float* s_alpha = reinterpret_cast<float*>(smem + SM::kRowOff);   // [2][128]
-  float* s_m = s_alpha + 2 * kBM;                                    // [2][128]
-  float* s_l = s_m + 2 * kBM;                                        // [2][128]
+  float* s_m = reinterpret_cast<float*>(smem + SM::kRowOff);   // [2][128]
+  float* s_l = s_m + 2 * kBM;                                   // [2][128]
   const uint32_t bar0 = sbase + SM::kBarOff;
   auto BAR_QFULL = [=](int t) { return bar0 + 8u * t; };
   auto BAR_FULL = [=](int s) { return bar0 + 8u * (2 + s); };
   auto BAR_EMPTY = [=](int s) { return bar0 + 8u * (2 + NS + s); };
-  auto BAR_VREADY = [=](int s) { return bar0 + 8u * (2 + 2 * NS + s); };
-  auto BAR_SFULL = [=](int t) { return bar0 + 8u * (2 + 3 * NS + t); };
-  auto BAR_PFULL = [=](int t) { return bar0 + 8u * (4 + 3 * NS + t); };
-  auto BAR_OREADY = [=](int t) { return bar0 + 8u * (6 + 3 * NS + t); };
-  const uint32_t BAR_DRAIN = bar0 + 8u * (8 + 3 * NS);
-  auto BAR_SMDONE = [=](int t) { return bar0 + 8u * (9 + 3 * NS + t); };
+  auto BAR_SFULL = [=](int t) { return bar0 + 8u * (2 + 2 * NS + t); };
+  auto BAR_PFULL = [=](int t) { return bar0 + 8u * (4 + 2 * NS + t); };
+  auto BAR_OREADY = [=](int t) { return bar0 + 8u * (6 + 2 * NS + t); };
+  const uint32_t BAR_DRAIN = bar0 + 8u * (8 + 2 * NS);
+  auto BAR_SMDONE = [=](int t) { return bar0 + 8u * (9 + 2 * NS + t); };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + SM::kMiscOff);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + SM::kMiscOff + 4);
   int* s_slot = reinterpret_cast<int*>(smem + SM::kMiscOff + 8);   // [2] n, [2] hilo
@@ -259,7 +262,6 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     for (int s = 0; s < NS; ++s) {
       mbar_init(BAR_FULL(s), 1);
       mbar_init(BAR_EMPTY(s), 1);
-      mbar_init(BAR_VREADY(s), kBM);    // every correction thread arrives
     }
     mbar_init(BAR_DRAIN, 1);
     *s_abort = 0;
@@ -323,7 +325,6 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   const int n0 = s_slot[0], n1 = s_slot[1];
   const bool shared_kv = !sparse ? (n0 >= 1 && n0 <= n1) : false;
   const WaitCtx wc{s_abort, p.status, p.timeout_ns};
-  auto kv_tile = [=](int t, int j) -> int { return sparse ? s_list[t * kMaxSel + j] : j; };
 
   if (warp < 8) {
     // ============================================================ softmax
@@ -340,12 +341,19 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + 128u * t + lane_off;
     const float c = p.scale_log2;
+    const uint64_t c2 = f2_pack(c, c);
     float m = -INFINITY, l = 0.f;
+    bool dead = false;   // a bounded wait expired: keep the hand-offs, skip the work
     for (int j = 0; j < nt; ++j) {
-      if (!__all_sync(0xffffffffu, wait_bar(BAR_SFULL(t), j & 1, wc))) break;
+      if (!dead && !__all_sync(0xffffffffu, wait_bar(BAR_SFULL(t), j & 1, wc))) dead = true;
+      if (dead) {
+        // the MMA issuer waits for one arrival per tile on a hardware barrier
+        named_arrive(kBarPReady + t, kBM + 32);
+        continue;
+      }
       if (row == 0) FA_TR(1, t, j);
       tc_fence_after();
-      const int kvt = kv_tile(t, j);
+      const int kvt = sparse ? s_list[t * kMaxSel + j] : j;
       const int kbase = kvt * kBN;
       const bool causal_here = (p.mask == 1) || (p.mask == 2 && kvt == qt);
       const bool need_mask =
@@ -370,9 +378,10 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = sv[i];
 #pragma unroll
-      for (int i = 8; i < kBN; ++i) mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
-      const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int i = 8; i < kBN; i += 16)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mx[q] = fmax3(mx[q], sv[i + q], sv[i + 8 + q]);
+      const float mb = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7])));
       const float m_new = fmaxf(m, mb);
       float m_use = m_new, alpha = 1.f;
       if (m != -INFINITY) {
@@ -384,111 +393,71 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         }
       }
       const float neg = (m_use == -INFINITY) ? 0.f : -m_use * c;
+      const uint64_t neg2 = f2_pack(neg, neg);
       // p = exp2(s c - m c); P (fp16) written over S (all of S is already in
       // registers), with the hi+lo split (second fp16 term p - fp16(p) in
       // columns 64..127) for rows that see few keys
-      float sm[4] = {0.f, 0.f, 0.f, 0.f};
-      if (!hilo) {
+      uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
-        for (int cc = 0; cc < kBN / 32; ++cc) {
-          uint32_t ph[16];
+      for (int cc = 0; cc < kBN / 32; ++cc) {
+        uint32_t ph[16], pl[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float a0 = ex2_approx(fmaf(sv[32 * cc + 2 * i], c, neg));
-            const float a1 = ex2_approx(fmaf(sv[32 * cc + 2 * i + 1], c, neg));
-            sm[i & 3] += a0 + a1;
-            ph[i] = pack_f16x2(a0, a1);
-          }
-          tmem_st16(tS + 16 * cc, ph);
+        for (int i = 0; i < 16; ++i) {
+          float a0, a1;
+          f2_unpack(f2_fma(f2_pack(sv[32 * cc + 2 * i], sv[32 * cc + 2 * i + 1]), c2, neg2), a0, a1);
+          a0 = ex2_approx(a0);
+          a1 = ex2_approx(a1);
+          sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(a0, a1));
+          ph[i] = pack_f16x2(a0, a1);
+          if (hilo) pl[i] = pack_f16x2(a0 - f16_lo_to_f32(ph[i]), a1 - f16_hi_to_f32(ph[i]));
         }
-      } else {
-#pragma unroll
-        for (int cc = 0; cc < kBN / 32; ++cc) {
-          uint32_t ph[16], pl[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float a0 = ex2_approx(fmaf(sv[32 * cc + 2 * i], c, neg));
-            const float a1 = ex2_approx(fmaf(sv[32 * cc + 2 * i + 1], c, neg));
-            sm[i & 3] += a0 + a1;
-            ph[i] = pack_f16x2(a0, a1);
-            pl[i] = pack_f16x2(a0 - f16_lo_to_f32(ph[i]), a1 - f16_hi_to_f32(ph[i]));
-          }
-          tmem_st16(tS + 16 * cc, ph);
-          tmem_st16(tS + 64 + 16 * cc, pl);
-        }
+        tmem_st16(tS + 16 * cc, ph);
+        if (hilo) tmem_st16(tS + 64 + 16 * cc, pl);
       }
-      const float rs = (sm[0] + sm[1]) + (sm[2] + sm[3]);
-      l = alpha * l + rs;
+      float r0, r1, r2, r3;
+      f2_unpack(sum2[0], r0, r1);
+      f2_unpack(sum2[1], r2, r3);
+      l = alpha * l + ((r0 + r1) + (r2 + r3));
       m = m_use;
-      // O_t *= alpha for the rows whose max moved.  The previous P.V product
-      // into O_t has landed (Q.K^T of this tile was issued after it and the
-      // tensor pipe completes in order); the wait only confirms it.
+      // O_t *= alpha for the rows whose max moved.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        if (!__all_sync(0xffffffffu, wait_bar(BAR_OREADY(t), (j - 1) & 1, wc))) break;
-        tc_fence_after();
+        // (the previous P.V product into O_t has completed: the commit that
+        // signalled S for this tile tracks every earlier MMA of the issuer)
         const uint32_t tO = tmem + 256u + 128u * t + lane_off;
+        const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
         for (int cc = 0; cc < Dv / 16; ++cc) {
           uint32_t r[16];
           tmem_ld16(tO + 16 * cc, r);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          for (int i = 0; i < 8; ++i) {
+            float x0, x1;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), a2), x0, x1);
+            r[2 * i] = __float_as_uint(x0);
+            r[2 * i + 1] = __float_as_uint(x1);
+          }
           tmem_st16(tO + 16 * cc, r);
         }
       }
       tmem_wait_st();
       tc_fence_before();
       if (row == 0) FA_TR(2, t, j);
-      mbar_arrive(BAR_PFULL(t));
+      // P_t (and the rescaled O_t) ready: hardware barrier to the MMA issuer
+      named_arrive(kBarPReady + t, kBM + 32);
     }
     // final row statistics for the epilogue warpgroup
     s_m[t * kBM + row] = m;
     s_l[t * kBM + row] = l;
     mbar_arrive(BAR_SMDONE(t));
   } else if (warp < 12) {
-    // ============================================================ correction + epilogue
+    // ============================================================ epilogue
     regs_dec<kCorrRegs>();
     FA_TR_ROLE(2);
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    bool ok = true;   // warp-uniform
-    int ld = 0, vc = 0;
-    uint32_t vmax = 0;   // largest |bf16 V| bit pattern seen (per 16-bit half)
-    const int ne = num_events(n0, n1);
-    for (int e = 0; e < ne && kBF16; ++e) {
-      const Event ev = event_at(e, n0, n1, shared_kv);
-      if (!ev.valid || !ev.load) continue;
-      const int s = ld % NS;
-      const uint32_t f = ld / NS;
-      ++ld;
-      if (!ev.pv) continue;
-      // bf16 -> fp16 in place as soon as the tile lands, so that P (fp16) and
-      // V share a type
-      ok = __all_sync(0xffffffffu, wait_bar(BAR_FULL(s), f & 1, wc));
-      if (!ok) break;
-      uint4* base = reinterpret_cast<uint4*>(smem + SM::kStageOff + s * SM::kStageBytes);
-#pragma unroll 4
-      for (int i = row; i < SM::kStageBytes / 16; i += kBM) {
-        uint4 w = base[i];
-        uint32_t* ww = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          vmax = max_u16x2(vmax, ww[q] & 0x7FFF7FFFu);
-          ww[q] = pack_f16x2(__uint_as_float(ww[q] << 16), __uint_as_float(ww[q] & 0xFFFF0000u));
-        }
-        base[i] = w;
-      }
-      fence_proxy_async_smem();
-      if (row == 0) FA_TR(8, ev.t, ev.j);
-      mbar_arrive(BAR_VREADY(vc % NS));
-      ++vc;
-    }
-    if (kBF16 && ((vmax & 0xFFFFu) > 0x477Fu || (vmax >> 16) > 0x477Fu))
-      atomicOr(p.status, kStatusRange);   // |v| >= 65536 became inf in fp16
-    // epilogue: O / l and LSE of both slots
 #pragma unroll 1
-    for (int t = 0; t < 2 && ok; ++t) {
+    for (int t = 0; t < 2; ++t) {
       const int qt = t ? qt1 : qt0;
       if (qt >= p.n_qt) continue;
       const int nt = t ? n1 : n0;
@@ -552,36 +521,16 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           tma_load_3d(sQ + t * SM::kQBytes + bx * (kBM * 128), &p.tm_q, BAR_QFULL(t), 64 * bx,
                       (t ? qt1 : qt0) * kBM, b * p.Hq + (t ? h1 : h0));
       }
-      // L2 prefetch of K and V tiles kL2Ahead iterations ahead of their use, so
-      // that the ring's TMA loads hit L2 instead of waiting on HBM
-      int pf0 = 0, pf1 = 0;
-      const CUtensorMap* tmk = &p.tm_k;
-      const CUtensorMap* tmv = &p.tm_v;
-      const int plane = b * p.Hkv + kvh;
-      auto prefetch_kv = [=](int t, int jj) {
-        const int kvt = sparse ? s_list[t * kMaxSel + jj] : jj;
-        for (int bx = 0; bx < kBoxes; ++bx) {
-          tma_prefetch_l2_3d(tmk, 64 * bx, kvt * kBN, plane);
-          tma_prefetch_l2_3d(tmv, 64 * bx, kvt * kBN, plane);
-        }
-      };
       int ld = 0;
       const int ne = num_events(n0, n1);
       for (int e = 0; e < ne; ++e) {
         const Event ev = event_at(e, n0, n1, shared_kv);
         if (!ev.valid || !ev.load) continue;
-        if (ev.t == 0 || shared_kv) {
-          const int lim = min(ev.j + kL2Ahead, shared_kv ? n1 : n0);
-          for (; pf0 < lim; ++pf0) prefetch_kv(shared_kv ? 1 : 0, pf0);
-        } else {
-          const int lim = min(ev.j + kL2Ahead, n1);
-          for (; pf1 < lim; ++pf1) prefetch_kv(1, pf1);
-        }
         const int s = ld % NS;
         const uint32_t f = ld / NS;
         ++ld;
         if (!wait_bar(BAR_EMPTY(s), (f & 1) ^ 1, wc)) break;
-        const int kvt = kv_tile(ev.t, ev.j);
+        const int kvt = sparse ? s_list[ev.t * kMaxSel + ev.j] : ev.j;
         FA_TR(5, ev.t, ev.j);
         mbar_arrive_expect_tx(BAR_FULL(s), SM::kStageBytes);
         const CUtensorMap* tm = ev.pv ? &p.tm_v : &p.tm_k;
@@ -598,88 +547,120 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 13) {
-    // ============================================================ MMA issuer
+  } else if (warp == 13 || warp == 14) {
+    // ============================================================ MMA issue
+    // Work is handed out as "groups": QK(0,0), QK(1,0), then per iteration j
+    // the pairs [PV(0,j) QK(0,j+1)] and [PV(1,j) QK(1,j+1)].  Warp 14 (the
+    // scheduler) waits on the TMA mbarriers a group depends on and releases the
+    // group to warp 13 (the issuer) through hardware named barriers, running up
+    // to two groups ahead; the softmax warps signal "P ready" to the issuer on
+    // a named barrier as well.  The issuer therefore never polls shared memory,
+    // which the tensor core's operand reads keep busy.
     regs_dec<kOtherRegs>();
-    FA_TR_ROLE(4);
-    if (lane == 0) {
-      int ld = 0, vc = 0;
-      uint32_t stK = 0, stV = 0;
-      const int hilo0 = s_slot[2], hilo1 = s_slot[3];
-      const uint64_t q_desc0 = sw128_desc(sQ, 16, 1024);               // K-major Q
-      const uint64_t k_desc0 = sw128_desc(sStage, 16, 1024);           // K-major K
-      const uint64_t v_desc0 = sw128_desc(sStage, kBN * 128, 1024);    // MN-major V
-      const int ne = num_events(n0, n1);
-      for (int e = 0; e < ne; ++e) {
-        const Event ev = event_at(e, n0, n1, shared_kv);
-        if (!ev.valid) continue;
-        const int t = ev.t, j = ev.j;
-        uint32_t s;
-        if (ev.load) {
-          s = ld % NS;
-          const uint32_t f = ld / NS;
-          ++ld;
-          if (ev.pv && kBF16) {
-            if (!wait_bar(BAR_VREADY(vc % NS), (vc / NS) & 1, wc)) break;
-            ++vc;
-          } else {
-            if (!wait_bar(BAR_FULL(s), f & 1, wc)) break;
-          }
-          FA_TR(14, t, j);
-          if (ev.pv) stV = s; else stK = s;
-        } else {
-          s = ev.pv ? stV : stK;
+    FA_TR_ROLE(warp == 13 ? 4 : 5);
+    const bool issuer = (warp == 13);
+    const int hilo0 = s_slot[2], hilo1 = s_slot[3];
+    const uint64_t q_desc0 = sw128_desc(sQ, 16, 1024);               // K-major Q
+    const uint64_t k_desc0 = sw128_desc(sStage, 16, 1024);           // K-major K
+    const uint64_t v_desc0 = sw128_desc(sStage, kBN * 128, 1024);    // MN-major V
+    const int nmax = n0 > n1 ? n0 : n1;
+    const int ngroups = nmax > 0 ? 2 + 2 * nmax : 0;
+    int ld = 0;            // ring loads consumed so far (independent K/V sequences)
+    bool aborted = false;
+#pragma unroll 1
+    for (int g = 0; g < ngroups; ++g) {
+      // ---- the group's events, ring stages and phases (same code in both warps)
+      const int t = g < 2 ? g : ((g - 2) & 1);
+      const int jpv = g < 2 ? -1 : ((g - 2) >> 1);         // P.V tile (none in groups 0, 1)
+      const int jqk = g < 2 ? 0 : jpv + 1;                 // Q.K^T tile
+      const int nt = t ? n1 : n0;
+      const bool pv_valid = jpv >= 0 && jpv < nt;
+      const bool qk_valid = jqk < nt;
+      // with shared K/V, slot 1 reuses slot 0's tiles and the load order is
+      // K_0 V_0 K_1 V_1 ...; otherwise every event loads its own tile, in order
+      const bool pv_load = pv_valid && (!shared_kv || t == 0 || jpv >= n0);
+      const bool qk_load = qk_valid && (!shared_kv || t == 0 || jqk >= n0);
+      int lpv, lqk;
+      if (shared_kv) {
+        lpv = 2 * jpv + 1;
+        lqk = 2 * jqk;
+      } else {
+        lpv = ld;
+        lqk = ld + (pv_load ? 1 : 0);
+        ld += (pv_load ? 1 : 0) + (qk_load ? 1 : 0);
+      }
+      const uint32_t sv_ = (uint32_t)lpv % NS, sk_ = (uint32_t)lqk % NS;
+      // ---- hand-off: the scheduler waits the TMA dependencies, then releases
+      if (!issuer) {
+        if (g >= 2) named_sync(3 + (g & 1), 64);      // issuer finished group g-2
+        if (lane == 0 && !aborted) {
+          if (pv_load && !wait_bar(BAR_FULL(sv_), (lpv / NS) & 1, wc)) aborted = true;
+          if (!aborted && qk_load && !wait_bar(BAR_FULL(sk_), (lqk / NS) & 1, wc)) aborted = true;
+          if (!aborted && qk_valid && jqk == 0 && !wait_bar(BAR_QFULL(t), 0, wc)) aborted = true;
         }
-        const uint32_t tS = tmem + 128u * t;
-        const uint32_t tO = tmem + 256u + 128u * t;
-        // descriptors: the start-address field is the low 14 bits (address >> 4)
-        // and never carries, so offsets are added to a base descriptor
-        const uint32_t stage16 = (s * SM::kStageBytes) >> 4;
-        if (!ev.pv) {
-          // S_t is free: the softmax read it before arriving on PFULL, which
-          // this thread waited on (with a fence) before the previous P.V
-          if (j == 0 && !wait_bar(BAR_QFULL(t), 0, wc)) break;
-          const uint64_t qd = q_desc0 + ((t * SM::kQBytes) >> 4);
-          const uint64_t kd = k_desc0 + stage16;
-#pragma unroll
-          for (int kk = 0; kk < kKSteps; ++kk) {
-            const uint32_t off16 = ((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4;
-            mma_ss(tS, qd + off16, kd + off16, kIdescQK, kk > 0);
-          }
-          mma_commit(BAR_SFULL(t));
-          FA_TR(6, t, j);
-        } else {
-          FA_TR(20, t, j);
-          if (!wait_bar(BAR_PFULL(t), j & 1, wc)) break;
-          FA_TR(9, t, j);
+        aborted = __shfl_sync(0xffffffffu, aborted, 0);
+        named_arrive(1 + (g & 1), 64);
+      } else {
+        named_sync(1 + (g & 1), 64);                   // TMA dependencies of group g met
+        // (after a timeout the scheduler still releases every group; the issuer
+        // then runs on stale operands, which is harmless: the status word
+        // already reports the failure and nothing waits on the results)
+        if (pv_valid) {
+          // P_t of tile jpv written by the four softmax warps of slot t
+          named_sync(kBarPReady + t, kBM + 32);
           tc_fence_after();
-          FA_TR(21, t, j);
-          const uint64_t vd = v_desc0 + stage16;
-#pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            mma_ts(tO, tS + 8 * kk, vd + (kk * 2048 >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-            if (kk == 0) FA_TR(22, t, j);
-          }
-          FA_TR(23, t, j);
-          if (t ? hilo1 : hilo0) {
+        }
+        if (lane == 0) {
+          const uint32_t tS = tmem + 128u * t;
+          if (pv_valid) {
+            FA_TR(7, t, jpv);
+            const uint32_t tO = tmem + 256u + 128u * t;
+            const uint64_t vd = v_desc0 + ((sv_ * SM::kStageBytes) >> 4);
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
-              mma_ts(tO, tS + 64 + 8 * kk, vd + (kk * 2048 >> 4), kIdescPV, 1u);
+              mma_ts(tO, tS + 8 * kk, vd + (kk * 2048 >> 4), kIdescPV,
+                     (jpv > 0 || kk > 0) ? 1u : 0u);
+            if (t ? hilo1 : hilo0) {
+#pragma unroll
+              for (int kk = 0; kk < kBN / 16; ++kk)
+                mma_ts(tO, tS + 64 + 8 * kk, vd + (kk * 2048 >> 4), kIdescPV, 1u);
+            }
+            mma_commit(BAR_OREADY(t));
+            // V's last reader is slot 1 (shared K/V) or this slot
+            if (!shared_kv || t == 1) mma_commit(BAR_EMPTY(sv_));
           }
-          mma_commit(BAR_OREADY(t));
-          FA_TR(7, t, j);
+          if (qk_valid) {
+            // S_t is free: the softmax read it before signalling P ready, which
+            // was waited on (and fenced) before the previous P.V
+            FA_TR(6, t, jqk);
+            const uint64_t qd = q_desc0 + ((t * SM::kQBytes) >> 4);
+            const uint64_t kd = k_desc0 + ((sk_ * SM::kStageBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < kKSteps; ++kk) {
+              const uint32_t off16 = ((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4;
+              mma_ss(tS, qd + off16, kd + off16, kIdescQK, kk > 0);
+            }
+            mma_commit(BAR_SFULL(t));
+            if (!shared_kv || t == 1) mma_commit(BAR_EMPTY(sk_));
+          }
         }
-        if (ev.rel) mma_commit(BAR_EMPTY(s));
       }
-      // every MMA has finished before TMEM is released
-      if (n0 + n1 > 0) {
-        mma_commit(BAR_DRAIN);
-        drain_bar(BAR_DRAIN, 0, wc.timeout);
-      }
+      __syncwarp();
+      if (issuer) named_arrive(3 + (g & 1), 64);     // group g issued
+    }
+    // the scheduler consumes the issuer's last two releases
+    if (!issuer) {
+      if (ngroups >= 2) named_sync(3 + (ngroups & 1), 64);
+      if (ngroups >= 1) named_sync(3 + ((ngroups - 1) & 1), 64);
+    }
+    // every MMA has finished before TMEM is released
+    if (issuer && lane == 0 && n0 + n1 > 0) {
+      mma_commit(BAR_DRAIN);
+      drain_bar(BAR_DRAIN, 0, wc.timeout);
     }
     __syncwarp();
   } else {
-    // warps 14-15: no role (they complete the fourth warpgroup)
+    // warp 15: no role (it completes the fourth warpgroup)
     regs_dec<kOtherRegs>();
   }
 
