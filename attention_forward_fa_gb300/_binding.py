@@ -52,6 +52,8 @@ def library() -> ctypes.CDLL:
         lib.fa_fwd.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 7 + [
             ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(fa_block_sparse_t),
             ctypes.POINTER(fa_topk_t), ctypes.c_float, ctypes.c_void_p]
+        lib.fa_fwd_noalloc.restype = ctypes.c_int
+        lib.fa_fwd_noalloc.argtypes = lib.fa_fwd.argtypes
         lib.fa_check_status.restype = ctypes.c_int
         lib.fa_check_status.argtypes = [ctypes.c_void_p]
         lib.fa_set_wait_timeout_ns.restype = None
@@ -104,6 +106,26 @@ def fa_fwd(q, k, v, o, lse, B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int
     return lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, D, Dv,
                       float(scale), int(mask_mode), _ptr(seqlens), bs, tk,
                       float(rescale_threshold), _stream(stream))
+
+
+def fa_fwd_noalloc(q, k, v, o, lse, B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int,
+                   Dv: int, scale: float, mask_mode: int, seqlens=None, kv_block_idx=None,
+                   topk_idx=None, rescale_threshold: float = 0.0, stream=None) -> int:
+    """fa_fwd without any memory allocation (fixed 32 MiB scratch inside the
+    library; bf16 V larger than that is rejected with FA_ERR_SCRATCH).  Same
+    arguments as fa_fwd.  Calls that overlap on the GPU race on the scratch."""
+    lib = library()
+    bs = None
+    if kv_block_idx is not None:
+        idx, max_sel, block, sb, sh = kv_block_idx
+        bs = ctypes.pointer(fa_block_sparse_t(_ptr(idx), max_sel, block, sb, sh))
+    tk = None
+    if topk_idx is not None:
+        idx, topk, sb = topk_idx
+        tk = ctypes.pointer(fa_topk_t(_ptr(idx), topk, sb))
+    return lib.fa_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv,
+                              D, Dv, float(scale), int(mask_mode), _ptr(seqlens), bs, tk,
+                              float(rescale_threshold), _stream(stream))
 
 
 def fa_check_status(stream=None) -> int:

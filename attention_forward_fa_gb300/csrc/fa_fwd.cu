@@ -20,6 +20,12 @@ namespace {
 // bit 0 = a bounded wait expired, bit 1 = a bf16 V value overflowed fp16.
 __device__ int g_fa_status;
 
+// Fixed scratch of fa_fwd_noalloc: room for the fp16 copy of a bf16 V of up
+// to kNoAllocScratchBytes.  It is part of the module image, so every device
+// that loads this library holds it until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;   // 32 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
 std::atomic<int> g_last_cuda{0};
 #ifdef FA_TRACE
 unsigned long long* g_trace = nullptr;
@@ -145,16 +151,12 @@ int launch_tiled(const fa::TiledParams& prm, int units, cudaStream_t st) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-}  // namespace
-
-extern "C" {
-
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
-           int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
-           const int32_t* seqlens, const fa_block_sparse_t* kv_block_idx,
-           const fa_topk_t* topk_idx, float rescale_threshold, void* stream) {
+// Argument checks shared by the entry points (nothing is launched on error).
+int validate(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
+             const int32_t* seqlens, const fa_block_sparse_t* kv_block_idx,
+             const fa_topk_t* topk_idx, float rescale_threshold) {
   const int mask = mask_mode & 0xF;
-  const bool fp16 = (mask_mode & FA_DTYPE_FP16) != 0;
   const bool v_from_k = (mask_mode & FA_V_FROM_K) != 0;
   if (mask_mode & ~(0xF | FA_DTYPE_FP16 | FA_V_FROM_K)) return FA_ERR_SHAPE;
   // ---- pointers
@@ -188,31 +190,17 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     return FA_ERR_ALIGN;
   if (seqlens && !aligned(seqlens, 4)) return FA_ERR_ALIGN;
   if (kv_block_idx && !aligned(kv_block_idx->idx, 4)) return FA_ERR_ALIGN;
+  return FA_OK;
+}
 
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  int* status = status_ptr();
-  if (!status) return cuda_fail(cudaGetLastError());
-
-  // bf16 V: an fp16 copy in stream-ordered scratch, freed on the same stream
-  const size_t nv = (size_t)B * Hkv * Skv * Dv;
-  void* v16 = const_cast<void*>(v);
-  if (!fp16) {
-    v16 = scratch_alloc(nv * 2, st);
-    if (!v16) return cuda_fail(cudaGetLastError());
-    const int rc = convert_v(v, v16, nv, status, st);
-    if (rc != FA_OK) {
-      cudaFreeAsync(v16, st);
-      return rc;
-    }
-  }
-  struct ScratchGuard {
-    void* ptr;
-    cudaStream_t st;
-    ~ScratchGuard() {
-      if (ptr) cudaFreeAsync(ptr, st);
-    }
-  } guard{fp16 ? nullptr : v16, st};
-
+// Tiled forward on validated arguments; `v16` is V in fp16 (the caller's V
+// for fp16 inputs, a converted copy for bf16 inputs).
+int run_tiled(const void* q, const void* k, const void* v16, void* o, float* lse, int B, int Hq,
+              int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
+              const int32_t* seqlens, const fa_block_sparse_t* kv_block_idx,
+              float rescale_threshold, int* status, cudaStream_t st) {
+  const int mask = mask_mode & 0xF;
+  const bool fp16 = (mask_mode & FA_DTYPE_FP16) != 0;
   fa::TiledParams prm;
   std::memset(&prm, 0, sizeof(prm));
   if (!encode_3d(&prm.tm_q, q, fp16, D, Sq, (uint64_t)B * Hq, fa::kBM) ||
@@ -268,6 +256,92 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
               : launch_tiled<64, true, 6>(prm, (int)units, st);
 }
 
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+           int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
+           const int32_t* seqlens, const fa_block_sparse_t* kv_block_idx,
+           const fa_topk_t* topk_idx, float rescale_threshold, void* stream) {
+  const int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
+                          kv_block_idx, topk_idx, rescale_threshold);
+  if (rc != FA_OK) return rc;
+  const bool fp16 = (mask_mode & FA_DTYPE_FP16) != 0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* status = status_ptr();
+  if (!status) return cuda_fail(cudaGetLastError());
+
+  // bf16 V: an fp16 copy in stream-ordered scratch, freed on the same stream
+  const size_t nv = (size_t)B * Hkv * Skv * Dv;
+  void* v16 = const_cast<void*>(v);
+  if (!fp16) {
+    v16 = scratch_alloc(nv * 2, st);
+    if (!v16) return cuda_fail(cudaGetLastError());
+    const int rcv = convert_v(v, v16, nv, status, st);
+    if (rcv != FA_OK) {
+      cudaFreeAsync(v16, st);
+      return rcv;
+    }
+  }
+  struct ScratchGuard {
+    void* ptr;
+    cudaStream_t st;
+    ~ScratchGuard() {
+      if (ptr) cudaFreeAsync(ptr, st);
+    }
+  } guard{fp16 ? nullptr : v16, st};
+  return run_tiled(q, k, v16, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
+                   kv_block_idx, rescale_threshold, status, st);
+}
+
+// Device address of g_noalloc_scratch for the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device (with that device current) and cached.
+static void* noalloc_scratch_address() {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+      g_last_cuda.store((int)e);
+      return nullptr;
+    }
+    addr[dev] = ptr;
+  }
+  return addr[dev];
+}
+
+int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                   int Hq, int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
+                   const int32_t* seqlens, const fa_block_sparse_t* kv_block_idx,
+                   const fa_topk_t* topk_idx, float rescale_threshold, void* stream) {
+  const int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
+                          kv_block_idx, topk_idx, rescale_threshold);
+  if (rc != FA_OK) return rc;
+  const bool fp16 = (mask_mode & FA_DTYPE_FP16) != 0;
+  const size_t nv = (size_t)B * Hkv * Skv * Dv;
+  if (!fp16 && nv * 2 > kNoAllocScratchBytes) return FA_ERR_SCRATCH;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* status = status_ptr();
+  if (!status) return cuda_fail(cudaGetLastError());
+  void* v16 = const_cast<void*>(v);
+  if (!fp16) {
+    // bf16 V -> fp16 into the fixed scratch (every element is overwritten, so
+    // nothing needs clearing first)
+    v16 = noalloc_scratch_address();
+    if (!v16) return FA_ERR_CUDA;
+    const int rcv = convert_v(v, v16, nv, status, st);
+    if (rcv != FA_OK) return rcv;
+  }
+  return run_tiled(q, k, v16, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
+                   kv_block_idx, rescale_threshold, status, st);
+}
+
 int fa_check_status(void* stream) {
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(st);
@@ -298,6 +372,7 @@ const char* fa_strerror(int code) {
     case FA_ERR_CUDA: return "CUDA call failed";
     case FA_ERR_DEVICE_TIMEOUT: return "bounded on-chip wait expired";
     case FA_ERR_RANGE: return "bf16 V value outside the fp16 range";
+    case FA_ERR_SCRATCH: return "bf16 V larger than the fixed scratch of fa_fwd_noalloc (32 MiB fp16)";
     default: return "unknown error code";
   }
 }

@@ -35,7 +35,10 @@
  *     NULL = the legacy default stream).  Argument errors are returned
  *     synchronously and nothing is launched.  Device-side errors are
  *     reported later through fa_check_status().
- *   - The library allocates no device memory per call.
+ *   - fa_fwd with bf16 inputs converts V to fp16 into stream-ordered scratch
+ *     (cudaMallocAsync from the device's default memory pool, released on
+ *     `stream` after use); it allocates nothing else.  fa_fwd_noalloc
+ *     allocates nothing at all.
  */
 #ifndef FA_FWD_H_
 #define FA_FWD_H_
@@ -58,6 +61,8 @@ extern "C" {
 #define FA_ERR_DEVICE_TIMEOUT  -7  /* a bounded on-chip wait expired (kernel bailed)  */
 #define FA_ERR_RANGE           -8  /* a bf16 V value outside the fp16 range (|v| >    */
                                    /* 65504) met the fp16 P.V product                 */
+#define FA_ERR_SCRATCH         -9  /* fa_fwd_noalloc: bf16 V needs more than its     */
+                                   /* fixed scratch (B*Hkv*Skv*Dv*2 > 32 MiB)         */
 
 /* ---- mask_mode flag word ----------------------------------------------- */
 /* bits 0-3: mask */
@@ -137,6 +142,35 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int mask_mode, const int32_t* seqlens,
            const fa_block_sparse_t* kv_block_idx, const fa_topk_t* topk_idx,
            float rescale_threshold, void* stream);
+
+/*
+ * fa_fwd_noalloc -- fa_fwd without any memory allocation.  (The pages define
+ * no counterpart: this is an interface for callers, not part of the method.)
+ *
+ * For callers that cannot let a library allocate device memory: programs that
+ * hand out all device memory from their own fixed arena and account for every
+ * byte, and latency-critical call sites where a driver allocation (and the
+ * synchronisation it may imply) is not acceptable.  fa_fwd converts a bf16 V
+ * to fp16 in stream-ordered scratch taken from the device's memory pool; this
+ * entry point uses a fixed array inside the library's device image instead
+ * (32 MiB, held by every device that loads the library until the process
+ * exits) and calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Same arguments, layouts and results as fa_fwd.  Differences:
+ *   - bf16 inputs with B*Hkv*Skv*Dv*2 bytes > 32 MiB are rejected with
+ *     FA_ERR_SCRATCH (fp16 inputs need no scratch and have no such limit);
+ *   - the first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture;
+ *   - every call shares the one array, which keeps the last call's contents:
+ *     calls whose work overlaps on the GPU (different streams without
+ *     ordering between them) race on it.  Serialise them, e.g. on one stream.
+ */
+int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int Hq, int Hkv, int Sq, int Skv, int D, int Dv, float scale,
+                   int mask_mode, const int32_t* seqlens,
+                   const fa_block_sparse_t* kv_block_idx, const fa_topk_t* topk_idx,
+                   float rescale_threshold, void* stream);
 
 /* Synchronises `stream`, then returns and clears the device status word of
  * the current device: FA_OK, FA_ERR_DEVICE_TIMEOUT or FA_ERR_RANGE (the first
