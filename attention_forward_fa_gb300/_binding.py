@@ -14,6 +14,7 @@ FA_MASK_CAUSAL = 1
 FA_MASK_CAUSAL_DIAG_BLOCK = 2
 FA_DTYPE_FP16 = 0x100
 FA_V_FROM_K = 0x200
+FA_V_FP16 = 0x400
 
 FA_OK = 0
 
@@ -54,6 +55,9 @@ def library() -> ctypes.CDLL:
             ctypes.POINTER(fa_topk_t), ctypes.c_float, ctypes.c_void_p]
         lib.fa_fwd_noalloc.restype = ctypes.c_int
         lib.fa_fwd_noalloc.argtypes = lib.fa_fwd.argtypes
+        lib.fa_convert_v_fp16.restype = ctypes.c_int
+        lib.fa_convert_v_fp16.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                          ctypes.c_void_p]
         lib.fa_check_status.restype = ctypes.c_int
         lib.fa_check_status.argtypes = [ctypes.c_void_p]
         lib.fa_set_wait_timeout_ns.restype = None
@@ -126,6 +130,11 @@ def fa_fwd_noalloc(q, k, v, o, lse, B: int, Hq: int, Hkv: int, Sq: int, Skv: int
     return lib.fa_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv,
                               D, Dv, float(scale), int(mask_mode), _ptr(seqlens), bs, tk,
                               float(rescale_threshold), _stream(stream))
+
+
+def fa_convert_v_fp16(v_bf16, v_fp16, n_elems: int, stream=None) -> int:
+    """fp16 copy of a bf16 V (see include/fa_fwd.h); returns the FA_* code."""
+    return library().fa_convert_v_fp16(_ptr(v_bf16), _ptr(v_fp16), int(n_elems), _stream(stream))
 
 
 def fa_check_status(stream=None) -> int:

@@ -78,11 +78,29 @@ int* status_ptr() {
 // bf16 -> fp16 copy of V (the P.V product runs on fp16 operands; fp16 keeps
 // three more mantissa bits of P than bf16).  bf16 -> fp16 is exact for
 // 2^-14 <= |v| <= 65504; larger magnitudes become inf and set status bit 1.
-__global__ void fa_convert_v_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
-                                    size_t n16, int* status) {
+__global__ void __launch_bounds__(256) fa_convert_v_kernel(const uint4* __restrict__ in,
+                                                            uint4* __restrict__ out, size_t n16,
+                                                            int* status) {
+  constexpr int kUnroll = 4;   // 16-byte loads in flight per thread
   uint32_t vmax = 0;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16;
-       i += (size_t)gridDim.x * blockDim.x) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  for (; i + (kUnroll - 1) * stride < n16; i += kUnroll * stride) {
+    uint4 w[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) w[u] = __ldcs(in + i + u * stride);   // read once
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      uint32_t* ww = reinterpret_cast<uint32_t*>(&w[u]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        vmax = fa::max_u16x2(vmax, ww[q] & 0x7FFF7FFFu);
+        ww[q] = fa::pack_f16x2(__uint_as_float(ww[q] << 16), __uint_as_float(ww[q] & 0xFFFF0000u));
+      }
+      out[i + u * stride] = w[u];
+    }
+  }
+  for (; i < n16; i += stride) {
     uint4 w = in[i];
     uint32_t* ww = reinterpret_cast<uint32_t*>(&w);
 #pragma unroll
@@ -158,7 +176,7 @@ int validate(const void* q, const void* k, const void* v, void* o, float* lse, i
              const fa_topk_t* topk_idx, float rescale_threshold) {
   const int mask = mask_mode & 0xF;
   const bool v_from_k = (mask_mode & FA_V_FROM_K) != 0;
-  if (mask_mode & ~(0xF | FA_DTYPE_FP16 | FA_V_FROM_K)) return FA_ERR_SHAPE;
+  if (mask_mode & ~(0xF | FA_DTYPE_FP16 | FA_V_FROM_K | FA_V_FP16)) return FA_ERR_SHAPE;
   // ---- pointers
   if (!q || !k || !o || !lse || (!v && !v_from_k)) return FA_ERR_NULL;
   if (kv_block_idx && !kv_block_idx->idx) return FA_ERR_NULL;
@@ -267,7 +285,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   const int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
                           kv_block_idx, topk_idx, rescale_threshold);
   if (rc != FA_OK) return rc;
-  const bool fp16 = (mask_mode & FA_DTYPE_FP16) != 0;
+  const bool fp16 = (mask_mode & (FA_DTYPE_FP16 | FA_V_FP16)) != 0;   // V already fp16
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* status = status_ptr();
   if (!status) return cuda_fail(cudaGetLastError());
@@ -323,7 +341,7 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* 
   const int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
                           kv_block_idx, topk_idx, rescale_threshold);
   if (rc != FA_OK) return rc;
-  const bool fp16 = (mask_mode & FA_DTYPE_FP16) != 0;
+  const bool fp16 = (mask_mode & (FA_DTYPE_FP16 | FA_V_FP16)) != 0;   // V already fp16
   const size_t nv = (size_t)B * Hkv * Skv * Dv;
   if (!fp16 && nv * 2 > kNoAllocScratchBytes) return FA_ERR_SCRATCH;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -340,6 +358,15 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* 
   }
   return run_tiled(q, k, v16, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
                    kv_block_idx, rescale_threshold, status, st);
+}
+
+int fa_convert_v_fp16(const void* v_bf16, void* v_fp16, int64_t n_elems, void* stream) {
+  if (!v_bf16 || !v_fp16) return FA_ERR_NULL;
+  if (n_elems <= 0 || n_elems % 8) return FA_ERR_SHAPE;
+  if (!aligned(v_bf16, 16) || !aligned(v_fp16, 16)) return FA_ERR_ALIGN;
+  int* status = status_ptr();
+  if (!status) return cuda_fail(cudaGetLastError());
+  return convert_v(v_bf16, v_fp16, (size_t)n_elems, status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fa_check_status(void* stream) {

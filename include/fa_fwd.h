@@ -75,6 +75,9 @@ extern "C" {
 /* top-k only: V is the first Dv columns of every K row (shared MLA latent);   */
 /* `v` may then be NULL */
 #define FA_V_FROM_K          0x200
+/* bf16 q / k / o with an fp16 `v` converted beforehand by fa_convert_v_fp16  */
+/* (e.g. once for a KV cache read by many calls): skips the in-call copy */
+#define FA_V_FP16            0x400
 
 /* ---- sparse descriptors ------------------------------------------------ */
 
@@ -171,6 +174,18 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* 
                    int mask_mode, const int32_t* seqlens,
                    const fa_block_sparse_t* kv_block_idx, const fa_topk_t* topk_idx,
                    float rescale_threshold, void* stream);
+
+/*
+ * fa_convert_v_fp16 -- fp16 copy of a bf16 tensor (the V operand).
+ *
+ * The P.V product runs on fp16 operands (fp16 keeps three more mantissa bits
+ * of the probabilities than bf16); fa_fwd converts a bf16 V itself, or takes
+ * this copy with FA_V_FP16.  v_bf16 and v_fp16 are device pointers, 16-byte
+ * aligned, n_elems a positive multiple of 8.  bf16 -> fp16 is exact for
+ * 2^-14 <= |v| <= 65504; larger magnitudes become inf and are reported as
+ * FA_ERR_RANGE by fa_check_status.  Asynchronous on `stream`.
+ */
+int fa_convert_v_fp16(const void* v_bf16, void* v_fp16, int64_t n_elems, void* stream);
 
 /* Synchronises `stream`, then returns and clears the device status word of
  * the current device: FA_OK, FA_ERR_DEVICE_TIMEOUT or FA_ERR_RANGE (the first

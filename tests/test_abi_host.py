@@ -59,7 +59,7 @@ def call(lib, **kw):
     (dict(q=None), -1), (dict(k=None), -1), (dict(o=None), -1), (dict(lse=None), -1),
     (dict(v=None), -1),
     (dict(B=0), -2), (dict(Hq=3, Hkv=2), -2), (dict(Sq=-1), -2), (dict(D=0), -2),
-    (dict(mask_mode=3), -2), (dict(mask_mode=2), -2), (dict(mask_mode=0x400), -2),
+    (dict(mask_mode=3), -2), (dict(mask_mode=2), -2), (dict(mask_mode=0x800), -2),
     (dict(kv_block_idx=(P, 17, 64, 0, 0)), -2), (dict(kv_block_idx=(P, 0, 128, 0, 0)), -2),
     (dict(kv_block_idx=(P, 513, 128, 0, 0)), -2),
     (dict(kv_block_idx=(P, 4, 128, 0, 0), topk_idx=(P, 8, 0)), -2),
@@ -75,3 +75,11 @@ def test_argument_errors_are_synchronous(lib, kw, code):
 def test_timeout_setter(lib):
     B.fa_set_wait_timeout_ns(5_000_000)
     B.fa_set_wait_timeout_ns(0)   # back to the default
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, P, 8), -1), ((P, None, 8), -1), ((P, P, 0), -2), ((P, P, 12), -2),
+    ((P + 8, P, 8), -4), ((P, P + 2, 8), -4),
+])
+def test_convert_v_argument_errors(lib, args, code):
+    assert B.fa_convert_v_fp16(*args, stream=0) == code

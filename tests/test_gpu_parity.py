@@ -141,3 +141,22 @@ def test_config4_full_size_sampled():
     p = W.config(4)
     rows = np.r_[0:2, 127:129, 8000:8002, 16382:16384]
     sampled_check(p, rows, [0, 9, 15], [0])
+
+
+def test_preconverted_fp16_v_equals_in_call_conversion():
+    """FA_V_FP16 with a V converted by fa_convert_v_fp16 gives the same bits as
+    letting fa_fwd convert V itself."""
+    import torch
+    import attention_forward_fa_gb300 as fa
+    p = W.dense(name="v16", B=2, Hq=4, Hkv=2, Sq=500, D=128, mask=W.MASK_CAUSAL, seed=23)
+    d = to_device(p)
+    O1, L1 = run_gpu(p, 0.0, d)
+    v16 = torch.empty(d["v"].shape, dtype=torch.float16, device="cuda")
+    assert fa.fa_convert_v_fp16(d["v"], v16, d["v"].numel()) == 0
+    o = torch.empty((p.B, p.Hq, p.Sq, p.Dv), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((p.B, p.Hq, p.Sq), dtype=torch.float32, device="cuda")
+    assert fa.fa_fwd(d["q"], d["k"], v16, o, lse, p.B, p.Hq, p.Hkv, p.Sq, p.Skv, p.D, p.Dv,
+                     p.scale, p.mask | fa.FA_V_FP16) == 0
+    assert fa.fa_check_status() == 0
+    assert np.array_equal(o.float().cpu().double().numpy(), O1)
+    assert np.array_equal(lse.cpu().double().numpy(), L1)
