@@ -13,6 +13,7 @@
 
 #include "../../include/fa_fwd.h"
 #include "fa_tiled.cuh"
+#include "fa_mla.cuh"
 
 namespace {
 
@@ -52,19 +53,35 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 // 3-D view (cols, rows, planes) of a contiguous [planes, rows, cols] 16-bit
-// tensor, tiled in boxes of 64 columns x box_rows rows with 128-byte swizzle.
+// tensor, tiled in boxes of 64 columns x box_rows rows x box_planes planes with
+// 128-byte swizzle.
 bool encode_3d(CUtensorMap* tm, const void* base, bool fp16, uint64_t cols, uint64_t rows,
-               uint64_t planes, uint32_t box_rows) {
+               uint64_t planes, uint32_t box_rows, uint32_t box_planes = 1) {
   auto enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[3] = {cols, rows, planes};
   cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
-  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t box[3] = {64, box_rows, box_planes};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(tm, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 2-D view (cols, rows) of a contiguous fp16 [rows, cols] tensor with a box of
+// 64 columns x 1 row and 128-byte swizzle: the map of four-row TMA gathers.
+bool encode_rows(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, 1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -193,7 +210,9 @@ int validate(const void* q, const void* k, const void* v, void* o, float* lse, i
     if (kv_block_idx->max_sel <= 0 || kv_block_idx->max_sel > fa::kMaxSel) return FA_ERR_SHAPE;
     if (kv_block_idx->stride_b < 0 || kv_block_idx->stride_h < 0) return FA_ERR_SHAPE;
   }
-  if (topk_idx && (topk_idx->topk <= 0 || topk_idx->stride_b < 0)) return FA_ERR_SHAPE;
+  if (topk_idx && (topk_idx->topk <= 0 || topk_idx->topk > fa::kMlaMaxTopk ||
+                   topk_idx->stride_b < 0))
+    return FA_ERR_SHAPE;
   if (!std::isfinite(scale)) return FA_ERR_SHAPE;
   if (!(rescale_threshold >= 0.f && rescale_threshold <= 15.f)) return FA_ERR_THRESHOLD;
   if ((long long)B * Hq > (1LL << 30) || (long long)Sq * 128 > (1LL << 31) ||
@@ -201,14 +220,73 @@ int validate(const void* q, const void* k, const void* v, void* o, float* lse, i
     return FA_ERR_SHAPE;
   // ---- supported variants
   const bool tiled = !topk_idx && !v_from_k && D == Dv && (D == 64 || D == 128);
-  if (!tiled) return FA_ERR_UNSUPPORTED;
+  const bool mla = topk_idx && v_from_k && D == fa::kMlaD && Dv == fa::kMlaDv && Hkv == 1;
+  if (!tiled && !mla) return FA_ERR_UNSUPPORTED;
+  if (mla) {
+    const long long units = (long long)B * Sq * ((Hq + fa::kMlaHeads - 1) / fa::kMlaHeads);
+    if ((long long)B * Skv > 0x7FFFFFFFLL || units * fa::kMlaSplit > 0x7FFFFFFFLL)
+      return FA_ERR_SHAPE;
+  }
   // ---- alignment (TMA: 16-byte bases; vector stores of O)
   if (!aligned(q, 16) || !aligned(k, 16) || (v && !aligned(v, 16)) || !aligned(o, 16) ||
       !aligned(lse, 4))
     return FA_ERR_ALIGN;
   if (seqlens && !aligned(seqlens, 4)) return FA_ERR_ALIGN;
   if (kv_block_idx && !aligned(kv_block_idx->idx, 4)) return FA_ERR_ALIGN;
+  if (topk_idx && !aligned(topk_idx->idx, 4)) return FA_ERR_ALIGN;
   return FA_OK;
+}
+
+template <bool BF16>
+int launch_mla(const fa::MlaParams& prm, long long units, cudaStream_t st) {
+  auto kern = fa::fa_mla_topk_kernel<BF16>;
+  constexpr int smem = fa::MlaSmem::kAlloc;
+  static std::once_flag once[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static cudaError_t attr_err[64];
+  std::call_once(once[dev & 63], [&] {
+    attr_err[dev & 63] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  if (attr_err[dev & 63] != cudaSuccess) return cuda_fail(attr_err[dev & 63]);
+  kern<<<(unsigned)units, fa::kMlaThreads, smem, st>>>(prm);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+// Top-k sparse MLA forward on validated arguments; `k16` is the key latent
+// [B, Skv, 576] in fp16 (the caller's for fp16 inputs or with FA_V_FP16, a
+// converted copy otherwise).
+int run_topk(const void* q, const void* k16, void* o, float* lse, int B, int Hq, int Sq, int Skv,
+             float scale, int mask_mode, const int32_t* seqlens, const fa_topk_t* tk,
+             float rescale_threshold, int* status, cudaStream_t st) {
+  const bool fp16 = (mask_mode & FA_DTYPE_FP16) != 0;
+  fa::MlaParams prm;
+  std::memset(&prm, 0, sizeof(prm));
+  const uint32_t q_rows = (uint32_t)std::min<long long>(fa::kMlaHeads, (long long)B * Hq);
+  if (!encode_3d(&prm.tm_q, q, fp16, fa::kMlaD, Sq, (uint64_t)B * Hq, 1, q_rows) ||
+      !encode_rows(&prm.tm_k, k16, fa::kMlaD, (uint64_t)B * Skv))
+    return cuda_fail(cudaErrorInvalidValue);
+  prm.q_rows = (int)q_rows;
+  prm.o = o;
+  prm.lse = lse;
+  prm.seqlens = seqlens;
+  prm.topk = tk->idx;
+  prm.topk_stride_b = tk->stride_b;
+  prm.W = tk->topk;
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Sq = Sq;
+  prm.Skv = Skv;
+  prm.n_hg = (Hq + fa::kMlaHeads - 1) / fa::kMlaHeads;
+  prm.causal = (mask_mode & 0xF) == FA_MASK_CAUSAL;
+  prm.scale = scale;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.threshold = rescale_threshold;
+  prm.timeout_ns = g_timeout_ns.load();
+  prm.status = status;
+  const long long units = (long long)B * Sq * prm.n_hg * fa::kMlaSplit;
+  return fp16 ? launch_mla<false>(prm, units, st) : launch_mla<true>(prm, units, st);
 }
 
 // Tiled forward on validated arguments; `v16` is V in fp16 (the caller's V
@@ -290,8 +368,10 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   int* status = status_ptr();
   if (!status) return cuda_fail(cudaGetLastError());
 
-  // bf16 V: an fp16 copy in stream-ordered scratch, freed on the same stream
-  const size_t nv = (size_t)B * Hkv * Skv * Dv;
+  // bf16 V (with top-k: the whole key latent, V being part of it): an fp16
+  // copy in stream-ordered scratch, freed on the same stream
+  const size_t nv = topk_idx ? (size_t)B * Skv * D : (size_t)B * Hkv * Skv * Dv;
+  if (topk_idx) v = k;
   void* v16 = const_cast<void*>(v);
   if (!fp16) {
     v16 = scratch_alloc(nv * 2, st);
@@ -309,6 +389,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
       if (ptr) cudaFreeAsync(ptr, st);
     }
   } guard{fp16 ? nullptr : v16, st};
+  if (topk_idx)
+    return run_topk(q, v16, o, lse, B, Hq, Sq, Skv, scale, mask_mode, seqlens, topk_idx,
+                    rescale_threshold, status, st);
   return run_tiled(q, k, v16, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
                    kv_block_idx, rescale_threshold, status, st);
 }
@@ -342,8 +425,9 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* 
                           kv_block_idx, topk_idx, rescale_threshold);
   if (rc != FA_OK) return rc;
   const bool fp16 = (mask_mode & (FA_DTYPE_FP16 | FA_V_FP16)) != 0;   // V already fp16
-  const size_t nv = (size_t)B * Hkv * Skv * Dv;
+  const size_t nv = topk_idx ? (size_t)B * Skv * D : (size_t)B * Hkv * Skv * Dv;
   if (!fp16 && nv * 2 > kNoAllocScratchBytes) return FA_ERR_SCRATCH;
+  if (topk_idx) v = k;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* status = status_ptr();
   if (!status) return cuda_fail(cudaGetLastError());
@@ -356,6 +440,9 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* 
     const int rcv = convert_v(v, v16, nv, status, st);
     if (rcv != FA_OK) return rcv;
   }
+  if (topk_idx)
+    return run_topk(q, v16, o, lse, B, Hq, Sq, Skv, scale, mask_mode, seqlens, topk_idx,
+                    rescale_threshold, status, st);
   return run_tiled(q, k, v16, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
                    kv_block_idx, rescale_threshold, status, st);
 }

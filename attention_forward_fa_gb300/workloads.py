@@ -38,10 +38,19 @@ BLOCK = 128  # block-sparse granularity (rows and keys per block)
 
 
 def round_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """fp32 -> bf16 bit patterns, round to nearest even (inputs are finite)."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return u.astype(np.uint16)
+    """fp32 -> bf16 bit patterns, round to nearest even (inputs are finite, so
+    the 32-bit sum below cannot wrap); chunked to stay in cache."""
+    src = np.ascontiguousarray(x, dtype=np.float32).reshape(-1).view(np.uint32)
+    out = np.empty(src.size, dtype=np.uint16)
+    step = 1 << 20
+    for s in range(0, src.size, step):
+        u = src[s:s + step]
+        r = (u >> 16) & 1
+        r += u
+        r += 0x7FFF
+        r >>= 16
+        out[s:s + step] = r
+    return out.reshape(np.shape(x))
 
 
 def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:

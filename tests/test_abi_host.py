@@ -72,6 +72,25 @@ def test_argument_errors_are_synchronous(lib, kw, code):
     assert call(lib, **kw) == code
 
 
+MLA = dict(Hq=128, Hkv=1, D=576, Dv=512, v=None, mask_mode=0x200, topk_idx=(P, 2048, 0))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(topk_idx=(P, 2049, 0)), -2), (dict(topk_idx=(P, 0, 0)), -2),
+    (dict(topk_idx=(P, 64, -1)), -2), (dict(mask_mode=0x202), -2),
+    (dict(Hq=4, Hkv=2), -3), (dict(mask_mode=0), -1), (dict(D=512), -3), (dict(Dv=576), -3),
+    (dict(topk_idx=(P + 2, 64, 0)), -4), (dict(q=P + 8), -4),
+])
+def test_topk_argument_errors(lib, kw, code):
+    a = dict(MLA)
+    a.update(kw)
+    assert call(lib, **a) == code
+
+
+def test_topk_without_latent_is_unsupported(lib):
+    assert call(lib, topk_idx=(P, 64, 0)) == -3   # D = Dv = 128 with a separate V
+
+
 def test_timeout_setter(lib):
     B.fa_set_wait_timeout_ns(5_000_000)
     B.fa_set_wait_timeout_ns(0)   # back to the default
