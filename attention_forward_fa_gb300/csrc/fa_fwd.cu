@@ -70,21 +70,6 @@ bool encode_3d(CUtensorMap* tm, const void* base, bool fp16, uint64_t cols, uint
   return r == CUDA_SUCCESS;
 }
 
-// 2-D view (cols, rows) of a contiguous fp16 [rows, cols] tensor with a box of
-// 64 columns x 1 row and 128-byte swizzle: the map of four-row TMA gathers.
-bool encode_rows(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows) {
-  auto enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, 1};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 int* status_ptr() {
   // the symbol's device address for the current device
   void* ptr = nullptr;
@@ -264,9 +249,9 @@ int run_topk(const void* q, const void* k16, void* o, float* lse, int B, int Hq,
   fa::MlaParams prm;
   std::memset(&prm, 0, sizeof(prm));
   const uint32_t q_rows = (uint32_t)std::min<long long>(fa::kMlaHeads, (long long)B * Hq);
-  if (!encode_3d(&prm.tm_q, q, fp16, fa::kMlaD, Sq, (uint64_t)B * Hq, 1, q_rows) ||
-      !encode_rows(&prm.tm_k, k16, fa::kMlaD, (uint64_t)B * Skv))
+  if (!encode_3d(&prm.tm_q, q, fp16, fa::kMlaD, Sq, (uint64_t)B * Hq, 1, q_rows))
     return cuda_fail(cudaErrorInvalidValue);
+  prm.kl = static_cast<const uint16_t*>(k16);
   prm.q_rows = (int)q_rows;
   prm.o = o;
   prm.lse = lse;

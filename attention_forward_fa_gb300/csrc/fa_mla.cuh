@@ -17,13 +17,15 @@
 // K is read from an fp16 copy of the latent (bf16 inputs are converted once per
 // call), so that the same shared-memory tile is the B operand of both
 // products: K-major for Q K^T over all 576 columns, MN-major for P V over this
-// CTA's 128 value columns.  Tiles of 64 gathered rows come from TMA row
-// gathers (four rows per instruction) into a ring of three stages; the Q tile
-// is first staged (bf16 or fp16, via TMA) in ring stages 0-1 and converted to
+// CTA's 128 value columns.  Tiles of 64 gathered rows are copied in 16-byte
+// chunks (cp.async, one producer warp per stage of a three-stage ring; TMA row
+// gathers move far fewer bytes per cycle for 128-byte rows); the Q tile is
+// first staged (bf16 or fp16, via TMA) in ring stages 0-1 and converted to
 // fp16 into TMEM.
 //
 // Warps: 0-3 Q conversion, softmax (one thread per head row) and epilogue;
-// warp 4 TMA producer; warp 5 TMEM allocator and MMA issuer.
+// warps 4-6 producers (warp 4 also issues the Q tile's TMA); warp 7 TMEM
+// allocator and MMA issuer.
 // MMA order: S_0, then per tile j: S_{j+1} = Q K_{j+1}^T, O += P_j V_j, so the
 // softmax of tile j overlaps the next Q K^T.  A tile gets a second P.V pass
 // with the residual P_lo = p - fp16(p) (written over P once the first pass has
@@ -43,14 +45,14 @@ constexpr int kMlaSplit = kMlaDv / kMlaDq;   // CTAs per (token, head group)
 constexpr int kMlaHeads = 128;               // query heads per CTA (MMA rows)
 constexpr int kMlaNS = 3;                    // ring stages
 constexpr int kMlaMaxTopk = 2048;            // longest slot list
-constexpr int kMlaThreads = 192;
+constexpr int kMlaThreads = 256;
 constexpr int kMlaBoxes = kMlaD / 64;        // 128-byte column boxes per key row
 constexpr int kMlaHiLoKeys = 256;
 constexpr uint32_t kMlaColO = 0, kMlaColS = 128, kMlaColP = 192, kMlaColQ = 224;
 
 struct MlaParams {
   CUtensorMap tm_q;   // 3-D (D, Sq, B*Hq), box 64 x 1 x 128 heads
-  CUtensorMap tm_k;   // 2-D (D, B*Skv) fp16, box 64 x 1 (row gathers)
+  const uint16_t* kl; // fp16 key latent [B, Skv, 576]
   void* o;
   float* lse;
   const int* seqlens;
@@ -151,7 +153,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     *s_nkeys = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 7) {
     tmem_alloc(smem_u32(s_tmem), 512);
     tmem_relinquish();
   }
@@ -161,7 +163,6 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   // compact the key list.
   if (warp == 4 && lane == 0 && live) {
     tma_prefetch_desc(&p.tm_q);
-    tma_prefetch_desc(&p.tm_k);
     mbar_arrive_expect_tx(BAR_QFULL, kMlaBoxes * 128 * p.q_rows);
     for (int bx = 0; bx < kMlaBoxes; ++bx)
       tma_load_3d(sRing + bx * SM::kQBoxBytes, &p.tm_q, BAR_QFULL, 64 * bx, t,
@@ -413,53 +414,50 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     if (write && qtr == 0)
       p.lse[(size_t)(b * p.Hq + h) * p.Sq + t] =
           (acc && l > 0.f) ? m * p.scale + __logf(l) : INFINITY;
-  } else if (warp == 4) {
-    // ============================================================ producer
-    int issued = 0;
+  } else if (warp < 4 + kMlaNS) {
+    // ============================================================ producers
+    // Warp 4 + s fills ring stage s: the tiles j with (j + 2) % 3 == s.  Each
+    // lane copies 16-byte chunks (4 rows x 128 bytes per warp instruction, so
+    // every 128-byte line is read whole) to their 128-byte-swizzle positions,
+    // then the warp waits for its copies, fences them for the tensor core (async
+    // proxy) and arrives on the stage's full barrier.
+    const int s = warp - 4;
+    const uint32_t stage = sRing + s * SM::kStageBytes;
+    const int sub = lane >> 3;       // row within a group of four
+    const int chunk = lane & 7;      // 16-byte chunk within a 128-byte row
     bool ab = false;
 #pragma unroll 1
-    for (int j = 0; j < nt; ++j) {
-      int s, use;
-      mla_stage(j, s, use);
+    for (int j = (s + 1) % kMlaNS; j < nt && !ab; j += kMlaNS) {
+      int s_, use;
+      mla_stage(j, s_, use);
       if (lane == 0) {
         if (use == 0 && s < 2) {
-          ab = !wait_bar(BAR_QDONE, 0, wc);                        // Q staging consumed
+          ab = !wait_bar(BAR_QDONE, 0, wc);                             // Q staging consumed
         } else if (use > 0) {
           ab = !wait_bar(bar0 + 8u * (kMlaNS + s), (use - 1) & 1, wc);   // stage released
         }
-        if (!ab) mbar_arrive_expect_tx(bar0 + 8u * s, SM::kStageBytes);
       }
       ab = __shfl_sync(0xffffffffu, ab, 0);
       if (ab) break;
+#pragma unroll 1
+      for (int g = 0; g < kMlaN / 4; ++g) {
+        // positions past the last key repeat a valid row (their scores are masked)
+        const int row = 4 * g + sub;
+        const int pos = j * kMlaN + row;
+        const int key = s_idx[pos < nkeys ? pos : nkeys - 1];
+        const uint16_t* src = p.kl + ((size_t)b * p.Skv + key) * kMlaD + chunk * 8;
+        const uint32_t dst = stage + row * 128 + ((chunk ^ (row & 7)) << 4);
+#pragma unroll
+        for (int bx = 0; bx < kMlaBoxes; ++bx) cp_async16(dst + bx * SM::kBoxBytes, src + bx * 64);
+      }
+      cp_async_commit();
+      cp_async_wait_all();
+      fence_proxy_async_smem();
       __syncwarp();
-      if (lane < kMlaN / 4) {
-        // lane g gathers rows 4g .. 4g+3 of the tile; positions past the last
-        // key repeat a valid row (their scores are masked)
-        int rows[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int pos = j * kMlaN + 4 * lane + i;
-          rows[i] = b * p.Skv + s_idx[pos < nkeys ? pos : nkeys - 1];
-        }
-        const uint32_t dst = sRing + s * SM::kStageBytes + lane * 512;
-#pragma unroll
-        for (int bx = 0; bx < kMlaBoxes; ++bx)
-          tma_gather4(dst + bx * SM::kBoxBytes, &p.tm_k, bar0 + 8u * s, 64 * bx, rows[0], rows[1],
-                      rows[2], rows[3]);
-      }
-      issued = j + 1;
+      if (lane == 0) mbar_arrive(bar0 + 8u * s);
     }
-    // let every copy in flight land before the CTA's shared memory goes away
-    if (lane == 0) {
-      if (*s_abort) {
-        for (int j = (issued > kMlaNS ? issued - kMlaNS : 0); j < issued; ++j) {
-          int s, use;
-          mla_stage(j, s, use);
-          drain_bar(bar0 + 8u * s, use & 1, wc.timeout);
-        }
-      }
-      if (live) drain_bar(BAR_QFULL, 0, wc.timeout);
-    }
+    // the Q tile's copy must land before the CTA's shared memory goes away
+    if (s == 0 && lane == 0 && live) drain_bar(BAR_QFULL, 0, wc.timeout);
     __syncwarp();
   } else {
     // ============================================================ MMA issue
@@ -521,7 +519,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   // ---------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 7) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

@@ -115,16 +115,32 @@ def dist_setup():
     return world, rank, local
 
 
-def workload_problem():
+WORKLOADS = {
+    "c2": (2, "dense causal attention forward, B=2 H=16 Sq=Skv=2048 D=Dv=128, bf16 Q/K/V ~ N(0,1), "
+              "scale 1/sqrt(128), fp32 LSE"),
+    "c3": (3, "GQA causal ragged attention forward, B=4 Hq=32 Hkv=8 S=4096 D=Dv=128, "
+              "seqlens [4096, 3001, 517, 14], bf16"),
+    "c4": (4, "block-sparse attention forward, B=1 H=16 S=16384 D=Dv=128, fp16, per (head, query "
+              "block) the diagonal + 15 random KV blocks of 128 (causal inside the diagonal block)"),
+    "c5": (5, "top-k sparse MLA forward, T=4096 tokens, 128 query heads, one latent KV head, "
+              "D=576 (512 latent + 64 rope), Dv=512, 2048 key slots per token, bf16"),
+}
+
+
+def workload_problem(name="c2"):
     from attention_forward_fa_gb300 import workloads as W
-    return W.config(2)
+    return W.config(WORKLOADS[name][0])
 
 
-def workload_desc(p):
-    return {"workload": "dense causal attention forward, B=2 H=16 Sq=Skv=2048 D=Dv=128, bf16 "
-                        "Q/K/V ~ N(0,1), scale 1/sqrt(128), fp32 LSE",
-            "B": p.B, "H": p.Hq, "Sq": p.Sq, "Skv": p.Skv, "D": p.D, "Dv": p.Dv,
-            "mask": "causal", "rescale_threshold": 0.0}
+def workload_desc(p, name="c2"):
+    from attention_forward_fa_gb300 import workloads as W
+    mask = {W.MASK_NONE: "none", W.MASK_CAUSAL: "causal",
+            W.MASK_CAUSAL_DIAG_BLOCK: "causal inside the diagonal block"}[p.mask]
+    d = {"workload": WORKLOADS[name][1], "B": p.B, "Hq": p.Hq, "Hkv": p.Hkv, "Sq": p.Sq,
+         "Skv": p.Skv, "D": p.D, "Dv": p.Dv, "mask": mask, "rescale_threshold": 0.0}
+    if p.topk_idx is not None:
+        d["topk"] = int(p.topk_idx.shape[-1])
+    return d
 
 
 def oracle_rows(p, q, k, v, b, h, rows):
@@ -222,40 +238,67 @@ def run_ours(args, world, rank, local):
         dist.barrier()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    p = workload_problem()
+    p = workload_problem(args.workload)
     flops = W.algorithmic_flops(p)
-    dt = torch.bfloat16
+    bf16 = p.dtype == "bf16"
+    dt = torch.bfloat16 if bf16 else torch.float16
 
     def up(bits):
         return torch.from_numpy(bits.view(np.int16).copy()).to(dev).view(dt)
 
-    q0, k0, v0 = up(p.q_bits), up(p.k_bits), up(p.v_bits)
-    nv = v0.numel()
-    per_set = 2 * (q0.numel() + k0.numel() + 2 * v0.numel() + q0.numel()) + 4 * p.B * p.Hq * p.Sq
+    def up_i32(a):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    q0, k0 = up(p.q_bits), up(p.k_bits)
+    v0 = None if p.v_from_k else up(p.v_bits)
+    seqlens = up_i32(p.seqlens)
+    blk = tk = None
+    if p.kv_block_idx is not None:
+        bi = up_i32(p.kv_block_idx)
+        nb, hh, nqb, ms = bi.shape
+        blk = (bi, ms, 128, hh * nqb * ms, nqb * ms if hh > 1 else 0)
+    if p.topk_idx is not None:
+        ti = up_i32(p.topk_idx)
+        tk = (ti, ti.shape[-1], ti.shape[-2] * ti.shape[-1])
+    # the tensor converted to fp16 for the P.V product: V, or the whole key
+    # latent when V is part of K
+    conv_src = k0 if p.v_from_k else v0
+    n_conv = conv_src.numel() if bf16 else 0
+    mode = p.mask | (fa.FA_V_FROM_K if p.v_from_k else 0)
+    mode |= fa.FA_V_FP16 if bf16 else fa.FA_DTYPE_FP16
+    o_bytes = 2 * p.B * p.Hq * p.Sq * p.Dv + 4 * p.B * p.Hq * p.Sq
+    per_set = 2 * (q0.numel() + k0.numel() + (0 if v0 is None else v0.numel())) + 2 * n_conv + o_bytes
     n_sets = max(2, int(np.ceil(2.5 * L2_BYTES / per_set)))
     sets = []
     for i in range(n_sets):
         o = torch.empty((p.B, p.Hq, p.Sq, p.Dv), dtype=dt, device=dev)
         lse = torch.empty((p.B, p.Hq, p.Sq), dtype=torch.float32, device=dev)
-        v16 = torch.empty(v0.shape, dtype=torch.float16, device=dev)
-        sets.append((q0.clone(), k0.clone(), v0.clone(), v16, o, lse))
+        q, k = q0.clone(), k0.clone()
+        v = None if v0 is None else v0.clone()
+        src = k if p.v_from_k else v
+        c16 = torch.empty(src.shape, dtype=torch.float16, device=dev) if bf16 else None
+        sets.append((q, k, v, src, c16, o, lse))
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
 
-    # one step = the whole hot path: bf16 -> fp16 copy of V, then the tiled
-    # forward on it (the two launches fa_fwd makes internally, issued through
-    # the C ABI one by one so that the tiled kernel can be timed on its own)
+    # One step = the whole hot path.  bf16 inputs: the fp16 copy of V (or of
+    # the key latent), then the forward on it -- the two launches fa_fwd makes
+    # internally, issued through the C ABI one by one so that the attention
+    # kernel can be timed on its own.  fp16 inputs: one launch.
     def step(i, ev=None):
-        q, k, v, v16, o, lse = sets[i % n_sets]
+        q, k, v, src, c16, o, lse = sets[i % n_sets]
         if ev:
             ev[0].record(stream)
-        code = fa.fa_convert_v_fp16(v, v16, nv, sp)
-        if code != 0:
-            raise RuntimeError(fa.fa_strerror(code))
+        if bf16:
+            code = fa.fa_convert_v_fp16(src, c16, n_conv, sp)
+            if code != 0:
+                raise RuntimeError(fa.fa_strerror(code))
         if ev:
             ev[1].record(stream)
-        code = fa.fa_fwd(q, k, v16, o, lse, p.B, p.Hq, p.Hkv, p.Sq, p.Skv, p.D, p.Dv, p.scale,
-                         p.mask | fa.FA_V_FP16, None, None, None, 0.0, sp)
+        kk = c16 if (bf16 and p.v_from_k) else k
+        vv = None if p.v_from_k else (c16 if bf16 else v)
+        code = fa.fa_fwd(q, kk, vv, o, lse, p.B, p.Hq, p.Hkv, p.Sq, p.Skv, p.D, p.Dv, p.scale,
+                         mode, seqlens, blk, tk, 0.0, sp)
         if code != 0:
             raise RuntimeError(fa.fa_strerror(code))
         if ev:
@@ -271,7 +314,7 @@ def run_ours(args, world, rank, local):
     t_soak = time.perf_counter()
     i = 0
     while time.perf_counter() - t_soak < args.soak:
-        for _ in range(200):
+        for _ in range(20):
             step(i)
             i += 1
         torch.cuda.synchronize()
@@ -307,19 +350,22 @@ def run_ours(args, world, rank, local):
 
     # end to end through the public entry point with host buffers
     pin = lambda x: x.cpu().pin_memory()  # noqa: E731
-    hq, hk, hv = pin(q0), pin(k0), pin(v0)
+    hq, hk = pin(q0), pin(k0)
+    hv = None if v0 is None else pin(v0)
     ho = torch.empty((p.B, p.Hq, p.Sq, p.Dv), dtype=dt).pin_memory()
     hl = torch.empty((p.B, p.Hq, p.Sq), dtype=torch.float32).pin_memory()
-    dq, dk, dv, _, do, dl = sets[0]
-    h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2
+    dq, dk, dv, _, _, do, dl = sets[0]
+    h2d = 2 * (hq.numel() + hk.numel() + (0 if hv is None else hv.numel()))
     d2h = ho.numel() * 2 + hl.numel() * 4
+    e2e_mode = p.mask | (fa.FA_V_FROM_K if p.v_from_k else 0) | (0 if bf16 else fa.FA_DTYPE_FP16)
 
     def e2e_step():
         dq.copy_(hq, non_blocking=True)
         dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
+        if hv is not None:
+            dv.copy_(hv, non_blocking=True)
         code = fa.fa_fwd(dq, dk, dv, do, dl, p.B, p.Hq, p.Hkv, p.Sq, p.Skv, p.D, p.Dv, p.scale,
-                         p.mask, None, None, None, 0.0, sp)
+                         e2e_mode, seqlens, blk, tk, 0.0, sp)
         if code != 0:
             raise RuntimeError(fa.fa_strerror(code))
         ho.copy_(do, non_blocking=True)
@@ -350,30 +396,35 @@ def run_ours(args, world, rank, local):
     peaks, peak_src = measured_peaks()
     peak = float(peaks["bf16_tflops"])
     achieved = flops / (kern_avg_ms * 1e-3) / 1e12
-    cfg = workload_desc(p)
+    cfg = workload_desc(p, args.workload)
     cfg.update({"parallelism": f"replicas x{world} (no exchange)",
                 "l2": f"{n_sets} rotating input/output sets of {per_set / 2**20:.0f} MiB "
                       f"(> 2 x 129 MiB L2), no flush",
                 "algorithmic_gflop_per_step": flops / 1e9})
+    if p.topk_idx is not None:
+        kernel = f"fa_mla_topk_kernel<{'bf16' if bf16 else 'fp16'}>"
+    else:
+        kernel = f"fa_fwd_tiled_kernel<{p.D},{'bf16' if bf16 else 'fp16'},{4 if p.D == 128 else 6}>"
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak,
+            "peak_source": f"{peak_src} bf16_tflops (burst); the fp16 products run at the same "
+                           f"nominal rate",
+            "traffic": dram_traffic(args.workload), "kernel": kernel,
+            "kernel_avg_ms": kern_avg_ms}
+    if bf16:
+        roof["other_kernel"] = {"name": "fa_convert_v_kernel (bf16 -> fp16 copy of "
+                                        + ("the key latent)" if p.v_from_k else "V)"),
+                                "avg_ms": conv_avg_ms}
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": cfg,
-            "pct_of_bf16_peak": 100.0 * achieved / peak,
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak,
-                         "peak_source": f"{peak_src} bf16_tflops (burst); P.V runs as fp16 at "
-                                        f"the same nominal rate",
-                         "traffic": dram_traffic("c2_causal"),
-                         "kernel": "fa_fwd_tiled_kernel<128,bf16,4>",
-                         "kernel_avg_ms": kern_avg_ms,
-                         "other_kernel": {"name": "fa_convert_v_kernel (bf16 -> fp16 V)",
-                                          "avg_ms": conv_avg_ms}},
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if bf16 else "fp16", "data": "synthetic", "config": cfg,
+            "pct_of_bf16_peak": 100.0 * achieved / peak, "roofline": roof,
             "clocks": clocks,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": 2 * args.steps}
-    if world == 1 and not args.no_cpu_baseline:
+            "gpu_launches": (2 if bf16 else 1) * args.steps}
+    if world == 1 and not args.no_cpu_baseline and args.workload == "c2":
         f, t, n = oracle_timed(p, args.cpu_seconds)
         line["cpu_baseline"] = {
             "value": f / t / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
@@ -395,6 +446,9 @@ def main():
     ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed load before timing")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c2",
+                    help="c2 (default) is the benchmark line; the others time the same path "
+                         "on the other workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
