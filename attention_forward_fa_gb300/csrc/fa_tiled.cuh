@@ -466,7 +466,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       bool acc = false;
       if (nt > 0) {
         acc = __all_sync(0xffffffffu, wait_bar(BAR_SMDONE(t), 0, wc)) &&
-              __all_sync(0xffffffffu, wait_bar(BAR_OREADY(t), (nt - 1) & 1, wc));
+              __all_sync(0xffffffffu, wait_bar(BAR_OREADY(t), 0, wc));   // the last P.V
         if (!acc) break;
         tc_fence_after();
       }
@@ -567,6 +567,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     const int ngroups = nmax > 0 ? 2 + 2 * nmax : 0;
     int ld = 0;            // ring loads consumed so far (independent K/V sequences)
     bool aborted = false;
+    const uint32_t lead = elect_lane();
 #pragma unroll 1
     for (int g = 0; g < ngroups; ++g) {
       // ---- the group's events, ring stages and phases (same code in both warps)
@@ -610,39 +611,42 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           named_sync(kBarPReady + t, kBM + 32);
           tc_fence_after();
         }
-        if (lane == 0) {
-          const uint32_t tS = tmem + 128u * t;
-          if (pv_valid) {
-            FA_TR(7, t, jpv);
-            const uint32_t tO = tmem + 256u + 128u * t;
-            const uint64_t vd = v_desc0 + ((sv_ * SM::kStageBytes) >> 4);
+        // The whole warp runs the issue code (warp-uniform branches only);
+        // the elected lane's predicate lets exactly one copy of each tcgen05
+        // instruction through (always the same lane: a commit tracks the MMAs
+        // of the thread that issues it).
+        const uint32_t tS = tmem + 128u * t;
+        if (pv_valid) {
+          if (lead) FA_TR(7, t, jpv);
+          const uint32_t tO = tmem + 256u + 128u * t;
+          const uint64_t vd = v_desc0 + ((sv_ * SM::kStageBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts_if(tO, tS + 8 * kk, vd + (kk * 2048 >> 4), kIdescPV,
+                      (jpv > 0 || kk > 0) ? 1u : 0u, lead);
+          if (t ? hilo1 : hilo0) {
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
-              mma_ts(tO, tS + 8 * kk, vd + (kk * 2048 >> 4), kIdescPV,
-                     (jpv > 0 || kk > 0) ? 1u : 0u);
-            if (t ? hilo1 : hilo0) {
-#pragma unroll
-              for (int kk = 0; kk < kBN / 16; ++kk)
-                mma_ts(tO, tS + 64 + 8 * kk, vd + (kk * 2048 >> 4), kIdescPV, 1u);
-            }
-            mma_commit(BAR_OREADY(t));
-            // V's last reader is slot 1 (shared K/V) or this slot
-            if (!shared_kv || t == 1) mma_commit(BAR_EMPTY(sv_));
+              mma_ts_if(tO, tS + 64 + 8 * kk, vd + (kk * 2048 >> 4), kIdescPV, 1u, lead);
           }
-          if (qk_valid) {
-            // S_t is free: the softmax read it before signalling P ready, which
-            // was waited on (and fenced) before the previous P.V
-            FA_TR(6, t, jqk);
-            const uint64_t qd = q_desc0 + ((t * SM::kQBytes) >> 4);
-            const uint64_t kd = k_desc0 + ((sk_ * SM::kStageBytes) >> 4);
+          // O_t is read only by the epilogue, after the slot's last P.V
+          if (jpv == nt - 1) mma_commit_if(BAR_OREADY(t), lead);
+          // V's last reader is slot 1 (shared K/V) or this slot
+          if (!shared_kv || t == 1) mma_commit_if(BAR_EMPTY(sv_), lead);
+        }
+        if (qk_valid) {
+          // S_t is free: the softmax read it before signalling P ready, which
+          // was waited on (and fenced) before the previous P.V
+          if (lead) FA_TR(6, t, jqk);
+          const uint64_t qd = q_desc0 + ((t * SM::kQBytes) >> 4);
+          const uint64_t kd = k_desc0 + ((sk_ * SM::kStageBytes) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < kKSteps; ++kk) {
-              const uint32_t off16 = ((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4;
-              mma_ss(tS, qd + off16, kd + off16, kIdescQK, kk > 0);
-            }
-            mma_commit(BAR_SFULL(t));
-            if (!shared_kv || t == 1) mma_commit(BAR_EMPTY(sk_));
+          for (int kk = 0; kk < kKSteps; ++kk) {
+            const uint32_t off16 = ((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4;
+            mma_ss_if(tS, qd + off16, kd + off16, kIdescQK, kk > 0, lead);
           }
+          mma_commit_if(BAR_SFULL(t), lead);
+          if (!shared_kv || t == 1) mma_commit_if(BAR_EMPTY(sk_), lead);
         }
       }
       __syncwarp();
@@ -654,7 +658,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       if (ngroups >= 1) named_sync(3 + ((ngroups - 1) & 1), 64);
     }
     // every MMA has finished before TMEM is released
-    if (issuer && lane == 0 && n0 + n1 > 0) {
+    if (issuer && lead && n0 + n1 > 0) {
       mma_commit(BAR_DRAIN);
       drain_bar(BAR_DRAIN, 0, wc.timeout);
     }
