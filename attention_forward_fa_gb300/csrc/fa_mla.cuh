@@ -461,8 +461,12 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     __syncwarp();
   } else {
     // ============================================================ MMA issue
-    if (lane == 0 && nt > 0) {
-      bool ok = wait_bar(BAR_QDONE, 0, wc);
+    // The whole warp waits and runs the issue code (warp-uniform control flow);
+    // only the elected lane's tcgen05 instructions take effect, always the same
+    // lane since a commit tracks the MMAs of the thread that issues it.
+    if (nt > 0) {
+      const uint32_t lead = elect_lane();
+      bool ok = __all_sync(0xffffffffu, wait_bar(BAR_QDONE, 0, wc));
       tc_fence_after();
       const uint64_t k_desc0 = sw128_desc(sRing, 16, 1024);                          // K-major
       const uint64_t v_desc0 = sw128_desc(sRing + qtr * 2 * SM::kBoxBytes, SM::kBoxBytes, 1024);
@@ -471,19 +475,19 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       for (int j = 0; j <= nt && ok; ++j) {
         if (j < nt) {
           // S_j = Q K_j^T, once the softmax of tile j-1 has read S
-          if (j > 0) ok = wait_bar(BAR_SFREE, (j - 1) & 1, wc);
+          if (j > 0) ok = __all_sync(0xffffffffu, wait_bar(BAR_SFREE, (j - 1) & 1, wc));
           int s, use;
           mla_stage(j, s, use);
-          if (ok) ok = wait_bar(bar0 + 8u * s, use & 1, wc);
+          if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar0 + 8u * s, use & 1, wc));
           if (!ok) break;
           tc_fence_after();
           const uint64_t kd = k_desc0 + ((uint32_t)(s * SM::kStageBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kMlaD / 16; ++kk) {
             const uint32_t off16 = (uint32_t)((kk >> 2) * SM::kBoxBytes + (kk & 3) * 32) >> 4;
-            mma_ts(tmem + kMlaColS, tmem + kMlaColQ + 8 * kk, kd + off16, kIdescQK, kk > 0);
+            mma_ts_if(tmem + kMlaColS, tmem + kMlaColQ + 8 * kk, kd + off16, kIdescQK, kk > 0, lead);
           }
-          mma_commit(BAR_SFULL);
+          mma_commit_if(BAR_SFULL, lead);
         }
         if (j == 0) continue;
         // O += P_{j-1} V_{j-1} (this CTA's 128 value columns of the tile), then
@@ -493,7 +497,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         mla_stage(jp, s, use);
         const uint64_t vd = v_desc0 + ((uint32_t)(s * SM::kStageBytes) >> 4);
         for (int pass = 0; pass < 2; ++pass) {
-          if (!wait_bar(BAR_PREADY, c_pready & 1, wc)) {
+          if (!__all_sync(0xffffffffu, wait_bar(BAR_PREADY, c_pready & 1, wc))) {
             ok = false;
             break;
           }
@@ -501,19 +505,21 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kMlaN / 16; ++kk)
-            mma_ts(tmem + kMlaColO, tmem + kMlaColP + 8 * kk, vd + ((kk * 2048) >> 4), kIdescPV,
-                   (jp > 0 || pass > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(BAR_PVDONE);
+            mma_ts_if(tmem + kMlaColO, tmem + kMlaColP + 8 * kk, vd + ((kk * 2048) >> 4), kIdescPV,
+                      (jp > 0 || pass > 0 || kk > 0) ? 1u : 0u, lead);
+          mma_commit_if(BAR_PVDONE, lead);
           if (pass == 0 && !s_lo[jp & 1]) break;
         }
         if (!ok) break;
-        mma_commit(bar0 + 8u * (kMlaNS + s));   // stage free
+        mma_commit_if(bar0 + 8u * (kMlaNS + s), lead);   // stage free
       }
       // every MMA has finished before TMEM is released
-      mma_commit(BAR_DRAIN);
-      drain_bar(BAR_DRAIN, 0, wc.timeout);
+      if (lead) {
+        mma_commit(BAR_DRAIN);
+        drain_bar(BAR_DRAIN, 0, wc.timeout);
+      }
+      __syncwarp();
     }
-    __syncwarp();
   }
 
   // ---------------------------------------------------------------- teardown
