@@ -260,8 +260,9 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         // Every softmax thread reaches the barrier reduction once per tile, also
         // after a bounded wait gave up, so that no thread waits on it forever.
         if (!dead && !__all_sync(0xffffffffu, wait_bar(BAR_SFULL, j & 1, wc))) dead = true;
-        uint32_t ph[32], pl[32], pr[32];
-        float alpha = 1.f;
+        uint32_t ph[32], pl[32];
+        float sv[kMlaN];
+        float alpha = 1.f, neg = 0.f;
         bool lo_row = false;
         if (!dead) {
           tc_fence_after();
@@ -272,7 +273,6 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(BAR_SFREE);   // S may be overwritten by the next Q K^T
-          float sv[kMlaN];
 #pragma unroll
           for (int i = 0; i < kMlaN; ++i) sv[i] = __uint_as_float(su[i]);
           const int lim = nkeys - j * kMlaN;   // columns >= lim hold no key
@@ -303,32 +303,44 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
           // p > 1 (a kept max below the block max) or a short row: this tile
           // also gets the residual pass P_lo = p - fp16(p)
           lo_row = hilo || mb > m_use;
-          const float neg = (m_use == -INFINITY) ? 0.f : -m_use * c;
+          neg = (m_use == -INFINITY) ? 0.f : -m_use * c;
+          m = m_use;
+        }
+        // residual pass for the whole CTA? (every softmax thread, once per tile)
+        const bool lo = named_or(2, kMlaHeads, lo_row);
+        if (!dead) {
           const uint64_t neg2 = f2_pack(neg, neg);
           uint64_t sum2[2] = {0ull, 0ull};
+          // (two copies of the loop: the residual test inside it would cost
+          // more instructions than the exponentials)
+          if (!lo) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            float a0, a1;
-            f2_unpack(f2_fma(f2_pack(sv[2 * i], sv[2 * i + 1]), c2, neg2), a0, a1);
-            a0 = ex2_approx(a0);
-            a1 = ex2_approx(a1);
-            sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(a0, a1));
-            ph[i] = pack_f16x2(a0, a1);
-            pl[i] = __float_as_uint(a0);   // p kept for the residual below
-            pr[i] = __float_as_uint(a1);
+            for (int i = 0; i < 32; ++i) {
+              float a0, a1;
+              f2_unpack(f2_fma(f2_pack(sv[2 * i], sv[2 * i + 1]), c2, neg2), a0, a1);
+              a0 = ex2_approx(a0);
+              a1 = ex2_approx(a1);
+              sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(a0, a1));
+              ph[i] = pack_f16x2(a0, a1);
+            }
+          } else {
+            // rows that do not need the residual contribute zeros to its pass
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              float a0, a1;
+              f2_unpack(f2_fma(f2_pack(sv[2 * i], sv[2 * i + 1]), c2, neg2), a0, a1);
+              a0 = ex2_approx(a0);
+              a1 = ex2_approx(a1);
+              sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(a0, a1));
+              ph[i] = pack_f16x2(a0, a1);
+              pl[i] = lo_row ? pack_f16x2(a0 - f16_lo_to_f32(ph[i]), a1 - f16_hi_to_f32(ph[i])) : 0u;
+            }
           }
           float r0, r1, r2, r3;
           f2_unpack(sum2[0], r0, r1);
           f2_unpack(sum2[1], r2, r3);
           l = alpha * l + ((r0 + r1) + (r2 + r3));
-          m = m_use;
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            pl[i] = lo_row ? pack_f16x2(__uint_as_float(pl[i]) - f16_lo_to_f32(ph[i]),
-                                        __uint_as_float(pr[i]) - f16_hi_to_f32(ph[i]))
-                           : 0u;
         }
-        const bool lo = named_or(2, kMlaHeads, lo_row);   // for the whole CTA
         if (dead) continue;
         // the previous tile's P.V passes have read P and written O
         if (j > 0 && !__all_sync(0xffffffffu, wait_bar(BAR_PVDONE, (npv - 1) & 1, wc))) {

@@ -398,21 +398,40 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       // registers), with the hi+lo split (second fp16 term p - fp16(p) in
       // columns 64..127) for rows that see few keys
       uint64_t sum2[2] = {0ull, 0ull};
+      // (two copies of the loop: a hi+lo test inside it costs more instructions
+      // than the exponentials themselves)
+      if (!hilo) {
 #pragma unroll
-      for (int cc = 0; cc < kBN / 32; ++cc) {
-        uint32_t ph[16], pl[16];
+        for (int cc = 0; cc < kBN / 32; ++cc) {
+          uint32_t ph[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float a0, a1;
-          f2_unpack(f2_fma(f2_pack(sv[32 * cc + 2 * i], sv[32 * cc + 2 * i + 1]), c2, neg2), a0, a1);
-          a0 = ex2_approx(a0);
-          a1 = ex2_approx(a1);
-          sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(a0, a1));
-          ph[i] = pack_f16x2(a0, a1);
-          if (hilo) pl[i] = pack_f16x2(a0 - f16_lo_to_f32(ph[i]), a1 - f16_hi_to_f32(ph[i]));
+          for (int i = 0; i < 16; ++i) {
+            float a0, a1;
+            f2_unpack(f2_fma(f2_pack(sv[32 * cc + 2 * i], sv[32 * cc + 2 * i + 1]), c2, neg2), a0, a1);
+            a0 = ex2_approx(a0);
+            a1 = ex2_approx(a1);
+            sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(a0, a1));
+            ph[i] = pack_f16x2(a0, a1);
+          }
+          tmem_st16(tS + 16 * cc, ph);
         }
-        tmem_st16(tS + 16 * cc, ph);
-        if (hilo) tmem_st16(tS + 64 + 16 * cc, pl);
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < kBN / 32; ++cc) {
+          uint32_t ph[16], pl[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float a0, a1;
+            f2_unpack(f2_fma(f2_pack(sv[32 * cc + 2 * i], sv[32 * cc + 2 * i + 1]), c2, neg2), a0, a1);
+            a0 = ex2_approx(a0);
+            a1 = ex2_approx(a1);
+            sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(a0, a1));
+            ph[i] = pack_f16x2(a0, a1);
+            pl[i] = pack_f16x2(a0 - f16_lo_to_f32(ph[i]), a1 - f16_hi_to_f32(ph[i]));
+          }
+          tmem_st16(tS + 16 * cc, ph);
+          tmem_st16(tS + 64 + 16 * cc, pl);
+        }
       }
       float r0, r1, r2, r3;
       f2_unpack(sum2[0], r0, r1);
@@ -423,22 +442,24 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         // (the previous P.V product into O_t has completed: the commit that
         // signalled S for this tile tracks every earlier MMA of the issuer)
+        // (all of the row in flight at once: the S row's registers are free here)
         const uint32_t tO = tmem + 256u + 128u * t + lane_off;
         const uint64_t a2 = f2_pack(alpha, alpha);
+        uint32_t r[Dv];
 #pragma unroll
-        for (int cc = 0; cc < Dv / 16; ++cc) {
-          uint32_t r[16];
-          tmem_ld16(tO + 16 * cc, r);
-          tmem_wait_ld();
+        for (int cc = 0; cc < Dv / 32; ++cc)
+          tmem_ld32(tO + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * cc]));
+        tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float x0, x1;
-            f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), a2), x0, x1);
-            r[2 * i] = __float_as_uint(x0);
-            r[2 * i + 1] = __float_as_uint(x1);
-          }
-          tmem_st16(tO + 16 * cc, r);
+        for (int i = 0; i < Dv / 2; ++i) {
+          float x0, x1;
+          f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), a2), x0, x1);
+          r[2 * i] = __float_as_uint(x0);
+          r[2 * i + 1] = __float_as_uint(x1);
         }
+#pragma unroll
+        for (int cc = 0; cc < Dv / 32; ++cc)
+          tmem_st32(tO + 32 * cc, *reinterpret_cast<const uint32_t(*)[32]>(&r[32 * cc]));
       }
       tmem_wait_st();
       tc_fence_before();
