@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       const bool causal_here = (p.mask == 1) || (p.mask == 2 && kvt == qt);
       const bool need_mask =
           !row_valid || kbase + kBN > kv_len || (causal_here && kbase + kBN - 1 > q0);
-      // keys at column >= lim are masked (only consulted when need_mask)
+      // keys at column >= lim are masked (lim >= kBN when nothing is)
       const int lim = !row_valid ? 0 : min(kv_len - kbase, causal_here ? qi - kbase + 1 : kBN);
       // the whole S row of this thread in registers (4 loads in flight)
       uint32_t su[kBN];
@@ -369,10 +369,27 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       float sv[kBN];
 #pragma unroll
       for (int i = 0; i < kBN; ++i) sv[i] = __uint_as_float(su[i]);
-      if (need_mask) {
+      if (__any_sync(0xffffffffu, need_mask)) {
+        // Warp-uniform decisions per 32-column chunk: chunks below every row's
+        // limit stay, chunks above every limit are cleared, and only a chunk
+        // that straddles the warp's limits (the diagonal block of a causal
+        // tile, a ragged tail) is masked element by element.
+        const int lim_lo = __reduce_min_sync(0xffffffffu, lim);
+        const int lim_hi = __reduce_max_sync(0xffffffffu, lim);
 #pragma unroll
-        for (int i = 0; i < kBN; ++i)
-          if (i >= lim) sv[i] = -INFINITY;
+        for (int cc = 0; cc < kBN / 32; ++cc) {
+          const bool clear = 32 * cc >= lim_hi;
+          const bool part = !clear && 32 * cc + 32 > lim_lo;
+          if (clear) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sv[32 * cc + i] = -INFINITY;
+          }
+          if (part) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (32 * cc + i >= lim) sv[32 * cc + i] = -INFINITY;
+          }
+        }
       }
       float mx[8];
 #pragma unroll
