@@ -143,9 +143,9 @@ void* scratch_alloc(size_t bytes, cudaStream_t st) {
   return ptr;
 }
 
-template <int D, bool BF16, int NS>
+template <int D, bool BF16, int NS, bool CONV>
 int launch_tiled(const fa::TiledParams& prm, int units, cudaStream_t st) {
-  auto kern = fa::fa_fwd_tiled_kernel<D, BF16, NS>;
+  auto kern = fa::fa_fwd_tiled_kernel<D, BF16, NS, CONV>;
   constexpr int smem = fa::TiledSmem<D, NS>::kAlloc;
   static std::once_flag once[64];
   int dev = 0;
@@ -274,19 +274,20 @@ int run_topk(const void* q, const void* k16, void* o, float* lse, int B, int Hq,
   return fp16 ? launch_mla<false>(prm, units, st) : launch_mla<true>(prm, units, st);
 }
 
-// Tiled forward on validated arguments; `v16` is V in fp16 (the caller's V
-// for fp16 inputs, a converted copy for bf16 inputs).
-int run_tiled(const void* q, const void* k, const void* v16, void* o, float* lse, int B, int Hq,
+// Tiled forward on validated arguments.  `v` is fp16 (fp16 inputs, or a bf16
+// call with FA_V_FP16), else bf16, converted tile by tile inside the kernel.
+int run_tiled(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
               int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
               const int32_t* seqlens, const fa_block_sparse_t* kv_block_idx,
               float rescale_threshold, int* status, cudaStream_t st) {
   const int mask = mask_mode & 0xF;
   const bool fp16 = (mask_mode & FA_DTYPE_FP16) != 0;
+  const bool conv = !fp16 && !(mask_mode & FA_V_FP16);   // V arrives as bf16
   fa::TiledParams prm;
   std::memset(&prm, 0, sizeof(prm));
   if (!encode_3d(&prm.tm_q, q, fp16, D, Sq, (uint64_t)B * Hq, fa::kBM) ||
       !encode_3d(&prm.tm_k, k, fp16, D, Skv, (uint64_t)B * Hkv, fa::kBN) ||
-      !encode_3d(&prm.tm_v, v16, /*fp16=*/true, Dv, Skv, (uint64_t)B * Hkv, fa::kBN))
+      !encode_3d(&prm.tm_v, v, /*fp16=*/!conv, Dv, Skv, (uint64_t)B * Hkv, fa::kBN))
     return cuda_fail(cudaErrorInvalidValue);
   prm.o = o;
   prm.lse = lse;
@@ -330,11 +331,13 @@ int run_tiled(const void* q, const void* k, const void* v16, void* o, float* lse
   if (units > 0x7FFFFFFF) return FA_ERR_SHAPE;
 
   if (D == 128) {
-    return fp16 ? launch_tiled<128, false, 4>(prm, (int)units, st)
-                : launch_tiled<128, true, 4>(prm, (int)units, st);
+    if (fp16) return launch_tiled<128, false, 4, false>(prm, (int)units, st);
+    return conv ? launch_tiled<128, true, 4, true>(prm, (int)units, st)
+                : launch_tiled<128, true, 4, false>(prm, (int)units, st);
   }
-  return fp16 ? launch_tiled<64, false, 6>(prm, (int)units, st)
-              : launch_tiled<64, true, 6>(prm, (int)units, st);
+  if (fp16) return launch_tiled<64, false, 6, false>(prm, (int)units, st);
+  return conv ? launch_tiled<64, true, 6, true>(prm, (int)units, st)
+              : launch_tiled<64, true, 6, false>(prm, (int)units, st);
 }
 
 }  // namespace
@@ -353,17 +356,19 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   int* status = status_ptr();
   if (!status) return cuda_fail(cudaGetLastError());
 
-  // bf16 V (with top-k: the whole key latent, V being part of it): an fp16
-  // copy in stream-ordered scratch, freed on the same stream
-  const size_t nv = topk_idx ? (size_t)B * Skv * D : (size_t)B * Hkv * Skv * Dv;
-  if (topk_idx) v = k;
-  void* v16 = const_cast<void*>(v);
+  if (!topk_idx)   // a bf16 V is converted inside the tiled kernel
+    return run_tiled(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
+                     kv_block_idx, rescale_threshold, status, st);
+  // top-k: an fp16 copy of the bf16 key latent (V is part of it) in
+  // stream-ordered scratch, freed on the same stream
+  const size_t nv = (size_t)B * Skv * D;
+  void* k16 = const_cast<void*>(k);
   if (!fp16) {
-    v16 = scratch_alloc(nv * 2, st);
-    if (!v16) return cuda_fail(cudaGetLastError());
-    const int rcv = convert_v(v, v16, nv, status, st);
+    k16 = scratch_alloc(nv * 2, st);
+    if (!k16) return cuda_fail(cudaGetLastError());
+    const int rcv = convert_v(k, k16, nv, status, st);
     if (rcv != FA_OK) {
-      cudaFreeAsync(v16, st);
+      cudaFreeAsync(k16, st);
       return rcv;
     }
   }
@@ -373,12 +378,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     ~ScratchGuard() {
       if (ptr) cudaFreeAsync(ptr, st);
     }
-  } guard{fp16 ? nullptr : v16, st};
-  if (topk_idx)
-    return run_topk(q, v16, o, lse, B, Hq, Sq, Skv, scale, mask_mode, seqlens, topk_idx,
-                    rescale_threshold, status, st);
-  return run_tiled(q, k, v16, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
-                   kv_block_idx, rescale_threshold, status, st);
+  } guard{fp16 ? nullptr : k16, st};
+  return run_topk(q, k16, o, lse, B, Hq, Sq, Skv, scale, mask_mode, seqlens, topk_idx,
+                  rescale_threshold, status, st);
 }
 
 // Device address of g_noalloc_scratch for the current device.  In host code the
@@ -409,27 +411,26 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* 
   const int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
                           kv_block_idx, topk_idx, rescale_threshold);
   if (rc != FA_OK) return rc;
-  const bool fp16 = (mask_mode & (FA_DTYPE_FP16 | FA_V_FP16)) != 0;   // V already fp16
-  const size_t nv = topk_idx ? (size_t)B * Skv * D : (size_t)B * Hkv * Skv * Dv;
-  if (!fp16 && nv * 2 > kNoAllocScratchBytes) return FA_ERR_SCRATCH;
-  if (topk_idx) v = k;
+  const bool fp16 = (mask_mode & (FA_DTYPE_FP16 | FA_V_FP16)) != 0;   // latent already fp16
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* status = status_ptr();
   if (!status) return cuda_fail(cudaGetLastError());
-  void* v16 = const_cast<void*>(v);
+  if (!topk_idx)   // no scratch: a bf16 V is converted inside the tiled kernel
+    return run_tiled(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
+                     kv_block_idx, rescale_threshold, status, st);
+  const size_t nv = (size_t)B * Skv * D;
+  if (!fp16 && nv * 2 > kNoAllocScratchBytes) return FA_ERR_SCRATCH;
+  void* k16 = const_cast<void*>(k);
   if (!fp16) {
-    // bf16 V -> fp16 into the fixed scratch (every element is overwritten, so
-    // nothing needs clearing first)
-    v16 = noalloc_scratch_address();
-    if (!v16) return FA_ERR_CUDA;
-    const int rcv = convert_v(v, v16, nv, status, st);
+    // bf16 key latent -> fp16 into the fixed scratch (every element is
+    // overwritten, so nothing needs clearing first)
+    k16 = noalloc_scratch_address();
+    if (!k16) return FA_ERR_CUDA;
+    const int rcv = convert_v(k, k16, nv, status, st);
     if (rcv != FA_OK) return rcv;
   }
-  if (topk_idx)
-    return run_topk(q, v16, o, lse, B, Hq, Sq, Skv, scale, mask_mode, seqlens, topk_idx,
-                    rescale_threshold, status, st);
-  return run_tiled(q, k, v16, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
-                   kv_block_idx, rescale_threshold, status, st);
+  return run_topk(q, k16, o, lse, B, Hq, Sq, Skv, scale, mask_mode, seqlens, topk_idx,
+                  rescale_threshold, status, st);
 }
 
 int fa_convert_v_fp16(const void* v_bf16, void* v_fp16, int64_t n_elems, void* stream) {
@@ -471,7 +472,7 @@ const char* fa_strerror(int code) {
     case FA_ERR_CUDA: return "CUDA call failed";
     case FA_ERR_DEVICE_TIMEOUT: return "bounded on-chip wait expired";
     case FA_ERR_RANGE: return "bf16 V value outside the fp16 range";
-    case FA_ERR_SCRATCH: return "bf16 V larger than the fixed scratch of fa_fwd_noalloc (32 MiB fp16)";
+    case FA_ERR_SCRATCH: return "bf16 key latent larger than the fixed scratch of fa_fwd_noalloc (32 MiB fp16)";
     default: return "unknown error code";
   }
 }

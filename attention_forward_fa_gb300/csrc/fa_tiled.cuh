@@ -7,14 +7,15 @@
 //   warps 0-3   softmax of slot 0 (one thread per query row), including the
 //               correction O *= exp2(m_old - m_new) of its rows when the max moves
 //   warps 4-7   softmax of slot 1
-//   warps 8-11  epilogue (O / l, LSE) of both slots
+//   warps 8-11  V converter during the tile loop (bf16 V), then the epilogue
+//               (O / l, LSE) of both slots
 //   warp  12    TMA producer: Q tiles, then K / V tiles into a ring of stages
 //   warp  13    TMEM allocator and tcgen05.mma issuer
 //   warp  14    MMA scheduler: waits on the mbarriers of the next MMA groups and
 //               releases them to warp 13 through named barriers
-// Q and K are bf16 or fp16; V is always fp16 here (bf16 V is converted to fp16
-// once per call by fa_convert_v_kernel), so that P and V share the fp16 type of
-// the P.V product.
+// Q and K are bf16 or fp16; the P.V product reads fp16 V (P and V share the
+// fp16 type): a bf16 V is converted in shared memory by warps 8-11 as its tiles
+// arrive (kConvV), or was converted beforehand by the caller.
 // The softmax warpgroups raise their register budget with setmaxnreg; the
 // other two lower theirs.
 //
@@ -117,8 +118,8 @@ struct TiledSmem {
   static constexpr int kRowOff = kListOff + 2 * kMaxSel * 4;   // m[2][128], l[2][128]
   static constexpr int kBarOff = kRowOff + 2 * 2 * kBM * 4;
   // barriers: q_full[2], full[NS], empty[NS], s_full[2], p_full[2], o_ready[2],
-  // drain, sm_done[2]
-  static constexpr int kNumBars = 2 + 2 * NS + 6 + 1 + 2;
+  // drain, sm_done[2], ready[NS] (a load passed the V converter)
+  static constexpr int kNumBars = 2 + 2 * NS + 6 + 1 + 2 + NS;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;   // tmem base, abort flag, slot info
   static constexpr int kBytes = kMiscOff + 64;
   static constexpr int kAlloc = kBytes + 1024;              // slack for 1024-byte alignment
@@ -187,7 +188,9 @@ __device__ __forceinline__ Event event_at(int e, int n0, int n1, bool shared) {
   return ev;
 }
 
-template <int D, bool kBF16, int NS>
+// kConvV: V arrives as bf16 and the epilogue warpgroup, idle during the tile
+// loop, converts each V tile to fp16 in shared memory before the MMA reads it.
+template <int D, bool kBF16, int NS, bool kConvV>
 __global__ void __launch_bounds__(kTiledThreads, 1)
     fa_fwd_tiled_kernel(const __grid_constant__ TiledParams p) {
   using SM = TiledSmem<D, NS>;
@@ -215,6 +218,9 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   auto BAR_OREADY = [=](int t) { return bar0 + 8u * (6 + 2 * NS + t); };
   const uint32_t BAR_DRAIN = bar0 + 8u * (8 + 2 * NS);
   auto BAR_SMDONE = [=](int t) { return bar0 + 8u * (9 + 2 * NS + t); };
+  // with kConvV every ring load passes the converter (V tiles converted, K
+  // tiles untouched) and the MMA side waits here instead of on BAR_FULL
+  auto BAR_READY = [=](int s) { return kConvV ? bar0 + 8u * (11 + 2 * NS + s) : bar0 + 8u * (2 + s); };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + SM::kMiscOff);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + SM::kMiscOff + 4);
   int* s_slot = reinterpret_cast<int*>(smem + SM::kMiscOff + 8);   // [2] n, [2] hilo
@@ -262,6 +268,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     for (int s = 0; s < NS; ++s) {
       mbar_init(BAR_FULL(s), 1);
       mbar_init(BAR_EMPTY(s), 1);
+      if (kConvV) mbar_init(BAR_READY(s), 4);   // one arrival per converter warp
     }
     mbar_init(BAR_DRAIN, 1);
     *s_abort = 0;
@@ -489,9 +496,45 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     s_l[t * kBM + row] = l;
     mbar_arrive(BAR_SMDONE(t));
   } else if (warp < 12) {
-    // ============================================================ epilogue
+    // ============================================================ V converter, then epilogue
     regs_dec<kCorrRegs>();
     FA_TR_ROLE(2);
+    if constexpr (kConvV) {
+      // Every ring load in the producer's order: wait until it landed; a V tile
+      // is converted bf16 -> fp16 in place (exact for 2^-14 <= |v| <= 65504;
+      // larger magnitudes become inf and set the range bit), then the load is
+      // released to the MMA side.
+      int ld = 0;
+      bool dead = false;
+      uint32_t vmax = 0;
+      const int ne = num_events(n0, n1);
+      for (int e = 0; e < ne; ++e) {
+        const Event ev = event_at(e, n0, n1, shared_kv);
+        if (!ev.valid || !ev.load) continue;
+        const int s = ld % NS;
+        const uint32_t f = ld / NS;
+        ++ld;
+        if (!dead && !__all_sync(0xffffffffu, wait_bar(BAR_FULL(s), f & 1, wc))) dead = true;
+        if (!dead && ev.pv) {
+          uint4* tile = reinterpret_cast<uint4*>(smem + SM::kStageOff + s * SM::kStageBytes);
+#pragma unroll 4
+          for (int i = tid - 256; i < SM::kStageBytes / 16; i += 128) {
+            uint4 w = tile[i];
+            uint32_t* ww = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              vmax = max_u16x2(vmax, ww[q] & 0x7FFF7FFFu);
+              ww[q] = pack_f16x2(__uint_as_float(ww[q] << 16), __uint_as_float(ww[q] & 0xFFFF0000u));
+            }
+            tile[i] = w;
+          }
+          fence_proxy_async_smem();   // generic-proxy writes -> tensor core reads
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR_READY(s));
+      }
+      if ((vmax & 0xFFFFu) > 0x477Fu || (vmax >> 16) > 0x477Fu) atomicOr(p.status, kStatusRange);
+    }
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
 #pragma unroll 1
@@ -633,8 +676,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       if (!issuer) {
         if (g >= 2) named_sync(3 + (g & 1), 64);      // issuer finished group g-2
         if (lane == 0 && !aborted) {
-          if (pv_load && !wait_bar(BAR_FULL(sv_), (lpv / NS) & 1, wc)) aborted = true;
-          if (!aborted && qk_load && !wait_bar(BAR_FULL(sk_), (lqk / NS) & 1, wc)) aborted = true;
+          if (pv_load && !wait_bar(BAR_READY(sv_), (lpv / NS) & 1, wc)) aborted = true;
+          if (!aborted && qk_load && !wait_bar(BAR_READY(sk_), (lqk / NS) & 1, wc)) aborted = true;
           if (!aborted && qk_valid && jqk == 0 && !wait_bar(BAR_QFULL(t), 0, wc)) aborted = true;
         }
         aborted = __shfl_sync(0xffffffffu, aborted, 0);

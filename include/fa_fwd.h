@@ -35,10 +35,12 @@
  *     NULL = the legacy default stream).  Argument errors are returned
  *     synchronously and nothing is launched.  Device-side errors are
  *     reported later through fa_check_status().
- *   - fa_fwd with bf16 inputs converts V to fp16 into stream-ordered scratch
- *     (cudaMallocAsync from the device's default memory pool, released on
- *     `stream` after use); it allocates nothing else.  fa_fwd_noalloc
- *     allocates nothing at all.
+ *   - The dense / GQA / block-sparse paths allocate nothing (a bf16 V is
+ *     converted to fp16 tile by tile inside the kernel).  The top-k path with
+ *     a bf16 key latent converts the latent to fp16 into stream-ordered
+ *     scratch (cudaMallocAsync from the device's default memory pool,
+ *     released on `stream` after use); fa_fwd_noalloc uses a fixed array
+ *     instead and allocates nothing at all.
  */
 #ifndef FA_FWD_H_
 #define FA_FWD_H_
@@ -59,10 +61,12 @@ extern "C" {
 #define FA_ERR_THRESHOLD       -5  /* rescale_threshold outside [0, 15] or not finite */
 #define FA_ERR_CUDA            -6  /* a CUDA call failed; see fa_last_cuda_error()    */
 #define FA_ERR_DEVICE_TIMEOUT  -7  /* a bounded on-chip wait expired (kernel bailed)  */
-#define FA_ERR_RANGE           -8  /* a bf16 V value outside the fp16 range (|v| >    */
-                                   /* 65504) met the fp16 P.V product                 */
-#define FA_ERR_SCRATCH         -9  /* fa_fwd_noalloc: bf16 V needs more than its     */
-                                   /* fixed scratch (B*Hkv*Skv*Dv*2 > 32 MiB)         */
+#define FA_ERR_RANGE           -8  /* a bf16 value outside the fp16 range (|x| >      */
+                                   /* 65504) met an fp16 product (V; with top-k also  */
+                                   /* Q and the key latent)                           */
+#define FA_ERR_SCRATCH         -9  /* fa_fwd_noalloc, top-k: the bf16 key latent     */
+                                   /* needs more than its fixed scratch               */
+                                   /* (B*Skv*D*2 > 32 MiB)                            */
 
 /* ---- mask_mode flag word ----------------------------------------------- */
 /* bits 0-3: mask */
@@ -75,8 +79,9 @@ extern "C" {
 /* top-k only: V is the first Dv columns of every K row (shared MLA latent);   */
 /* `v` may then be NULL */
 #define FA_V_FROM_K          0x200
-/* bf16 q / k / o with an fp16 `v` converted beforehand by fa_convert_v_fp16  */
-/* (e.g. once for a KV cache read by many calls): skips the in-call copy */
+/* bf16 q / o with an fp16 copy of the value operand made beforehand by      */
+/* fa_convert_v_fp16 (e.g. once for a KV cache read by many calls): `v`, or   */
+/* with FA_V_FROM_K the key latent `k`, is fp16; skips the conversion */
 #define FA_V_FP16            0x400
 
 /* ---- sparse descriptors ------------------------------------------------ */
@@ -153,15 +158,16 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  * For callers that cannot let a library allocate device memory: programs that
  * hand out all device memory from their own fixed arena and account for every
  * byte, and latency-critical call sites where a driver allocation (and the
- * synchronisation it may imply) is not acceptable.  fa_fwd converts a bf16 V
- * to fp16 in stream-ordered scratch taken from the device's memory pool; this
- * entry point uses a fixed array inside the library's device image instead
- * (32 MiB, held by every device that loads the library until the process
- * exits) and calls no cudaMalloc, cudaFree or other allocating routine.
+ * synchronisation it may imply) is not acceptable.  fa_fwd's top-k path
+ * converts a bf16 key latent to fp16 in stream-ordered scratch taken from the
+ * device's memory pool; this entry point uses a fixed array inside the
+ * library's device image instead (32 MiB, held by every device that loads the
+ * library until the process exits) and calls no cudaMalloc, cudaFree or other
+ * allocating routine.  (The other paths allocate nothing in either entry.)
  *
  * Same arguments, layouts and results as fa_fwd.  Differences:
- *   - bf16 inputs with B*Hkv*Skv*Dv*2 bytes > 32 MiB are rejected with
- *     FA_ERR_SCRATCH (fp16 inputs need no scratch and have no such limit);
+ *   - top-k calls with a bf16 key latent of B*Skv*D*2 bytes > 32 MiB are
+ *     rejected with FA_ERR_SCRATCH (fp16 latents need no scratch);
  *   - the first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
  *     stream capture;
@@ -179,8 +185,9 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* 
  * fa_convert_v_fp16 -- fp16 copy of a bf16 tensor (the V operand).
  *
  * The P.V product runs on fp16 operands (fp16 keeps three more mantissa bits
- * of the probabilities than bf16); fa_fwd converts a bf16 V itself, or takes
- * this copy with FA_V_FP16.  v_bf16 and v_fp16 are device pointers, 16-byte
+ * of the probabilities than bf16); fa_fwd converts a bf16 V itself (inside
+ * the kernel; the top-k latent into scratch), or takes this copy with
+ * FA_V_FP16.  v_bf16 and v_fp16 are device pointers, 16-byte
  * aligned, n_elems a positive multiple of 8.  bf16 -> fp16 is exact for
  * 2^-14 <= |v| <= 65504; larger magnitudes become inf and are reported as
  * FA_ERR_RANGE by fa_check_status.  Asynchronous on `stream`.

@@ -1,8 +1,10 @@
 """fa_fwd_noalloc: the entry point for callers that cannot let a library
 allocate device memory (programs that hand out all device memory from their
 own arena, latency-critical call sites where a driver allocation is not
-acceptable).  It uses a fixed 32 MiB array inside the library instead of
-stream-ordered scratch; its results must equal fa_fwd's on the same inputs,
+acceptable).  The dense, GQA and block-sparse paths allocate nothing anyway
+(a bf16 V is converted inside the kernel); the top-k path's fp16 copy of the
+bf16 key latent goes to a fixed 32 MiB array inside the library instead of
+stream-ordered scratch.  Results must equal fa_fwd's on the same inputs,
 including on a second call, which finds the previous call's data still in the
 shared array.
 
@@ -14,10 +16,15 @@ import pytest
 pytestmark = pytest.mark.gpu
 
 
-def _problem(seed, dtype="bf16"):
+def _dense(seed, dtype="bf16"):
     from attention_forward_fa_gb300 import workloads as W
     return W.dense(name=f"noalloc{seed}", B=2, Hq=4, Hkv=2, Sq=700, D=128, dtype=dtype,
                    mask=W.MASK_CAUSAL, seqlens=[700, 333], seed=seed)
+
+
+def _mla(seed, dtype="bf16"):
+    from attention_forward_fa_gb300 import workloads as W
+    return W.sparse_mla(name=f"noalloc_mla{seed}", T=300, W=320, seed=seed, dtype=dtype)
 
 
 def _run(entry, p):
@@ -26,8 +33,12 @@ def _run(entry, p):
     d = to_device(p)
     o = torch.empty((p.B, p.Hq, p.Sq, p.Dv), dtype=d["q"].dtype, device="cuda")
     lse = torch.empty((p.B, p.Hq, p.Sq), dtype=torch.float32, device="cuda")
-    code = entry(d["q"], d["k"], d["v"], o, lse, p.B, p.Hq, p.Hkv, p.Sq, p.Skv, p.D, p.Dv,
-                 p.scale, p.mask_mode, d["seqlens"], None, None, 0.0)
+    tk = None
+    if d["topk_idx"] is not None:
+        ti = d["topk_idx"]
+        tk = (ti, ti.shape[-1], ti.shape[-2] * ti.shape[-1])
+    code = entry(d["q"], d["k"], None if p.v_from_k else d["v"], o, lse, p.B, p.Hq, p.Hkv, p.Sq,
+                 p.Skv, p.D, p.Dv, p.scale, p.mask_mode, d["seqlens"], None, tk, 0.0)
     assert code == 0
     import attention_forward_fa_gb300 as fa
     assert fa.fa_check_status() == 0
@@ -40,20 +51,22 @@ def test_noalloc_matches_fa_fwd_on_two_calls_in_a_row():
     build.build()
     import attention_forward_fa_gb300 as fa
     from tests.parity import compare
-    for seed, dtype in ((31, "bf16"), (32, "bf16"), (33, "fp16")):
-        p = _problem(seed, dtype)
+    cases = [_dense(31), _dense(32), _dense(33, "fp16"), _mla(34), _mla(35), _mla(36, "fp16")]
+    for p in cases:
         O_ref, L_ref = _run(fa.fa_fwd, p)
         O, L = _run(fa.fa_fwd_noalloc, p)
-        compare(O, L, O_ref, L_ref, where=f"noalloc vs fa_fwd, seed {seed}")
+        compare(O, L, O_ref, L_ref, where=f"noalloc vs fa_fwd, {p.name}")
 
 
-def test_noalloc_rejects_v_beyond_its_scratch():
-    """bf16 V of more than 32 MiB (fp16 copy) is refused before anything runs."""
+def test_noalloc_rejects_a_latent_beyond_its_scratch():
+    """A bf16 key latent whose fp16 copy exceeds 32 MiB is refused before
+    anything runs."""
     import attention_forward_fa_gb300 as fa
     import torch
-    P = 0x10000   # aligned stand-in addresses: validation fails before any use
-    B, Hkv, Skv, Dv = 1, 8, 16384, 128   # 16M elements -> 32 MiB fp16 + 1 row more
-    code = fa.fa_fwd_noalloc(P, P, P, P, P, B, Hkv, Hkv, 128, Skv + 1, 128, Dv, 0.1, 0,
-                             None, None, None, 0.0, torch.cuda.current_stream())
+    P = 0x10000   # aligned stand-in addresses: the size check fails before any use
+    Skv = 29128   # 29128 * 576 * 2 bytes > 32 MiB
+    code = fa.fa_fwd_noalloc(P, P, None, P, P, 1, 128, 1, 128, Skv, 576, 512, 0.1,
+                             fa.FA_V_FROM_K, None, None, (P, 2048, 0), 0.0,
+                             torch.cuda.current_stream())
     assert code == -9
     assert "scratch" in fa.fa_strerror(code)
