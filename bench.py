@@ -287,22 +287,24 @@ def run_ours(args, world, rank, local):
     # One step = the whole hot path: one fa_fwd launch, plus for a bf16 top-k
     # latent the conversion pass before it (issued through the C ABI on its own
     # so that the attention kernel can be timed alone).
-    def step(i, ev=None):
+    def step(i, ev=None, strm=None):
+        strm = strm or stream
+        ssp = strm.cuda_stream
         q, k, v, c16, o, lse = sets[i % n_sets]
         if ev:
-            ev[0].record(stream)
+            ev[0].record(strm)
         if conv_pass:
-            code = fa.fa_convert_v_fp16(k, c16, n_conv, sp)
+            code = fa.fa_convert_v_fp16(k, c16, n_conv, ssp)
             if code != 0:
                 raise RuntimeError(fa.fa_strerror(code))
         if ev:
-            ev[1].record(stream)
+            ev[1].record(strm)
         code = fa.fa_fwd(q, c16 if conv_pass else k, v, o, lse, p.B, p.Hq, p.Hkv, p.Sq, p.Skv,
-                         p.D, p.Dv, p.scale, mode, seqlens, blk, tk, 0.0, sp)
+                         p.D, p.Dv, p.scale, mode, seqlens, blk, tk, 0.0, ssp)
         if code != 0:
             raise RuntimeError(fa.fa_strerror(code))
         if ev:
-            ev[2].record(stream)
+            ev[2].record(strm)
 
     # warm-up, then an untimed soak so that clocks are sampled under load
     for i in range(args.warmup):
@@ -318,16 +320,38 @@ def run_ours(args, world, rank, local):
             step(i)
             i += 1
         torch.cuda.synchronize()
-    # timed region: exactly K steps, events around each launch
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # Timed region: exactly K steps.  A step that is one launch (every workload
+    # but a bf16 top-k latent) runs as a CUDA graph of the K launches, captured
+    # beforehand: the events around the replay then time K launches of that one
+    # kernel, so its average launch duration is the step time.  A two-launch
+    # step runs eagerly with events around each launch.
+    use_graph = not conv_pass and not args.no_graph
+    evs = None
+    graph = None
+    if use_graph:
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            step(0, strm=cap)
+            cap.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=cap):
+                for s_ in range(args.steps):
+                    step(s_, strm=cap)
+        torch.cuda.synchronize()
+    else:
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     t_all0 = torch.cuda.Event(enable_timing=True)
     t_all1 = torch.cuda.Event(enable_timing=True)
     t_all0.record(stream)
-    for s_ in range(args.steps):
-        step(s_, evs[s_])
+    if use_graph:
+        graph.replay()
+    else:
+        for s_ in range(args.steps):
+            step(s_, evs[s_])
     t_all1.record(stream)
     torch.cuda.synchronize()
     if dist:
@@ -337,10 +361,14 @@ def run_ours(args, world, rank, local):
     if status != 0:
         raise RuntimeError("device status after timed region: " + fa.fa_strerror(status))
     total_ms = t_all0.elapsed_time(t_all1)
-    kern_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    conv_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    kern_avg_ms = sum(kern_ms) / len(kern_ms)
-    conv_avg_ms = sum(conv_ms) / len(conv_ms)
+    if use_graph:
+        kern_avg_ms = total_ms / args.steps
+        conv_avg_ms = 0.0
+    else:
+        kern_ms = [e[1].elapsed_time(e[2]) for e in evs]
+        conv_ms = [e[0].elapsed_time(e[1]) for e in evs]
+        kern_avg_ms = sum(kern_ms) / len(kern_ms)
+        conv_avg_ms = sum(conv_ms) / len(conv_ms)
     if dist:
         t = torch.tensor([total_ms, kern_avg_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -397,7 +425,10 @@ def run_ours(args, world, rank, local):
     peak = float(peaks["bf16_tflops"])
     achieved = flops / (kern_avg_ms * 1e-3) / 1e12
     cfg = workload_desc(p, args.workload)
-    cfg.update({"parallelism": f"replicas x{world} (no exchange)",
+    cfg.update({"timing": ("CUDA graph of the K steps (captured before the timed region), "
+                           "events around its replay" if use_graph else
+                           "eager launches, CUDA events around each launch"),
+                "parallelism": f"replicas x{world} (no exchange)",
                 "l2": f"{n_sets} rotating input/output sets of {per_set / 2**20:.0f} MiB "
                       f"(> 2 x 129 MiB L2), no flush",
                 "algorithmic_gflop_per_step": flops / 1e9})
@@ -445,6 +476,8 @@ def main():
     ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed load before timing")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the timed steps eagerly with events around each launch")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c2",
                     help="c2 (default) is the benchmark line; the others time the same path "
                          "on the other workloads")
