@@ -160,3 +160,20 @@ def test_preconverted_fp16_v_equals_in_call_conversion():
     assert fa.fa_check_status() == 0
     assert np.array_equal(o.float().cpu().double().numpy(), O1)
     assert np.array_equal(lse.cpu().double().numpy(), L1)
+
+
+def test_bf16_v_beyond_fp16_range_is_reported():
+    """A bf16 V value above 65504 cannot enter the fp16 P.V product: the call
+    completes and fa_check_status reports FA_ERR_RANGE once, then clears."""
+    import torch
+    import attention_forward_fa_gb300 as fa
+    p = W.dense(name="range", B=1, Hq=2, Sq=256, D=128, mask=W.MASK_CAUSAL, seed=27)
+    d = to_device(p)
+    d["v"][0, 1, 77, 5] = 70000.0
+    o = torch.empty((p.B, p.Hq, p.Sq, p.Dv), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((p.B, p.Hq, p.Sq), dtype=torch.float32, device="cuda")
+    assert fa.fa_check_status() == 0
+    assert fa.fa_fwd(d["q"], d["k"], d["v"], o, lse, p.B, p.Hq, p.Hkv, p.Sq, p.Skv, p.D, p.Dv,
+                     p.scale, p.mask) == 0
+    assert fa.fa_check_status() == -8
+    assert fa.fa_check_status() == 0

@@ -137,3 +137,22 @@ def test_config5_full_size_sampled(threshold, reverse):
     floor = M.bf16_row_gain_floor(Or)
     if threshold == 0.0:
         assert gain <= 2.0 * floor, (gain, floor)
+
+
+def test_bf16_query_beyond_fp16_range_is_reported():
+    """Q.K^T of the top-k path runs on fp16 copies: a bf16 query value above
+    65504 is reported as FA_ERR_RANGE (once), like an out-of-range latent."""
+    import torch
+    import attention_forward_fa_gb300 as fa
+    p = W.sparse_mla(name="mla_range", T=130, W=160, seed=49)
+    d = to_device(p)
+    d["q"][0, 3, 100, 17] = -80000.0
+    assert fa.fa_check_status() == 0
+    o, lse = fa.flash_attention_forward(d["q"], d["k"], None, scale=p.scale,
+                                        topk_idx=d["topk_idx"])
+    assert fa.fa_check_status() == -8
+    d["k"][0, 0, 5, 3] = 66000.0
+    fa.flash_attention_forward(d["q"][:, :, :1].contiguous(), d["k"], None, scale=p.scale,
+                               topk_idx=d["topk_idx"][:, :1].contiguous())
+    assert fa.fa_check_status() == -8
+    assert fa.fa_check_status() == 0
