@@ -127,8 +127,10 @@ WORKLOADS = {
 }
 
 
-def workload_problem(name="c2"):
+def workload_problem(name="c2", mla_tokens=4096):
     from attention_forward_fa_gb300 import workloads as W
+    if name == "c5" and mla_tokens != 4096:
+        return W.sparse_mla(name=f"sparse_mla_T{mla_tokens}", T=mla_tokens, seed=1005)
     return W.config(WORKLOADS[name][0])
 
 
@@ -140,6 +142,8 @@ def workload_desc(p, name="c2"):
          "Skv": p.Skv, "D": p.D, "Dv": p.Dv, "mask": mask, "rescale_threshold": 0.0}
     if p.topk_idx is not None:
         d["topk"] = int(p.topk_idx.shape[-1])
+        if p.Sq != 4096:
+            d["workload"] = d["workload"].replace("T=4096", f"T={p.Sq}")
     return d
 
 
@@ -238,7 +242,7 @@ def run_ours(args, world, rank, local):
         dist.barrier()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    p = workload_problem(args.workload)
+    p = workload_problem(args.workload, args.mla_tokens)
     flops = W.algorithmic_flops(p)
     bf16 = p.dtype == "bf16"
     dt = torch.bfloat16 if bf16 else torch.float16
@@ -476,6 +480,8 @@ def main():
     ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed load before timing")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mla-tokens", type=int, default=4096,
+                    help="tokens of the top-k workload (c5); smaller values for profiling captures")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps eagerly with events around each launch")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c2",
