@@ -155,6 +155,16 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, long lo
   }
 }
 
+// KV tiles of a dense (not block-sparse) query tile: up to the causal bound
+// and the batch's length; 0 for a tile past the query length.
+__device__ __forceinline__ int dense_tiles(int qt, int n_qt, int q_len, int kv_len, int mask) {
+  const int q0 = qt * kBM;
+  if (qt >= n_qt || q0 >= q_len || kv_len <= 0) return 0;
+  int nkv = (kv_len + kBN - 1) / kBN;
+  if (mask == 1) nkv = min(nkv, min(q0 + kBM - 1, q_len - 1) / kBN + 1);
+  return nkv;
+}
+
 // The order in which the MMA warp consumes K / V tiles, as a numbered event
 // list: 0 = QK(0,0), 1 = QK(1,0), then per iteration j four events PV(0,j),
 // QK(0,j+1), PV(1,j), QK(1,j+1).  `load` marks the first use of a tile (a
@@ -257,7 +267,12 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     FA_TR_ROLE(6);
     if (tid == 0) FA_TR(12, 0, 0);
   }
-  if (tid == 0) {
+  // The producer thread initialises the barriers and, for dense units, starts
+  // the first loads (Q of slot 0, the first K tile, Q of slot 1) before the
+  // CTA-wide setup barrier: at a wave's start every CTA loads at once.
+  int early = 0;          // producer: ring loads already issued
+  bool q_early[2] = {false, false};
+  if (warp == 12 && lane == 0) {
     for (int t = 0; t < 2; ++t) {
       mbar_init(BAR_QFULL(t), 1);
       mbar_init(BAR_SFULL(t), 1);
@@ -273,6 +288,29 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     mbar_init(BAR_DRAIN, 1);
     *s_abort = 0;
     fence_mbar_init();
+    tma_prefetch_desc(&p.tm_q);
+    tma_prefetch_desc(&p.tm_k);
+    tma_prefetch_desc(&p.tm_v);
+    if (!sparse) {
+      const int e0 = dense_tiles(qt0, p.n_qt, q_len, kv_len, p.mask);
+      const int e1 = dense_tiles(qt1, p.n_qt, q_len, kv_len, p.mask);
+      for (int t = 0; t < 2; ++t) {
+        if ((t ? e1 : e0) == 0) continue;
+        mbar_arrive_expect_tx(BAR_QFULL(t), SM::kQBytes);
+        for (int bx = 0; bx < kBoxes; ++bx)
+          tma_load_3d(sQ + t * SM::kQBytes + bx * (kBM * 128), &p.tm_q, BAR_QFULL(t), 64 * bx,
+                      (t ? qt1 : qt0) * kBM, b * p.Hq + (t ? h1 : h0));
+        q_early[t] = true;
+        if (t == 0) {
+          // the first ring load is K tile 0 for Q.K^T(0,0) in every event order
+          mbar_arrive_expect_tx(BAR_FULL(0), SM::kStageBytes);
+          for (int bx = 0; bx < kBoxes; ++bx)
+            tma_load_3d(sStage + bx * (kBN * 128), &p.tm_k, BAR_FULL(0), 64 * bx, 0,
+                        b * p.Hkv + kvh);
+          early = 1;
+        }
+      }
+    }
   }
   if (warp == 13) {
     tmem_alloc(smem_u32(s_tmem), 512);
@@ -592,11 +630,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     regs_dec<kOtherRegs>();
     FA_TR_ROLE(3);
     if (lane == 0) {
-      tma_prefetch_desc(&p.tm_q);
-      tma_prefetch_desc(&p.tm_k);
-      tma_prefetch_desc(&p.tm_v);
       for (int t = 0; t < 2; ++t) {
-        if ((t ? n1 : n0) == 0) continue;
+        if ((t ? n1 : n0) == 0 || q_early[t]) continue;
         mbar_arrive_expect_tx(BAR_QFULL(t), SM::kQBytes);
         for (int bx = 0; bx < kBoxes; ++bx)
           tma_load_3d(sQ + t * SM::kQBytes + bx * (kBM * 128), &p.tm_q, BAR_QFULL(t), 64 * bx,
@@ -610,6 +645,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         const int s = ld % NS;
         const uint32_t f = ld / NS;
         ++ld;
+        if (ld <= early) continue;   // issued before the setup barrier
         if (!wait_bar(BAR_EMPTY(s), (f & 1) ^ 1, wc)) break;
         const int kvt = sparse ? s_list[ev.t * kMaxSel + ev.j] : ev.j;
         FA_TR(5, ev.t, ev.j);
