@@ -57,7 +57,7 @@ constexpr int kBarPReady = 5;
 enum : int { kStatusTimeout = 1, kStatusRange = 2 };
 
 struct TiledParams {
-  CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;
   void* o;
   float* lse;
   const int* seqlens;
@@ -593,38 +593,51 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       const float l = acc ? s_l[t * kBM + row] : 0.f;
       const float m = acc ? s_m[t * kBM + row] : 0.f;
       const bool write = qi < p.Sq;
-      uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + ((size_t)(b * p.Hq + h) * p.Sq + qi) * Dv;
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       const uint32_t tO = tmem + 256u + 128u * t + lane_off;
-#pragma unroll
-      for (int cc = 0; cc < Dv / 32; ++cc) {
-        uint32_t r[32];
+      // O / l into the slot's Q buffer (its last Q.K^T finished before the last
+      // P.V) in the 128-byte-swizzle layout of the output's tensor map, then one
+      // thread stores the tile with TMA (rows past Sq are clipped)
+      uint8_t* stage_o = smem + SM::kQOff + t * SM::kQBytes + row * 128;
+      const int sw = row & 7;
+#pragma unroll 2
+      for (int cc = 0; cc < Dv / 16; ++cc) {
+        uint32_t r[16];
         if (acc) {
-          tmem_ld32(tO + 32 * cc, r);   // warp-collective: all lanes, even rows past Sq
+          tmem_ld16(tO + 16 * cc, r);   // warp-collective: all lanes, even rows past Sq
           tmem_wait_ld();
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = 0;
+          for (int i = 0; i < 16; ++i) r[i] = 0;
         }
-        if (write) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cc);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint32_t w[4];
+        for (int i = 0; i < 2; ++i) {
+          uint32_t w[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float a0 = __uint_as_float(r[8 * i + 2 * e]) * inv_l;
-              const float a1 = __uint_as_float(r[8 * i + 2 * e + 1]) * inv_l;
-              w[e] = kBF16 ? pack_bf16x2(a0, a1) : pack_f16x2(a0, a1);
-            }
-            dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int e = 0; e < 4; ++e) {
+            const float a0 = __uint_as_float(r[8 * i + 2 * e]) * inv_l;
+            const float a1 = __uint_as_float(r[8 * i + 2 * e + 1]) * inv_l;
+            w[e] = kBF16 ? pack_bf16x2(a0, a1) : pack_f16x2(a0, a1);
           }
+          const int chunk = (cc & 3) * 2 + i;   // 16-byte chunk within the 64-column box
+          *reinterpret_cast<uint4*>(stage_o + (cc >> 2) * (kBM * 128) + ((chunk ^ sw) << 4)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
         }
+      }
+      fence_proxy_async_smem();
+      named_sync(7, kBM);   // the four epilogue warps
+      if (warp == 8 && lane == 0) {
+        for (int bx = 0; bx < kBoxes; ++bx)
+          tma_store_3d(&p.tm_o, sQ + t * SM::kQBytes + bx * (kBM * 128), 64 * bx, qt * kBM,
+                       b * p.Hq + h);
+        bulk_commit();
       }
       if (write)
         p.lse[(size_t)(b * p.Hq + h) * p.Sq + qi] = (l > 0.f) ? m * p.scale + __logf(l) : INFINITY;
       if (row == 0) FA_TR(11, t, 0);
     }
+    // the tiles' shared memory must outlive the stores' reads
+    if (warp == 8 && lane == 0) bulk_wait_read();
   } else if (warp == 12) {
     // ============================================================ producer
     regs_dec<kOtherRegs>();
