@@ -33,10 +33,17 @@ METRIC = "attention fwd TFLOP/s on 1 GB300 and % of dense BF16 tensor peak; ms/c
 L2_BYTES = 129 * 2 ** 20
 
 
-def kernel_source_hash() -> str:
+KERNEL_SOURCES = {
+    # device code of each kernel: the headers its translation unit pulls in
+    "dense": ("fa_ptx.cuh", "fa_tiled.cuh"),
+    "topk": ("fa_ptx.cuh", "fa_tiled.cuh", "fa_mla.cuh"),
+}
+
+
+def kernel_source_hash(kind: str = "dense") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_forward_fa_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES[kind]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -58,7 +65,8 @@ def dram_traffic(workload: str):
         return None
     d = json.load(open(path))
     e = d.get(workload)
-    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+    kind = "topk" if workload == "c5" else "dense"
+    if not e or e.get("kernel_source_hash") != kernel_source_hash(kind):
         return None
     return e.get("dram_bytes_per_launch")
 
