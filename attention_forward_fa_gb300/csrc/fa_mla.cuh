@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
           float r0, r1, r2, r3;
           f2_unpack(sum2[0], r0, r1);
           f2_unpack(sum2[1], r2, r3);
-          l = alpha * l + ((r0 + r1) + (r2 + r3));
+          l = __fmaf_rn(alpha, l, (r0 + r1) + (r2 + r3));   // (one rounding in every build)
         }
         if (dead) continue;
         // the previous tile's P.V passes have read P and written O
@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     }
     if (write && qtr == 0)
       p.lse[(size_t)(b * p.Hq + h) * p.Sq + t] =
-          (acc && l > 0.f) ? m * p.scale + __logf(l) : INFINITY;
+          (acc && l > 0.f) ? __fmaf_rn(m, p.scale, __logf(l)) : INFINITY;
   } else if (warp < 4 + kMlaNS) {
     // ============================================================ producers
     // Warp 4 + s fills ring stage s: the tiles j with (j + 2) % 3 == s.  Each

@@ -336,11 +336,12 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
-// three-input maximum
+// three-input maximum, as a chain of two-input maxima (the compiler may fuse
+// it): the inline three-input max.f32 returned maxima that were not among its
+// inputs in one build of the softmax (a too-large row max, hidden by the
+// rescale since l and O scale alike, but not in the LSE's last bits)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
+  return fmaxf(fmaxf(a, b), c);
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {

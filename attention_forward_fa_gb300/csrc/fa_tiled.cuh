@@ -498,7 +498,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       float r0, r1, r2, r3;
       f2_unpack(sum2[0], r0, r1);
       f2_unpack(sum2[1], r2, r3);
-      l = alpha * l + ((r0 + r1) + (r2 + r3));
+      l = __fmaf_rn(alpha, l, (r0 + r1) + (r2 + r3));   // (one rounding in every build)
       m = m_use;
       // O_t *= alpha for the rows whose max moved.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -633,7 +633,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         bulk_commit();
       }
       if (write)
-        p.lse[(size_t)(b * p.Hq + h) * p.Sq + qi] = (l > 0.f) ? m * p.scale + __logf(l) : INFINITY;
+        p.lse[(size_t)(b * p.Hq + h) * p.Sq + qi] = (l > 0.f) ? __fmaf_rn(m, p.scale, __logf(l)) : INFINITY;
       if (row == 0) FA_TR(11, t, 0);
     }
     // the tiles' shared memory must outlive the stores' reads
