@@ -156,3 +156,26 @@ def test_bf16_query_beyond_fp16_range_is_reported():
                                topk_idx=d["topk_idx"][:, :1].contiguous())
     assert fa.fa_check_status() == -8
     assert fa.fa_check_status() == 0
+
+
+def test_config5_order_difference_exact_max():
+    """The same problem with its slots in the given and in the reversed order,
+    exact running max: the coherent (whole-row) part of the difference of the
+    two outputs stays under twice its noise floor, elem_rms * sqrt(3 / Dv)
+    ("Sparse-MLA training forward: exact running max vs lazy rescale", cf-1.com,
+    section "Measurement")."""
+    import torch
+    import attention_forward_fa_gb300 as fa
+    outs = []
+    for reverse in (False, True):
+        p = c5(reverse)
+        d = to_device(p)
+        o, _ = fa.flash_attention_forward(d["q"], d["k"], None, scale=p.scale, mask_mode=p.mask,
+                                          topk_idx=d["topk_idx"], rescale_threshold=0.0)
+        assert fa.fa_check_status() == 0
+        sel = torch.from_numpy(TOKENS).to(o.device)
+        outs.append(o[:, :, sel].float().cpu().double().numpy())
+        del o, d
+    Or, _ = oracle_tokens(c5(False), TOKENS)
+    coherent, floor = M.order_difference(outs[0], outs[1], Or)
+    assert coherent < 2.0 * floor, (coherent, floor)
