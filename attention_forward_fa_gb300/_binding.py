@@ -62,6 +62,8 @@ def library() -> ctypes.CDLL:
         lib.fa_check_status.argtypes = [ctypes.c_void_p]
         lib.fa_set_wait_timeout_ns.restype = None
         lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_int64]
+        lib.fa_wait_probe.restype = ctypes.c_int
+        lib.fa_wait_probe.argtypes = [ctypes.c_void_p]
         lib.fa_strerror.restype = ctypes.c_char_p
         lib.fa_strerror.argtypes = [ctypes.c_int]
         lib.fa_last_cuda_error.restype = ctypes.c_int
@@ -143,6 +145,10 @@ def fa_check_status(stream=None) -> int:
 
 def fa_set_wait_timeout_ns(ns: int) -> None:
     library().fa_set_wait_timeout_ns(int(ns))
+
+
+def fa_wait_probe(stream=None) -> int:
+    return library().fa_wait_probe(_stream(stream))
 
 
 def _raise(code: int):

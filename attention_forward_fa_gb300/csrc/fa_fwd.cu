@@ -341,6 +341,22 @@ int run_tiled(const void* q, const void* k, const void* v, void* o, float* lse, 
               : launch_tiled<64, true, 6, false>(prm, (int)units, st);
 }
 
+// One warp waits, with the kernels' bounded wait, on an mbarrier that nothing
+// ever arrives at: the wait gives up after the configured limit and reports
+// the timeout in the status word, and the kernel returns.
+__global__ void fa_wait_probe_kernel(int* status, long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    fa::mbar_init(fa::smem_u32(&bar), 1);
+    abort_flag = 0;
+    fa::fence_mbar_init();
+  }
+  __syncthreads();
+  const fa::WaitCtx wc{reinterpret_cast<volatile int*>(&abort_flag), status, timeout_ns};
+  (void)fa::wait_bar(fa::smem_u32(&bar), 0, wc);
+}
+
 }  // namespace
 
 extern "C" {
@@ -461,6 +477,15 @@ int fa_check_status(void* stream) {
 }
 
 void fa_set_wait_timeout_ns(int64_t ns) { g_timeout_ns.store(ns > 0 ? ns : 2000000000LL); }
+
+int fa_wait_probe(void* stream) {
+  int* status = status_ptr();
+  if (!status) return cuda_fail(cudaGetLastError());
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  fa_wait_probe_kernel<<<1, 32, 0, st>>>(status, g_timeout_ns.load());
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
 
 const char* fa_strerror(int code) {
   switch (code) {

@@ -147,8 +147,13 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, WaitCtx 
     }
   }
 }
-// Bounded wait that ignores the abort flag (teardown: let copies in flight land).
+// Bounded wait that ignores the abort flag (teardown: let copies and MMAs in
+// flight finish before their shared memory or TMEM is released).  It waits at
+// least kDrainNs, whatever the caller's wait limit, since a short limit must
+// not cut a copy's landing short.
+constexpr long long kDrainNs = 100000000;   // 100 ms
 __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, long long timeout) {
+  if (timeout < kDrainNs) timeout = kDrainNs;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if ((long long)(globaltimer_ns() - t0) > timeout) return;
@@ -390,7 +395,15 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     float m = -INFINITY, l = 0.f;
     bool dead = false;   // a bounded wait expired: keep the hand-offs, skip the work
     for (int j = 0; j < nt; ++j) {
-      if (!dead && !__all_sync(0xffffffffu, wait_bar(BAR_SFULL(t), j & 1, wc))) dead = true;
+      if (!dead && !__all_sync(0xffffffffu, wait_bar(BAR_SFULL(t), j & 1, wc))) {
+        dead = true;
+      } else if (dead) {
+        // Paced by the issuer's S commits (a bounded wait past the abort
+        // flag): the issuer commits S of tile j only after its "P ready" wait
+        // for tile j - 1, so these arrivals never run two generations ahead
+        // of it (which would leave it waiting on the hardware barrier).
+        drain_bar(BAR_SFULL(t), j & 1, wc.timeout);
+      }
       if (dead) {
         // the MMA issuer waits for one arrival per tile on a hardware barrier
         named_arrive(kBarPReady + t, kBM + 32);
@@ -586,7 +599,10 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       if (nt > 0) {
         acc = __all_sync(0xffffffffu, wait_bar(BAR_SMDONE(t), 0, wc)) &&
               __all_sync(0xffffffffu, wait_bar(BAR_OREADY(t), 0, wc));   // the last P.V
-        if (!acc) break;
+        // one decision for the four epilogue warps (each reaches this barrier
+        // once per slot), so that none waits at the staging barrier below for
+        // a warp that gave up
+        if (named_or(7, kBM, !acc)) break;
         tc_fence_after();
       }
       if (row == 0) FA_TR(10, t, 0);
@@ -737,7 +753,9 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         // then runs on stale operands, which is harmless: the status word
         // already reports the failure and nothing waits on the results)
         if (pv_valid) {
-          // P_t of tile jpv written by the four softmax warps of slot t
+          // P_t of tile jpv written by the four softmax warps of slot t (a
+          // softmax warp that gave up still arrives once per tile, paced by
+          // the S commits, so this wait always ends)
           named_sync(kBarPReady + t, kBM + 32);
           tc_fence_after();
         }

@@ -204,6 +204,14 @@ int fa_check_status(void* stream);
  * values <= 0 restore the default.  Affects launches made after the call. */
 void fa_set_wait_timeout_ns(int64_t ns);
 
+/* Failure-detection probe: one warp waits, with the same bounded wait as the
+ * attention kernels, on an mbarrier that nothing ever arrives at, so that the
+ * wait runs out after the limit set by fa_set_wait_timeout_ns, sets the
+ * timeout bit of the status word and returns.  The next fa_check_status()
+ * reports FA_ERR_DEVICE_TIMEOUT; the context stays usable.  Asynchronous on
+ * `stream`; FA_OK once launched, FA_ERR_CUDA if the launch failed. */
+int fa_wait_probe(void* stream);
+
 /* Static string for a return code. */
 const char* fa_strerror(int code);
 
