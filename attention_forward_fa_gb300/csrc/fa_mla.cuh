@@ -6,22 +6,29 @@
 // row (Dv = 512): "Sparse-MLA training forward: exact running max vs lazy
 // rescale" (cf-1.com), section "Background: sparse MLA and top-k gathered KV".
 //
-// One CTA per (token, group of 128 query heads, quarter of Dv): the 128 heads
-// are the 128 rows of every MMA.  The fp32 O accumulator of all 512 value
-// columns would fill the whole TMEM, so each CTA keeps a quarter (128
-// columns) and recomputes S = Q K^T for its quarter.  TMEM (512 columns):
-//   [0, 128)    O (this CTA's quarter of Dv), fp32
-//   [128, 192)  S of the current 64-key tile, fp32
-//   [192, 224)  P, fp16 pairs
-//   [224, 512)  Q as fp16 pairs, the A operand of S = Q K^T (576 / 2 columns)
-// K is read from an fp16 copy of the latent (bf16 inputs are converted once per
-// call), so that the same shared-memory tile is the B operand of both
-// products: K-major for Q K^T over all 576 columns, MN-major for P V over this
-// CTA's 128 value columns.  Tiles of 64 gathered rows are copied in 16-byte
-// chunks (cp.async, one producer warp per stage of a three-stage ring; TMA row
-// gathers move far fewer bytes per cycle for 128-byte rows); the Q tile is
-// first staged (bf16 or fp16, via TMA) in ring stages 0-1 and converted to
-// fp16 into TMEM.
+// Two CTAs per (token, group of 128 query heads), one per half of Dv: the 128
+// heads are the 128 rows of every MMA.  The fp32 O accumulator of all 512
+// value columns would fill the whole TMEM, so each CTA keeps half of it and
+// computes S = Q K^T itself.  TMEM (512 columns):
+//   [0, 256)    O (this CTA's half of Dv), fp32
+//   [256, 320)  S of the current 64-key tile, fp32
+//   [320, 352)  P, fp16 pairs
+//   [352, 512)  query columns 0-319 as fp16 pairs (A operand of Q K^T from TMEM)
+// Query columns 320-575 are kept in shared memory as fp16 (A operand of those
+// Q K^T steps from shared memory).  K is read from an fp16 copy of the latent
+// (bf16 inputs are converted once per call), so that one gathered tile is the
+// B operand of both products: K-major for Q K^T over all 576 columns,
+// MN-major for P V over this CTA's 256 value columns.
+//
+// A ring stage holds one tile of 64 gathered rows (nine 64-column boxes).  It
+// has two regions with their own full / empty barriers: V, this CTA's four
+// value boxes (read by Q K^T and P V), and X, the other five boxes (read by
+// Q K^T only).  X is free again once Q K^T of its tile is done, V once its
+// P V is done; Q K^T of the next tile multiplies the X boxes first, which
+// gives the gather of the V boxes the time of those steps.  Three producer
+// warps copy every tile together in 16-byte chunks (cp.async); the Q tile is
+// first staged (bf16 or fp16, via TMA) in both ring stages and converted to
+// fp16 into TMEM and shared memory.
 //
 // Warps: 0-3 Q conversion, softmax (one thread per head row) and epilogue;
 // warps 4-6 producers (warp 4 also issues the Q tile's TMA); warp 7 TMEM
@@ -40,15 +47,19 @@ namespace fa {
 constexpr int kMlaD = 576;                   // key / query width: latent 512 + rope 64
 constexpr int kMlaDv = 512;                  // value width (the latent part of a key row)
 constexpr int kMlaN = 64;                    // gathered keys per tile
-constexpr int kMlaDq = 128;                  // value columns per CTA
+constexpr int kMlaDq = 256;                  // value columns per CTA
 constexpr int kMlaSplit = kMlaDv / kMlaDq;   // CTAs per (token, head group)
 constexpr int kMlaHeads = 128;               // query heads per CTA (MMA rows)
-constexpr int kMlaNS = 3;                    // ring stages
+constexpr int kMlaNS = 2;                    // ring stages
+constexpr int kMlaProducers = 3;             // producer warps, all on every tile
+constexpr int kMlaMmaWarp = 4 + kMlaProducers;
+constexpr int kMlaThreads = 32 * (kMlaMmaWarp + 1);
 constexpr int kMlaMaxTopk = 2048;            // longest slot list
-constexpr int kMlaThreads = 256;
 constexpr int kMlaBoxes = kMlaD / 64;        // 128-byte column boxes per key row
+constexpr int kMlaQtBoxes = 5;               // query boxes kept in TMEM (columns 0-319)
 constexpr int kMlaHiLoKeys = 256;
-constexpr uint32_t kMlaColO = 0, kMlaColS = 128, kMlaColP = 192, kMlaColQ = 224;
+constexpr uint32_t kMlaColO = 0, kMlaColS = 256, kMlaColP = 320, kMlaColQ = 352;
+static_assert(kMlaColQ + 32 * kMlaQtBoxes == 512, "TMEM plan");
 
 struct MlaParams {
   CUtensorMap tm_q;   // 3-D (D, Sq, B*Hq), box 64 x 1 x 128 heads
@@ -70,29 +81,61 @@ struct MlaParams {
 
 struct MlaSmem {
   static constexpr int kBoxBytes = kMlaN * 128;                  // 64 key rows x 64 columns
-  static constexpr int kStageBytes = kMlaBoxes * kBoxBytes;      // one gathered tile
+  static constexpr int kStageBytes = kMlaBoxes * kBoxBytes;      // one gathered tile (72 KB)
   static constexpr int kQBoxBytes = kMlaHeads * 128;             // 128 heads x 64 columns
   static constexpr int kRingOff = 0;
-  static constexpr int kIdxOff = kRingOff + kMlaNS * kStageBytes;
+  static constexpr int kQsOff = kRingOff + kMlaNS * kStageBytes;  // query columns 320-575
+  static constexpr int kIdxOff = kQsOff + (kMlaBoxes - kMlaQtBoxes) * kQBoxBytes;
   static constexpr int kCntOff = kIdxOff + kMlaMaxTopk * 4;
   static constexpr int kBarOff = kCntOff + (kMlaMaxTopk / 128) * 4 * 4;
-  // full[NS], empty[NS], q_full, q_done, s_full, s_free, p_ready, pv_done, drain
-  static constexpr int kNumBars = 2 * kMlaNS + 7;
+  // full_x[NS], full_v[NS], empty_x[NS], empty_v[NS], q_full, q_done, s_full,
+  // s_free, p_ready, pv_done, drain
+  static constexpr int kNumBars = 4 * kMlaNS + 7;
   // tmem base, abort flag, key count, residual-pass flags of two tiles
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 32;
   static constexpr int kAlloc = kBytes + 1024;
-  static_assert(kMlaBoxes * kQBoxBytes <= 2 * kStageBytes, "Q staging must fit in stages 0-1");
+  static_assert(kMlaBoxes * kQBoxBytes <= kMlaNS * kStageBytes, "Q staging must fit in the ring");
   static_assert(kAlloc <= 232448, "shared memory per CTA");
 };
 
-// Ring position of gathered tile j: the Q tile occupies the first two stages
-// at first, so tile 0 goes to stage 2 and tile j to stage (j + 2) % 3.  `use`
-// counts the tiles placed in that stage before this one.
-__device__ __forceinline__ void mla_stage(int j, int& s, int& use) {
-  const int u = j + 2;
-  s = u % kMlaNS;
-  use = (s == 2) ? u / kMlaNS : u / kMlaNS - 1;
+// The V boxes of the CTA for value half `half` are 4 half .. 4 half + 3; every
+// other box of a key row is an X box.
+__device__ __forceinline__ bool mla_is_v_box(int bx, int half) { return (bx >> 2) == half && bx < 8; }
+
+// Q K^T of one tile, the X boxes first, then the V boxes (k-step kk covers
+// query columns 16 kk .. 16 kk + 15: box kk / 4).  Query columns below 320 come
+// from TMEM, the others from shared memory.  The V steps wait for the V region.
+template <int kHalf>
+__device__ __forceinline__ bool mla_issue_qk(uint32_t tmem, uint64_t kd, uint64_t qs_desc0,
+                                             uint32_t idesc, uint32_t lead, uint32_t bar_full_v,
+                                             uint32_t parity, const WaitCtx& wc) {
+  constexpr int kSteps = kMlaD / 16;
+  bool first = true;
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    if (pass == 1) {
+      if (!__all_sync(0xffffffffu, wait_bar(bar_full_v, parity, wc))) return false;
+      tc_fence_after();
+    }
+#pragma unroll
+    for (int kk = 0; kk < kSteps; ++kk) {
+      const bool in_v = ((kk >> 4) == kHalf) && kk < 32;
+      if (in_v != (pass == 1)) continue;
+      const uint32_t boff16 =
+          (uint32_t)((kk >> 2) * MlaSmem::kBoxBytes + (kk & 3) * 32) >> 4;
+      if (kk < 4 * kMlaQtBoxes) {
+        mma_ts_if(tmem + kMlaColS, tmem + kMlaColQ + 8 * kk, kd + boff16, idesc, first ? 0u : 1u,
+                  lead);
+      } else {
+        const int qk = kk - 4 * kMlaQtBoxes;
+        const uint32_t aoff16 = (uint32_t)((qk >> 2) * MlaSmem::kQBoxBytes + (qk & 3) * 32) >> 4;
+        mma_ss_if(tmem + kMlaColS, qs_desc0 + aoff16, kd + boff16, idesc, first ? 0u : 1u, lead);
+      }
+      first = false;
+    }
+  }
+  return true;
 }
 
 template <bool kBF16>
@@ -107,10 +150,15 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sRing = sbase + SM::kRingOff;
+  const uint32_t sQs = sbase + SM::kQsOff;
   int* s_idx = reinterpret_cast<int*>(smem + SM::kIdxOff);
   int* s_cnt = reinterpret_cast<int*>(smem + SM::kCntOff);
   const uint32_t bar0 = sbase + SM::kBarOff;
-  const uint32_t BAR_QFULL = bar0 + 8u * (2 * kMlaNS);
+  auto BAR_FULL_X = [=](int s) { return bar0 + 8u * s; };
+  auto BAR_FULL_V = [=](int s) { return bar0 + 8u * (kMlaNS + s); };
+  auto BAR_EMPTY_X = [=](int s) { return bar0 + 8u * (2 * kMlaNS + s); };
+  auto BAR_EMPTY_V = [=](int s) { return bar0 + 8u * (3 * kMlaNS + s); };
+  const uint32_t BAR_QFULL = bar0 + 8u * (4 * kMlaNS);
   const uint32_t BAR_QDONE = BAR_QFULL + 8;
   const uint32_t BAR_SFULL = BAR_QFULL + 16;
   const uint32_t BAR_SFREE = BAR_QFULL + 24;
@@ -127,7 +175,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   const int lane = tid & 31;
 
   // ---------------------------------------------------------------- unit
-  const int qtr = blockIdx.x % kMlaSplit;
+  const int half = blockIdx.x % kMlaSplit;
   const int rest = blockIdx.x / kMlaSplit;
   const int hg = rest % p.n_hg;
   const int bt = rest / p.n_hg;
@@ -139,8 +187,10 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kMlaNS; ++s) {
-      mbar_init(bar0 + 8u * s, 1);              // full: TMA bytes
-      mbar_init(bar0 + 8u * (kMlaNS + s), 1);   // empty: MMA commit
+      mbar_init(BAR_FULL_X(s), kMlaProducers);   // one arrival per producer warp
+      mbar_init(BAR_FULL_V(s), kMlaProducers);
+      mbar_init(BAR_EMPTY_X(s), 1);              // MMA commits
+      mbar_init(BAR_EMPTY_V(s), 1);
     }
     mbar_init(BAR_QFULL, 1);
     mbar_init(BAR_QDONE, 4);     // one arrival per softmax warp
@@ -153,14 +203,14 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     *s_nkeys = 0;
     fence_mbar_init();
   }
-  if (warp == 7) {
+  if (warp == kMlaMmaWarp) {
     tmem_alloc(smem_u32(s_tmem), 512);
     tmem_relinquish();
   }
   __syncthreads();
 
-  // The Q tile (bf16 or fp16) into ring stages 0-1 while the softmax warps
-  // compact the key list.
+  // The Q tile (bf16 or fp16) into the ring while the softmax warps compact
+  // the key list.
   if (warp == 4 && lane == 0 && live) {
     tma_prefetch_desc(&p.tm_q);
     mbar_arrive_expect_tx(BAR_QFULL, kMlaBoxes * 128 * p.q_rows);
@@ -220,7 +270,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     float m = -INFINITY, l = 0.f;
     int npv = 0;   // P.V passes of the tiles done so far (the MMA warp counts the same)
     if (nt > 0) {
-      // ---- Q: staging -> fp16 pairs in TMEM columns [224, 512)
+      // ---- Q: staging -> fp16; columns 0-319 as pairs into TMEM columns
+      // [352, 512), columns 320-575 into shared memory (same swizzled layout)
       if (!__all_sync(0xffffffffu, wait_bar(BAR_QFULL, 0, wc))) dead = true;
       if (!dead) {
         uint32_t amax = 0;
@@ -243,15 +294,24 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
               }
             }
           }
-          tmem_st32(tmem + lane_off + kMlaColQ + 32 * bx, w);
+          if (bx < kMlaQtBoxes) {
+            tmem_st32(tmem + lane_off + kMlaColQ + 32 * bx, w);
+          } else {
+            uint8_t* dst = smem + SM::kQsOff + (bx - kMlaQtBoxes) * SM::kQBoxBytes + r * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) << 4)) =
+                  make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+          }
         }
         tmem_wait_st();
+        fence_proxy_async_smem();   // generic-proxy writes -> tensor core reads
         if (kBF16 && row_ok && ((amax & 0xFFFFu) > 0x477Fu || (amax >> 16) > 0x477Fu))
           atomicOr(p.status, kStatusRange);
         tc_fence_before();
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(BAR_QDONE);   // Q in TMEM, staging free
+      if (lane == 0) mbar_arrive(BAR_QDONE);   // Q in TMEM / shared memory, staging free
 
       const float c = p.scale_log2;
       const uint64_t c2 = f2_pack(c, c);
@@ -350,7 +410,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         tc_fence_after();
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll
+#pragma unroll 1
           for (int cc = 0; cc < kMlaDq / 32; ++cc) {
             uint32_t o32[32];
             tmem_ld32(tO + 32 * cc, o32);
@@ -390,14 +450,14 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       }
     }
 
-    // ---- epilogue: O / l for this CTA's 128 value columns, LSE (quarter 0)
+    // ---- epilogue: O / l for this CTA's 256 value columns, LSE (first half)
     const bool acc = nt > 0 && !dead &&
                      __all_sync(0xffffffffu, wait_bar(BAR_PVDONE, (npv - 1) & 1, wc));
     if (acc) tc_fence_after();
     const bool write = row_ok;
     const float inv_l = (acc && l > 0.f) ? 1.f / l : 0.f;
     uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
-                     ((size_t)(b * p.Hq + h) * p.Sq + t) * kMlaDv + qtr * kMlaDq;
+                     ((size_t)(b * p.Hq + h) * p.Sq + t) * kMlaDv + half * kMlaDq;
 #pragma unroll 1
     for (int cc = 0; cc < kMlaDq / 32; ++cc) {
       uint32_t o32[32];
@@ -423,53 +483,60 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         }
       }
     }
-    if (write && qtr == 0)
+    if (write && half == 0)
       p.lse[(size_t)(b * p.Hq + h) * p.Sq + t] =
           (acc && l > 0.f) ? __fmaf_rn(m, p.scale, __logf(l)) : INFINITY;
-  } else if (warp < 4 + kMlaNS) {
+  } else if (warp < kMlaMmaWarp) {
     // ============================================================ producers
-    // Warp 4 + s fills ring stage s: the tiles j with (j + 2) % 3 == s.  Each
-    // lane copies 16-byte chunks (4 rows x 128 bytes per warp instruction, so
-    // every 128-byte line is read whole) to their 128-byte-swizzle positions,
-    // then the warp waits for its copies, fences them for the tensor core (async
-    // proxy) and arrives on the stage's full barrier.
-    const int s = warp - 4;
-    const uint32_t stage = sRing + s * SM::kStageBytes;
+    // All three warps copy every tile j into stage j % 2: warp 4 + w the row
+    // groups w, w + 3, w + 6, ... (four rows each).  First the X boxes,
+    // once Q K^T of the tile two back has read them, then the V boxes, once
+    // its P.V has.  Each lane copies 16-byte chunks (4 rows x 128 bytes per
+    // warp instruction, so every 128-byte line is read whole) to their
+    // 128-byte-swizzle positions; the warp waits for its copies, fences them
+    // for the tensor core (async proxy) and arrives on the region's full
+    // barrier.  The first use of each stage waits for the Q staging instead.
+    const int w = warp - 4;
     const int sub = lane >> 3;       // row within a group of four
     const int chunk = lane & 7;      // 16-byte chunk within a 128-byte row
     bool ab = false;
 #pragma unroll 1
-    for (int j = (s + 1) % kMlaNS; j < nt && !ab; j += kMlaNS) {
-      int s_, use;
-      mla_stage(j, s_, use);
-      if (lane == 0) {
-        if (use == 0 && s < 2) {
-          ab = !wait_bar(BAR_QDONE, 0, wc);                             // Q staging consumed
-        } else if (use > 0) {
-          ab = !wait_bar(bar0 + 8u * (kMlaNS + s), (use - 1) & 1, wc);   // stage released
-        }
-      }
-      ab = __shfl_sync(0xffffffffu, ab, 0);
-      if (ab) break;
+    for (int j = 0; j < nt && !ab; ++j) {
+      const int s = j % kMlaNS, use = j / kMlaNS;
+      const uint32_t stage = sRing + s * SM::kStageBytes;
 #pragma unroll 1
-      for (int g = 0; g < kMlaN / 4; ++g) {
-        // positions past the last key repeat a valid row (their scores are masked)
-        const int row = 4 * g + sub;
-        const int pos = j * kMlaN + row;
-        const int key = s_idx[pos < nkeys ? pos : nkeys - 1];
-        const uint16_t* src = p.kl + ((size_t)b * p.Skv + key) * kMlaD + chunk * 8;
-        const uint32_t dst = stage + row * 128 + ((chunk ^ (row & 7)) << 4);
+      for (int region = 0; region < 2 && !ab; ++region) {
+        if (lane == 0) {
+          if (use == 0) {
+            ab = region == 0 && !wait_bar(BAR_QDONE, 0, wc);             // Q staging consumed
+          } else {
+            ab = !wait_bar(region ? BAR_EMPTY_V(s) : BAR_EMPTY_X(s), (use - 1) & 1, wc);
+          }
+        }
+        ab = __shfl_sync(0xffffffffu, ab, 0);
+        if (ab) break;
+#pragma unroll 1
+        for (int g = w; g < kMlaN / 4; g += kMlaProducers) {
+          // positions past the last key repeat a valid row (their scores are masked)
+          const int row = 4 * g + sub;
+          const int pos = j * kMlaN + row;
+          const int key = s_idx[pos < nkeys ? pos : nkeys - 1];
+          const uint16_t* src = p.kl + ((size_t)b * p.Skv + key) * kMlaD + chunk * 8;
+          const uint32_t dst = stage + row * 128 + ((chunk ^ (row & 7)) << 4);
 #pragma unroll
-        for (int bx = 0; bx < kMlaBoxes; ++bx) cp_async16(dst + bx * SM::kBoxBytes, src + bx * 64);
+          for (int bx = 0; bx < kMlaBoxes; ++bx)
+            if (mla_is_v_box(bx, half) == (region == 1))
+              cp_async16(dst + bx * SM::kBoxBytes, src + bx * 64);
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(region ? BAR_FULL_V(s) : BAR_FULL_X(s));
       }
-      cp_async_commit();
-      cp_async_wait_all();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar0 + 8u * s);
     }
     // the Q tile's copy must land before the CTA's shared memory goes away
-    if (s == 0 && lane == 0 && live) drain_bar(BAR_QFULL, 0, wc.timeout);
+    if (w == 0 && lane == 0 && live) drain_bar(BAR_QFULL, 0, wc.timeout);
     __syncwarp();
   } else {
     // ============================================================ MMA issue
@@ -481,32 +548,31 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       bool ok = __all_sync(0xffffffffu, wait_bar(BAR_QDONE, 0, wc));
       tc_fence_after();
       const uint64_t k_desc0 = sw128_desc(sRing, 16, 1024);                          // K-major
-      const uint64_t v_desc0 = sw128_desc(sRing + qtr * 2 * SM::kBoxBytes, SM::kBoxBytes, 1024);
+      const uint64_t qs_desc0 = sw128_desc(sQs, 16, 1024);                           // K-major
+      const uint64_t v_desc0 =
+          sw128_desc(sRing + half * 4 * SM::kBoxBytes, SM::kBoxBytes, 1024);         // MN-major
       int c_pready = 0;   // P-ready phases consumed
 #pragma unroll 1
       for (int j = 0; j <= nt && ok; ++j) {
         if (j < nt) {
           // S_j = Q K_j^T, once the softmax of tile j-1 has read S
           if (j > 0) ok = __all_sync(0xffffffffu, wait_bar(BAR_SFREE, (j - 1) & 1, wc));
-          int s, use;
-          mla_stage(j, s, use);
-          if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar0 + 8u * s, use & 1, wc));
+          const int s = j % kMlaNS, use = j / kMlaNS;
+          if (ok) ok = __all_sync(0xffffffffu, wait_bar(BAR_FULL_X(s), use & 1, wc));
           if (!ok) break;
           tc_fence_after();
           const uint64_t kd = k_desc0 + ((uint32_t)(s * SM::kStageBytes) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < kMlaD / 16; ++kk) {
-            const uint32_t off16 = (uint32_t)((kk >> 2) * SM::kBoxBytes + (kk & 3) * 32) >> 4;
-            mma_ts_if(tmem + kMlaColS, tmem + kMlaColQ + 8 * kk, kd + off16, kIdescQK, kk > 0, lead);
-          }
+          ok = half ? mla_issue_qk<1>(tmem, kd, qs_desc0, kIdescQK, lead, BAR_FULL_V(s), use & 1, wc)
+                    : mla_issue_qk<0>(tmem, kd, qs_desc0, kIdescQK, lead, BAR_FULL_V(s), use & 1, wc);
+          if (!ok) break;
           mma_commit_if(BAR_SFULL, lead);
+          mma_commit_if(BAR_EMPTY_X(s), lead);   // the X boxes are read by Q K^T only
         }
         if (j == 0) continue;
-        // O += P_{j-1} V_{j-1} (this CTA's 128 value columns of the tile), then
+        // O += P_{j-1} V_{j-1} (this CTA's 256 value columns of the tile), then
         // the residual pass with P_lo when the softmax asked for one
         const int jp = j - 1;
-        int s, use;
-        mla_stage(jp, s, use);
+        const int s = jp % kMlaNS;
         const uint64_t vd = v_desc0 + ((uint32_t)(s * SM::kStageBytes) >> 4);
         for (int pass = 0; pass < 2; ++pass) {
           if (!__all_sync(0xffffffffu, wait_bar(BAR_PREADY, c_pready & 1, wc))) {
@@ -523,7 +589,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
           if (pass == 0 && !s_lo[jp & 1]) break;
         }
         if (!ok) break;
-        mma_commit_if(bar0 + 8u * (kMlaNS + s), lead);   // stage free
+        mma_commit_if(BAR_EMPTY_V(s), lead);   // the V boxes are free again
       }
       // every MMA has finished before TMEM is released
       if (lead) {
@@ -537,7 +603,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   // ---------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 7) {
+  if (warp == kMlaMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
