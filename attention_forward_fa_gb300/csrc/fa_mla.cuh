@@ -24,8 +24,9 @@
 // has two regions with their own full / empty barriers: V, this CTA's four
 // value boxes (read by Q K^T and P V), and X, the other five boxes (read by
 // Q K^T only).  X is free again once Q K^T of its tile is done, V once its
-// P V is done; Q K^T of the next tile multiplies the X boxes first, which
-// gives the gather of the V boxes the time of those steps.  Three producer
+// P V is done; Q K^T multiplies the X boxes first, and P V of the previous
+// tile runs between the two parts, which gives the gather of the V boxes of
+// tile j+1 the time of the V steps of tile j and the X steps of tile j+1.  Three producer
 // warps copy every tile together in 16-byte chunks (cp.async); the Q tile is
 // first staged (bf16 or fp16, via TMA) in both ring stages and converted to
 // fp16 into TMEM and shared memory.
@@ -33,8 +34,9 @@
 // Warps: 0-3 Q conversion, softmax (one thread per head row) and epilogue;
 // warps 4-6 producers (warp 4 also issues the Q tile's TMA); warp 7 TMEM
 // allocator and MMA issuer.
-// MMA order: S_0, then per tile j: S_{j+1} = Q K_{j+1}^T, O += P_j V_j, so the
-// softmax of tile j overlaps the next Q K^T.  A tile gets a second P.V pass
+// MMA order per tile j: the X steps of S_j = Q K_j^T, O += P_{j-1} V_{j-1},
+// the V steps of S_j; so the softmax of tile j-1 overlaps the X steps of S_j,
+// and the V region of tile j-1 is free (for tile j+1) before the V steps of S_j.  A tile gets a second P.V pass
 // with the residual P_lo = p - fp16(p) (written over P once the first pass has
 // read it) when the token has fewer than kMlaHiLoKeys keys, or when a row keeps
 // a stale max below the tile's max (lazy rescale): that row's dominant p is
@@ -103,39 +105,30 @@ struct MlaSmem {
 // other box of a key row is an X box.
 __device__ __forceinline__ bool mla_is_v_box(int bx, int half) { return (bx >> 2) == half && bx < 8; }
 
-// Q K^T of one tile, the X boxes first, then the V boxes (k-step kk covers
-// query columns 16 kk .. 16 kk + 15: box kk / 4).  Query columns below 320 come
-// from TMEM, the others from shared memory.  The V steps wait for the V region.
-template <int kHalf>
-__device__ __forceinline__ bool mla_issue_qk(uint32_t tmem, uint64_t kd, uint64_t qs_desc0,
-                                             uint32_t idesc, uint32_t lead, uint32_t bar_full_v,
-                                             uint32_t parity, const WaitCtx& wc) {
+// One part of Q K^T for a tile: the steps over the X boxes (kV false, the
+// first steps of the product) or over the V boxes (k-step kk covers query
+// columns 16 kk .. 16 kk + 15: box kk / 4).  Query columns below 320 come from
+// TMEM, the others from shared memory.
+template <int kHalf, bool kV>
+__device__ __forceinline__ void mla_issue_qk(uint32_t tmem, uint64_t kd, uint64_t qs_desc0,
+                                             uint32_t idesc, uint32_t lead) {
   constexpr int kSteps = kMlaD / 16;
-  bool first = true;
+  bool first = !kV;
 #pragma unroll
-  for (int pass = 0; pass < 2; ++pass) {
-    if (pass == 1) {
-      if (!__all_sync(0xffffffffu, wait_bar(bar_full_v, parity, wc))) return false;
-      tc_fence_after();
+  for (int kk = 0; kk < kSteps; ++kk) {
+    const bool in_v = ((kk >> 4) == kHalf) && kk < 32;
+    if (in_v != kV) continue;
+    const uint32_t boff16 = (uint32_t)((kk >> 2) * MlaSmem::kBoxBytes + (kk & 3) * 32) >> 4;
+    if (kk < 4 * kMlaQtBoxes) {
+      mma_ts_if(tmem + kMlaColS, tmem + kMlaColQ + 8 * kk, kd + boff16, idesc, first ? 0u : 1u,
+                lead);
+    } else {
+      const int qk = kk - 4 * kMlaQtBoxes;
+      const uint32_t aoff16 = (uint32_t)((qk >> 2) * MlaSmem::kQBoxBytes + (qk & 3) * 32) >> 4;
+      mma_ss_if(tmem + kMlaColS, qs_desc0 + aoff16, kd + boff16, idesc, first ? 0u : 1u, lead);
     }
-#pragma unroll
-    for (int kk = 0; kk < kSteps; ++kk) {
-      const bool in_v = ((kk >> 4) == kHalf) && kk < 32;
-      if (in_v != (pass == 1)) continue;
-      const uint32_t boff16 =
-          (uint32_t)((kk >> 2) * MlaSmem::kBoxBytes + (kk & 3) * 32) >> 4;
-      if (kk < 4 * kMlaQtBoxes) {
-        mma_ts_if(tmem + kMlaColS, tmem + kMlaColQ + 8 * kk, kd + boff16, idesc, first ? 0u : 1u,
-                  lead);
-      } else {
-        const int qk = kk - 4 * kMlaQtBoxes;
-        const uint32_t aoff16 = (uint32_t)((qk >> 2) * MlaSmem::kQBoxBytes + (qk & 3) * 32) >> 4;
-        mma_ss_if(tmem + kMlaColS, qs_desc0 + aoff16, kd + boff16, idesc, first ? 0u : 1u, lead);
-      }
-      first = false;
-    }
+    first = false;
   }
-  return true;
 }
 
 template <bool kBF16>
@@ -554,42 +547,52 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       int c_pready = 0;   // P-ready phases consumed
 #pragma unroll 1
       for (int j = 0; j <= nt && ok; ++j) {
+        // Per tile j: the X steps of S_j = Q K_j^T, then O += P_{j-1} V_{j-1}
+        // (which frees the V region of stage (j-1) % 2 for tile j+1 early),
+        // then the V steps of S_j.
+        const int s = j % kMlaNS, use = j / kMlaNS;
+        const uint64_t kd = k_desc0 + ((uint32_t)(s * SM::kStageBytes) >> 4);
         if (j < nt) {
-          // S_j = Q K_j^T, once the softmax of tile j-1 has read S
+          // once the softmax of tile j-1 has read S
           if (j > 0) ok = __all_sync(0xffffffffu, wait_bar(BAR_SFREE, (j - 1) & 1, wc));
-          const int s = j % kMlaNS, use = j / kMlaNS;
           if (ok) ok = __all_sync(0xffffffffu, wait_bar(BAR_FULL_X(s), use & 1, wc));
           if (!ok) break;
           tc_fence_after();
-          const uint64_t kd = k_desc0 + ((uint32_t)(s * SM::kStageBytes) >> 4);
-          ok = half ? mla_issue_qk<1>(tmem, kd, qs_desc0, kIdescQK, lead, BAR_FULL_V(s), use & 1, wc)
-                    : mla_issue_qk<0>(tmem, kd, qs_desc0, kIdescQK, lead, BAR_FULL_V(s), use & 1, wc);
+          if (half) mla_issue_qk<1, false>(tmem, kd, qs_desc0, kIdescQK, lead);
+          else      mla_issue_qk<0, false>(tmem, kd, qs_desc0, kIdescQK, lead);
+        }
+        if (j > 0) {
+          // O += P_{j-1} V_{j-1} (this CTA's 256 value columns of the tile), then
+          // the residual pass with P_lo when the softmax asked for one
+          const int jp = j - 1;
+          const int sp = jp % kMlaNS;
+          const uint64_t vd = v_desc0 + ((uint32_t)(sp * SM::kStageBytes) >> 4);
+          for (int pass = 0; pass < 2; ++pass) {
+            if (!__all_sync(0xffffffffu, wait_bar(BAR_PREADY, c_pready & 1, wc))) {
+              ok = false;
+              break;
+            }
+            ++c_pready;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kMlaN / 16; ++kk)
+              mma_ts_if(tmem + kMlaColO, tmem + kMlaColP + 8 * kk, vd + ((kk * 2048) >> 4),
+                        kIdescPV, (jp > 0 || pass > 0 || kk > 0) ? 1u : 0u, lead);
+            mma_commit_if(BAR_PVDONE, lead);
+            if (pass == 0 && !s_lo[jp & 1]) break;
+          }
           if (!ok) break;
+          mma_commit_if(BAR_EMPTY_V(sp), lead);   // the V boxes of tile j-1 are free again
+        }
+        if (j < nt) {
+          ok = __all_sync(0xffffffffu, wait_bar(BAR_FULL_V(s), use & 1, wc));
+          if (!ok) break;
+          tc_fence_after();
+          if (half) mla_issue_qk<1, true>(tmem, kd, qs_desc0, kIdescQK, lead);
+          else      mla_issue_qk<0, true>(tmem, kd, qs_desc0, kIdescQK, lead);
           mma_commit_if(BAR_SFULL, lead);
           mma_commit_if(BAR_EMPTY_X(s), lead);   // the X boxes are read by Q K^T only
         }
-        if (j == 0) continue;
-        // O += P_{j-1} V_{j-1} (this CTA's 256 value columns of the tile), then
-        // the residual pass with P_lo when the softmax asked for one
-        const int jp = j - 1;
-        const int s = jp % kMlaNS;
-        const uint64_t vd = v_desc0 + ((uint32_t)(s * SM::kStageBytes) >> 4);
-        for (int pass = 0; pass < 2; ++pass) {
-          if (!__all_sync(0xffffffffu, wait_bar(BAR_PREADY, c_pready & 1, wc))) {
-            ok = false;
-            break;
-          }
-          ++c_pready;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kMlaN / 16; ++kk)
-            mma_ts_if(tmem + kMlaColO, tmem + kMlaColP + 8 * kk, vd + ((kk * 2048) >> 4), kIdescPV,
-                      (jp > 0 || pass > 0 || kk > 0) ? 1u : 0u, lead);
-          mma_commit_if(BAR_PVDONE, lead);
-          if (pass == 0 && !s_lo[jp & 1]) break;
-        }
-        if (!ok) break;
-        mma_commit_if(BAR_EMPTY_V(s), lead);   // the V boxes are free again
       }
       // every MMA has finished before TMEM is released
       if (lead) {
