@@ -475,7 +475,8 @@ def run_ours(args, world, rank, local):
     if p.topk_idx is not None:
         kernel = f"fa_mla_topk_kernel<{'bf16' if bf16 else 'fp16'}>"
     else:
-        kernel = f"fa_fwd_tiled_kernel<{p.D},{'bf16' if bf16 else 'fp16'},{4 if p.D == 128 else 6}>"
+        kernel = (f"fa_fwd_tiled_kernel<{p.D},{'bf16' if bf16 else 'fp16'},{4 if p.D == 128 else 6}"
+                  f"{',convert-V' if bf16 else ''}>")
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak,
             "peak_source": f"{peak_src} bf16_tflops (burst); the fp16 products run at the same "
