@@ -31,6 +31,8 @@
 // source": keep the stale max while the block max exceeds it by no more than
 // `threshold` log2 units (0 = exact running max).
 #pragma once
+#include <type_traits>
+
 #include "fa_ptx.cuh"
 
 namespace fa {
@@ -50,9 +52,12 @@ static_assert(kSoftmaxRegs % 8 == 0 && kCorrRegs % 8 == 0 && kOtherRegs % 8 == 0
 static_assert(kRegsNeeded <= 65536 / kTiledThreads, "register split exceeds the register file");
 constexpr int kMaxSel = 512;      // longest block list a CTA stages in smem
 constexpr int kHiLoKeys = 256;    // rows with fewer valid keys use the hi+lo P split
-// hardware named barriers (0 is __syncthreads): 1-2 scheduler -> issuer release,
-// 3-4 issuer -> scheduler consumed, 5-6 softmax slot t -> issuer "P ready"
+// hardware named barriers (0 is __syncthreads): 1-2 scheduler -> issuer release
+// of groups 0 and 1, 3-4 issuer -> scheduler "group issued", 5-6 "P ready" of
+// slot t (its softmax warps and the scheduler -> issuer: P written and the
+// group's copies landed)
 constexpr int kBarPReady = 5;
+constexpr int kPReadyCount = kBM + 64;   // slot's softmax threads, scheduler, issuer
 
 enum : int { kStatusTimeout = 1, kStatusRange = 2 };
 
@@ -406,7 +411,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       }
       if (dead) {
         // the MMA issuer waits for one arrival per tile on a hardware barrier
-        named_arrive(kBarPReady + t, kBM + 32);
+        named_arrive(kBarPReady + t, kPReadyCount);
         continue;
       }
       if (row == 0) FA_TR(1, t, j);
@@ -540,7 +545,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       tc_fence_before();
       if (row == 0) FA_TR(2, t, j);
       // P_t (and the rescaled O_t) ready: hardware barrier to the MMA issuer
-      named_arrive(kBarPReady + t, kBM + 32);
+      named_arrive(kBarPReady + t, kPReadyCount);
     }
     // final row statistics for the epilogue warpgroup
     s_m[t * kBM + row] = m;
@@ -699,9 +704,10 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     // the pairs [PV(0,j) QK(0,j+1)] and [PV(1,j) QK(1,j+1)].  Warp 14 (the
     // scheduler) waits on the TMA mbarriers a group depends on and releases the
     // group to warp 13 (the issuer) through hardware named barriers, running up
-    // to two groups ahead; the softmax warps signal "P ready" to the issuer on
-    // a named barrier as well.  The issuer therefore never polls shared memory,
-    // which the tensor core's operand reads keep busy.
+    // to two groups ahead: for every group with a P.V it arrives on the slot's
+    // "P ready" barrier, where the softmax warps arrive too, so the issuer
+    // waits once per group.  The issuer never polls shared memory, which the
+    // tensor core's operand reads keep busy.
     regs_dec<kOtherRegs>();
     FA_TR_ROLE(warp == 13 ? 4 : 5);
     const bool issuer = (warp == 13);
@@ -711,34 +717,35 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     const uint64_t v_desc0 = sw128_desc(sStage, kBN * 128, 1024);    // MN-major V
     const int nmax = n0 > n1 ? n0 : n1;
     const int ngroups = nmax > 0 ? 2 + 2 * nmax : 0;
-    int ld = 0;            // ring loads consumed so far (independent K/V sequences)
-    bool aborted = false;
-    const uint32_t lead = elect_lane();
+    if (!issuer) {
+      // ---- scheduler: walks the groups in order, waits for the TMA copies a
+      // group reads and releases it: groups 0 and 1 (Q.K^T only) on named
+      // barrier 1 + g, every later group on the slot's "P ready" barrier,
+      // which the softmax warps of the slot complete as well
+      int ld = 0;            // ring loads consumed so far (independent K/V sequences)
+      bool aborted = false;
 #pragma unroll 1
-    for (int g = 0; g < ngroups; ++g) {
-      // ---- the group's events, ring stages and phases (same code in both warps)
-      const int t = g < 2 ? g : ((g - 2) & 1);
-      const int jpv = g < 2 ? -1 : ((g - 2) >> 1);         // P.V tile (none in groups 0, 1)
-      const int jqk = g < 2 ? 0 : jpv + 1;                 // Q.K^T tile
-      const int nt = t ? n1 : n0;
-      const bool pv_valid = jpv >= 0 && jpv < nt;
-      const bool qk_valid = jqk < nt;
-      // with shared K/V, slot 1 reuses slot 0's tiles and the load order is
-      // K_0 V_0 K_1 V_1 ...; otherwise every event loads its own tile, in order
-      const bool pv_load = pv_valid && (!shared_kv || t == 0 || jpv >= n0);
-      const bool qk_load = qk_valid && (!shared_kv || t == 0 || jqk >= n0);
-      int lpv, lqk;
-      if (shared_kv) {
-        lpv = 2 * jpv + 1;
-        lqk = 2 * jqk;
-      } else {
-        lpv = ld;
-        lqk = ld + (pv_load ? 1 : 0);
-        ld += (pv_load ? 1 : 0) + (qk_load ? 1 : 0);
-      }
-      const uint32_t sv_ = (uint32_t)lpv % NS, sk_ = (uint32_t)lqk % NS;
-      // ---- hand-off: the scheduler waits the TMA dependencies, then releases
-      if (!issuer) {
+      for (int g = 0; g < ngroups; ++g) {
+        const int t = g < 2 ? g : ((g - 2) & 1);
+        const int jpv = g < 2 ? -1 : ((g - 2) >> 1);         // P.V tile (none in groups 0, 1)
+        const int jqk = g < 2 ? 0 : jpv + 1;                 // Q.K^T tile
+        const int nt = t ? n1 : n0;
+        const bool pv_valid = jpv >= 0 && jpv < nt;
+        const bool qk_valid = jqk < nt;
+        // with shared K/V, slot 1 reuses slot 0's tiles and the load order is
+        // K_0 V_0 K_1 V_1 ...; otherwise every event loads its own tile, in order
+        const bool pv_load = pv_valid && (!shared_kv || t == 0 || jpv >= n0);
+        const bool qk_load = qk_valid && (!shared_kv || t == 0 || jqk >= n0);
+        int lpv, lqk;
+        if (shared_kv) {
+          lpv = 2 * jpv + 1;
+          lqk = 2 * jqk;
+        } else {
+          lpv = ld;
+          lqk = ld + (pv_load ? 1 : 0);
+          ld += (pv_load ? 1 : 0) + (qk_load ? 1 : 0);
+        }
+        const uint32_t sv_ = (uint32_t)lpv % NS, sk_ = (uint32_t)lqk % NS;
         if (g >= 2) named_sync(3 + (g & 1), 64);      // issuer finished group g-2
         if (lane == 0 && !aborted) {
           if (pv_load && !wait_bar(BAR_READY(sv_), (lpv / NS) & 1, wc)) aborted = true;
@@ -746,36 +753,72 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           if (!aborted && qk_valid && jqk == 0 && !wait_bar(BAR_QFULL(t), 0, wc)) aborted = true;
         }
         aborted = __shfl_sync(0xffffffffu, aborted, 0);
-        named_arrive(1 + (g & 1), 64);
-      } else {
-        named_sync(1 + (g & 1), 64);                   // TMA dependencies of group g met
-        // (after a timeout the scheduler still releases every group; the issuer
-        // then runs on stale operands, which is harmless: the status word
-        // already reports the failure and nothing waits on the results)
-        if (pv_valid) {
+        // (after a timeout every group is still released; the issuer then runs
+        // on stale operands, which is harmless: the status word already
+        // reports the failure and nothing waits on the results)
+        if (g < 2) {
+          named_arrive(1 + g, 64);
+        } else if (pv_valid) {
+          named_arrive(kBarPReady + t, kPReadyCount);
+        }
+      }
+      // the issuer's last two "group issued" arrivals
+      if (ngroups >= 2) named_sync(3 + (ngroups & 1), 64);
+      if (ngroups >= 1) named_sync(3 + ((ngroups - 1) & 1), 64);
+    } else {
+      // ---- issuer: the same groups, two per step (slot 0, slot 1) so that
+      // everything that depends on the slot is fixed at compile time.  The
+      // whole warp runs the issue code (warp-uniform branches only); the
+      // elected lane's predicate lets exactly one copy of each tcgen05
+      // instruction through (always the same lane: a commit tracks the MMAs
+      // of the thread that issues it).
+      const uint32_t lead = elect_lane();
+      int ld = 0;
+      auto group = [&](auto slot, int jpv) {
+        constexpr int t = decltype(slot)::value;
+        const int nt = t ? n1 : n0;
+        const int jqk = jpv + 1;
+        const bool pv_valid = jpv >= 0 && jpv < nt;
+        const bool qk_valid = jqk < nt;
+        int lpv, lqk;
+        if (shared_kv) {
+          lpv = 2 * jpv + 1;
+          lqk = 2 * jqk;
+        } else {   // every valid event loads its own tile
+          lpv = ld;
+          lqk = ld + (pv_valid ? 1 : 0);
+          ld += (pv_valid ? 1 : 0) + (qk_valid ? 1 : 0);
+        }
+        const uint32_t sv_ = (uint32_t)lpv % NS, sk_ = (uint32_t)lqk % NS;
+        if (jpv < 0) {
+          named_sync(1 + t, 64);   // the first K tile and Q_t landed
+        } else if (pv_valid) {
           // P_t of tile jpv written by the four softmax warps of slot t (a
           // softmax warp that gave up still arrives once per tile, paced by
-          // the S commits, so this wait always ends)
-          named_sync(kBarPReady + t, kBM + 32);
+          // the S commits, so this wait always ends) and the group's copies
+          // landed (the scheduler's arrival)
+          named_sync(kBarPReady + t, kPReadyCount);
           tc_fence_after();
         }
-        // The whole warp runs the issue code (warp-uniform branches only);
-        // the elected lane's predicate lets exactly one copy of each tcgen05
-        // instruction through (always the same lane: a commit tracks the MMAs
-        // of the thread that issues it).
-        const uint32_t tS = tmem + 128u * t;
+        constexpr uint32_t kS = 128u * t, kO = 256u + 128u * t;
+        // the group's operand bases pass an empty asm, so that the compiler
+        // derives each MMA's operands here instead of keeping those of every
+        // MMA of both slots live across the loop
+        uint32_t tb = tmem;
+        uint64_t vb = v_desc0, kb = k_desc0, qb = q_desc0;
+        asm volatile("" : "+r"(tb), "+l"(vb), "+l"(kb), "+l"(qb));
         if (pv_valid) {
           if (lead) FA_TR(7, t, jpv);
-          const uint32_t tO = tmem + 256u + 128u * t;
-          const uint64_t vd = v_desc0 + ((sv_ * SM::kStageBytes) >> 4);
+          const uint64_t vd = vb + ((sv_ * SM::kStageBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
-            mma_ts_if(tO, tS + 8 * kk, vd + (kk * 2048 >> 4), kIdescPV,
+            mma_ts_if(tb + kO, tb + kS + 8 * kk, vd + (kk * 2048 >> 4), kIdescPV,
                       (jpv > 0 || kk > 0) ? 1u : 0u, lead);
           if (t ? hilo1 : hilo0) {
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
-              mma_ts_if(tO, tS + 64 + 8 * kk, vd + (kk * 2048 >> 4), kIdescPV, 1u, lead);
+              mma_ts_if(tb + kO, tb + kS + 64 + 8 * kk, vd + (kk * 2048 >> 4), kIdescPV, 1u,
+                        lead);
           }
           // O_t is read only by the epilogue, after the slot's last P.V
           if (jpv == nt - 1) mma_commit_if(BAR_OREADY(t), lead);
@@ -786,27 +829,31 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           // S_t is free: the softmax read it before signalling P ready, which
           // was waited on (and fenced) before the previous P.V
           if (lead) FA_TR(6, t, jqk);
-          const uint64_t qd = q_desc0 + ((t * SM::kQBytes) >> 4);
-          const uint64_t kd = k_desc0 + ((sk_ * SM::kStageBytes) >> 4);
+          const uint64_t qd = qb + ((t * SM::kQBytes) >> 4);
+          const uint64_t kd = kb + ((sk_ * SM::kStageBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kKSteps; ++kk) {
             const uint32_t off16 = ((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4;
-            mma_ss_if(tS, qd + off16, kd + off16, kIdescQK, kk > 0, lead);
+            mma_ss_if(tb + kS, qd + off16, kd + off16, kIdescQK, kk > 0, lead);
           }
           mma_commit_if(BAR_SFULL(t), lead);
           if (!shared_kv || t == 1) mma_commit_if(BAR_EMPTY(sk_), lead);
         }
+        __syncwarp();
+        named_arrive(3 + t, 64);   // group issued (its index has the slot's parity)
+      };
+      if (ngroups > 0) {
+        group(std::integral_constant<int, 0>{}, -1);
+        group(std::integral_constant<int, 1>{}, -1);
+#pragma unroll 1
+        for (int j = 0; j < nmax; ++j) {
+          group(std::integral_constant<int, 0>{}, j);
+          group(std::integral_constant<int, 1>{}, j);
+        }
       }
-      __syncwarp();
-      if (issuer) named_arrive(3 + (g & 1), 64);     // group g issued
-    }
-    // the scheduler consumes the issuer's last two releases
-    if (!issuer) {
-      if (ngroups >= 2) named_sync(3 + (ngroups & 1), 64);
-      if (ngroups >= 1) named_sync(3 + ((ngroups - 1) & 1), 64);
     }
     // every MMA has finished before TMEM is released
-    if (issuer && lead && n0 + n1 > 0) {
+    if (issuer && elect_lane() && n0 + n1 > 0) {
       mma_commit(BAR_DRAIN);
       drain_bar(BAR_DRAIN, 0, wc.timeout);
     }
