@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <utility>
 #include <algorithm>
 #include <mutex>
 
@@ -143,6 +144,26 @@ void* scratch_alloc(size_t bytes, cudaStream_t st) {
   return ptr;
 }
 
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// while the previous kernel on the stream drains; it waits for that kernel
+// (griddepcontrol.wait) before its first global memory access.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kern)(Params...), unsigned grid, unsigned block, size_t smem,
+                             cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 template <int D, bool BF16, int NS, bool CONV>
 int launch_tiled(const fa::TiledParams& prm, int units, cudaStream_t st) {
   auto kern = fa::fa_fwd_tiled_kernel<D, BF16, NS, CONV>;
@@ -163,8 +184,7 @@ int launch_tiled(const fa::TiledParams& prm, int units, cudaStream_t st) {
   });
   if (attr_err != cudaSuccess) return cuda_fail(attr_err);
   if (regs_ok[dev & 63] != 1) return cuda_fail(cudaErrorInvalidConfiguration);
-  kern<<<units, fa::kTiledThreads, smem, st>>>(prm);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(kern, (unsigned)units, fa::kTiledThreads, smem, st, prm);
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;
 }
@@ -234,8 +254,7 @@ int launch_mla(const fa::MlaParams& prm, long long units, cudaStream_t st) {
     attr_err[dev & 63] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   if (attr_err[dev & 63] != cudaSuccess) return cuda_fail(attr_err[dev & 63]);
-  kern<<<(unsigned)units, fa::kMlaThreads, smem, st>>>(prm);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(kern, (unsigned)units, fa::kMlaThreads, smem, st, prm);
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 

@@ -138,6 +138,12 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   constexpr uint32_t kIdescQK = idesc_f16(kMlaHeads, kMlaN, false, false);   // fp16 Q x fp16 K
   constexpr uint32_t kIdescPV = idesc_f16(kMlaHeads, kMlaDq, false, true);   // fp16 P x fp16 V
 
+  // The next call on the stream may be scheduled once every CTA of this one
+  // has started; nothing below touches global memory before the previous
+  // kernel (the latent conversion, or the previous call) has completed.
+  pdl_launch_dependents();
+  pdl_wait_prior();
+
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));

@@ -57,6 +57,18 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return ok != 0;
 }
 
+// Programmatic dependent launch.  launch_dependents: the next kernel on the
+// stream may be scheduled once every CTA of this grid has executed it (or
+// exited).  wait_prior: returns once the previous kernel on the stream has
+// completed and its memory operations are visible; a kernel launched without
+// the attribute, or with no kernel before it, returns at once.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_prior() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");

@@ -245,6 +245,12 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + SM::kMiscOff + 4);
   int* s_slot = reinterpret_cast<int*>(smem + SM::kMiscOff + 8);   // [2] n, [2] hilo
 
+  // The next call on the stream may be scheduled once every CTA of this one
+  // has started (its CTAs then wait here for this grid to finish); nothing
+  // below touches global memory before the previous kernel has completed.
+  pdl_launch_dependents();
+  pdl_wait_prior();
+
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
