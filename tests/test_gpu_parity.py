@@ -115,6 +115,32 @@ def test_repeated_calls_are_deterministic():
     assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
 
 
+def test_chained_calls_wait_for_the_previous_call():
+    """Two calls back to back on one stream, the second taking the first's
+    output as its queries.  The second kernel may be scheduled while the first
+    drains (programmatic dependent launch) and must still wait for it before
+    its first read: its result equals that of the synchronised run, bit for bit."""
+    import torch
+    import attention_forward_fa_gb300 as fa
+    p = W.dense(name="chain", B=2, Hq=16, Sq=2048, D=128, mask=W.MASK_CAUSAL, seed=23)
+    d = to_device(p)
+    kw = dict(scale=p.scale, mask_mode=p.mask)
+    o1, _ = fa.flash_attention_forward(d["q"], d["k"], d["v"], **kw)
+    torch.cuda.synchronize()
+    o2_ref, l2_ref = fa.flash_attention_forward(o1.clone(), d["k"], d["v"], **kw)
+    torch.cuda.synchronize()
+    a = torch.empty_like(o1)
+    b = torch.empty_like(o1)
+    lb = torch.empty_like(l2_ref)
+    for _ in range(4):
+        a.fill_(0.5)   # stale values that the second call must not read
+        fa.flash_attention_forward(d["q"], d["k"], d["v"], out=a, **kw)
+        fa.flash_attention_forward(a, d["k"], d["v"], out=b, lse=lb, **kw)
+        torch.cuda.synchronize()
+        assert fa.fa_check_status() == 0
+        assert torch.equal(b, o2_ref) and torch.equal(lb, l2_ref)
+
+
 # ------------------------------------------------------------ full-size workloads, sampled rows
 
 def sampled_check(p, rows, heads, batches, threshold=0.0):
