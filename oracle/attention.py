@@ -123,6 +123,37 @@ def attention_fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
     return O, LSE
 
 
+def merge_partials(o_parts: np.ndarray, lse_parts: np.ndarray):
+    """Merge attention results computed over disjoint key subsets of each row.
+
+    The pages' blockwise merge (FlashAttention correctness verification,
+    ai6s.net, section "Standard Attention vs FlashAttention: mathematical
+    equivalence", the final merge): block i with row max m_i and row sum l_i
+    enters with weight exp(m_i - m) * l_i / L, L = sum_i exp(m_i - m) * l_i
+    (the page prints "/ l_i" where the sum needs the factor l_i; reading taken:
+    multiply).  With each part carried as its normalised output O_i and its
+    LSE_i = m_i + ln l_i, that weight is exp(LSE_i - m) / L with
+    m = max_i LSE_i and L = sum_i exp(LSE_i - m), and the merged LSE is
+    m + ln L.
+
+    o_parts [n, ..., Dv], lse_parts [n, ...] (float64).  A part with no key
+    carries LSE_i = -inf and weight 0; a row with no key in any part gets
+    O = 0 and LSE = +inf, as the forward does.
+    """
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    m = lse_parts.max(axis=0)
+    empty = ~np.isfinite(m)
+    m_safe = np.where(empty, 0.0, m)
+    w = np.exp(lse_parts - m_safe[None])            # exp(-inf) = 0 for empty parts
+    L = w.sum(axis=0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        wn = np.where(empty[None], 0.0, w / np.where(empty, 1.0, L)[None])
+        lse = np.where(empty, np.inf, m_safe + np.log(np.where(empty, 1.0, L)))
+    o = (wn[..., None] * o_parts).sum(axis=0)
+    return o, lse
+
+
 def _multiplicity(ri, b, h, qlen, kvlen, Skv, nkb, block, mask, kv_block_idx, topk_idx):
     """Integer weight of every (row, key) pair: how many valid slots list the
     key for the row (1 for dense), 0 where masked."""

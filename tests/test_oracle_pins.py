@@ -237,6 +237,48 @@ def test_block_sparse_matches_dense_mask_and_multiplicity():
             assert np.allclose(got[~empty.numpy()], lse.numpy()[~empty.numpy()], atol=1e-13)
 
 
+def _parts_over_block_ranges(q, k, v, scale, mask, cuts, bs):
+    """The oracle over each key-block range [cuts[i], cuts[i+1]) of every row,
+    through its block-list path (a different code path from the dense one):
+    normalised O_i and LSE_i, with -inf for a part that sees no key."""
+    B, H, S, _ = q.shape
+    nqb = S // bs
+    os_, ls_ = [], []
+    for a, b_ in zip(cuts[:-1], cuts[1:]):
+        width = b_ - a
+        idx = np.full((B, H, nqb, width), -1, np.int32)
+        idx[..., :] = np.arange(a, b_, dtype=np.int32)
+        O, L = A.attention_fwd(q, k, v, scale, mask=mask, kv_block_idx=idx, block=bs)
+        os_.append(O)
+        ls_.append(np.where(np.isposinf(L), -np.inf, L))
+    return np.stack(os_), np.stack(ls_)
+
+
+@pytest.mark.parametrize("mask", [A.MASK_NONE, A.MASK_CAUSAL])
+@pytest.mark.parametrize("cuts", [(0, 3, 8), (0, 1, 2, 5, 8), (0, 8)])
+def test_merge_of_key_ranges_equals_full_attention(mask, cuts):
+    """Attention over disjoint key ranges, merged, equals attention over all
+    keys (the pages' blockwise merge); with causal masking some parts of the
+    early rows see no key and must weigh nothing."""
+    bs, S, D = 8, 64, 16
+    q, k, v = rnd((2, 3, S, D), 41, 2.0), rnd((2, 3, S, D), 42), rnd((2, 3, S, D), 43)
+    full_o, full_l = A.attention_fwd(q, k, v, 0.25, mask=mask)
+    o_p, l_p = _parts_over_block_ranges(q, k, v, 0.25, mask, list(cuts), bs)
+    o, l = A.merge_partials(o_p, l_p)
+    assert np.allclose(o, full_o, rtol=1e-12, atol=1e-13)
+    assert np.allclose(l, full_l, rtol=0, atol=1e-12)
+
+
+def test_merge_rows_without_keys():
+    """A row with no key in any part: O = 0, LSE = +inf; a part without keys
+    next to one with keys changes nothing."""
+    o_p = np.stack([np.full((2, 4), 7.0), np.arange(8.0).reshape(2, 4)])
+    l_p = np.array([[-np.inf, -np.inf], [-np.inf, 1.5]])
+    o, l = A.merge_partials(o_p, l_p)
+    assert np.array_equal(o[0], np.zeros(4)) and np.isposinf(l[0])
+    assert np.array_equal(o[1], o_p[1, 1]) and l[1] == 1.5
+
+
 def test_topk_matches_per_token_gather():
     """Top-k (MQA, shared indices): per token, softmax over the gathered keys
     only, with -1 and out-of-range slots ignored."""
