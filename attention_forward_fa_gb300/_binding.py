@@ -62,6 +62,8 @@ def library() -> ctypes.CDLL:
         lib.fa_check_status.argtypes = [ctypes.c_void_p]
         lib.fa_set_wait_timeout_ns.restype = None
         lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_int64]
+        lib.fa_set_max_kv_split.restype = ctypes.c_int
+        lib.fa_set_max_kv_split.argtypes = [ctypes.c_int]
         lib.fa_wait_probe.restype = ctypes.c_int
         lib.fa_wait_probe.argtypes = [ctypes.c_void_p]
         lib.fa_strerror.restype = ctypes.c_char_p
@@ -145,6 +147,11 @@ def fa_check_status(stream=None) -> int:
 
 def fa_set_wait_timeout_ns(ns: int) -> None:
     library().fa_set_wait_timeout_ns(int(ns))
+
+
+def fa_set_max_kv_split(n: int) -> int:
+    """Most KV pieces per unit for under-filled dense problems (1 = never split)."""
+    return library().fa_set_max_kv_split(int(n))
 
 
 def fa_wait_probe(stream=None) -> int:

@@ -33,6 +33,28 @@ std::atomic<int> g_last_cuda{0};
 unsigned long long* g_trace = nullptr;
 #endif
 std::atomic<long long> g_timeout_ns{2000000000LL};
+std::atomic<int> g_max_kv_split{fa::kMaxSplit};   // pieces per unit at most (1: never split)
+
+// Device address of g_noalloc_scratch for the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device (with that device current) and cached.
+static void* noalloc_scratch_address() {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+      g_last_cuda.store((int)e);
+      return nullptr;
+    }
+    addr[dev] = ptr;
+  }
+  return addr[dev];
+}
 
 int cuda_fail(cudaError_t e) {
   g_last_cuda.store((int)e);
@@ -142,6 +164,70 @@ void* scratch_alloc(size_t bytes, cudaStream_t st) {
   void* ptr = nullptr;
   if (cudaMallocAsync(&ptr, bytes, st) != cudaSuccess) return nullptr;
   return ptr;
+}
+
+// Merge of the pieces of split units, the blockwise merge of the pages in LSE
+// form: one warp per output row, O = sum_p exp(LSE_p - LSE) O_p with
+// LSE = m + ln sum_p exp(LSE_p - m), m = max_p LSE_p; a row that no piece saw
+// a key of gets O = 0 and LSE = +inf.  Launched as a programmatic dependent of
+// the tiled kernel: it may be scheduled while that kernel drains and waits for
+// it before reading the pieces.
+template <bool BF16>
+__global__ void __launch_bounds__(256) fa_merge_kernel(const float* __restrict__ part_o,
+                                                       const float* __restrict__ part_lse,
+                                                       void* __restrict__ o,
+                                                       float* __restrict__ lse, long long rows,
+                                                       int Dv, int nsplit) {
+  fa::pdl_launch_dependents();
+  fa::pdl_wait_prior();
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float lp[fa::kMaxSplit];
+  float m = -INFINITY;
+#pragma unroll
+  for (int s = 0; s < fa::kMaxSplit; ++s) {
+    lp[s] = s < nsplit ? part_lse[(size_t)s * rows + row] : -INFINITY;
+    m = fmaxf(m, lp[s]);
+  }
+  const bool empty = !(m > -INFINITY);
+  float w[fa::kMaxSplit];
+  float L = 0.f;
+#pragma unroll
+  for (int s = 0; s < fa::kMaxSplit; ++s) {
+    w[s] = empty ? 0.f : expf(lp[s] - m);   // 0 for a piece without keys
+    L += w[s];
+  }
+  const float inv = empty ? 0.f : 1.f / L;
+  for (int c = 4 * lane; c < Dv; c += 128) {
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < fa::kMaxSplit; ++s) {
+      if (w[s] == 0.f) continue;
+      const float4 x = *reinterpret_cast<const float4*>(part_o + ((size_t)s * rows + row) * Dv + c);
+      a.x = fmaf(w[s], x.x, a.x);
+      a.y = fmaf(w[s], x.y, a.y);
+      a.z = fmaf(w[s], x.z, a.z);
+      a.w = fmaf(w[s], x.w, a.w);
+    }
+    uint2 pk;
+    pk.x = BF16 ? fa::pack_bf16x2(a.x * inv, a.y * inv) : fa::pack_f16x2(a.x * inv, a.y * inv);
+    pk.y = BF16 ? fa::pack_bf16x2(a.z * inv, a.w * inv) : fa::pack_f16x2(a.z * inv, a.w * inv);
+    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(o) + ((size_t)row * Dv + c) * 2) = pk;
+  }
+  if (lane == 0) lse[row] = empty ? INFINITY : m + logf(L);
+}
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count() {
+  static int sms[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) sms[dev] = n;
+  }
+  return sms[dev];
 }
 
 // Launch with programmatic stream serialisation: the kernel may be scheduled
@@ -298,7 +384,7 @@ int run_topk(const void* q, const void* k16, void* o, float* lse, int B, int Hq,
 int run_tiled(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
               int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
               const int32_t* seqlens, const fa_block_sparse_t* kv_block_idx,
-              float rescale_threshold, int* status, cudaStream_t st) {
+              float rescale_threshold, int* status, cudaStream_t st, bool may_alloc) {
   const int mask = mask_mode & 0xF;
   const bool fp16 = (mask_mode & FA_DTYPE_FP16) != 0;
   const bool conv = !fp16 && !(mask_mode & FA_V_FP16);   // V arrives as bf16
@@ -350,14 +436,59 @@ int run_tiled(const void* q, const void* k, const void* v, void* o, float* lse, 
   const long long units = (long long)prm.units_per_q * prm.n_qpos;
   if (units > 0x7FFFFFFF) return FA_ERR_SHAPE;
 
-  if (D == 128) {
-    if (fp16) return launch_tiled<128, false, 4, false>(prm, (int)units, st);
-    return conv ? launch_tiled<128, true, 4, true>(prm, (int)units, st)
-                : launch_tiled<128, true, 4, false>(prm, (int)units, st);
+  // Split-KV when the units cannot fill half the GPU: each unit's KV tiles are
+  // cut into up to g_max_kv_split pieces of at least two tiles, one CTA each;
+  // the pieces leave O / l and the LSE in fp32 scratch and a merge kernel
+  // combines them (dense problems only).
+  prm.kv_split = 1;
+  const int sms = sm_count();
+  const int n_kb = (Skv + fa::kBN - 1) / fa::kBN;
+  if (!kv_block_idx && sms > 0 && units * 2 <= sms) {
+    int ks = std::min(g_max_kv_split.load(), (int)((sms + units - 1) / units));
+    ks = std::min(ks, n_kb / 2);
+    if (ks >= 2) prm.kv_split = ks;
   }
-  if (fp16) return launch_tiled<64, false, 6, false>(prm, (int)units, st);
-  return conv ? launch_tiled<64, true, 6, true>(prm, (int)units, st)
-              : launch_tiled<64, true, 6, false>(prm, (int)units, st);
+  void* parts = nullptr;
+  bool parts_owned = false;
+  const size_t rows_all = (size_t)B * Hq * Sq;
+  if (prm.kv_split > 1) {
+    const size_t o_bytes = (size_t)prm.kv_split * rows_all * Dv * 4;
+    const size_t bytes = o_bytes + (size_t)prm.kv_split * rows_all * 4;
+    if (may_alloc) {
+      parts = scratch_alloc(bytes, st);
+      parts_owned = parts != nullptr;
+    } else if (bytes <= kNoAllocScratchBytes) {
+      parts = noalloc_scratch_address();
+    }
+    if (parts) {
+      prm.part_o = static_cast<float*>(parts);
+      prm.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(parts) + o_bytes);
+    } else {
+      prm.kv_split = 1;   // no scratch: run unsplit
+    }
+  }
+  const int grid = (int)std::min<long long>(units * prm.kv_split, 0x7FFFFFFF);
+  int rc;
+  if (D == 128) {
+    if (fp16) rc = launch_tiled<128, false, 4, false>(prm, grid, st);
+    else rc = conv ? launch_tiled<128, true, 4, true>(prm, grid, st)
+                   : launch_tiled<128, true, 4, false>(prm, grid, st);
+  } else {
+    if (fp16) rc = launch_tiled<64, false, 6, false>(prm, grid, st);
+    else rc = conv ? launch_tiled<64, true, 6, true>(prm, grid, st)
+                   : launch_tiled<64, true, 6, false>(prm, grid, st);
+  }
+  if (rc == FA_OK && prm.kv_split > 1) {
+    const unsigned blocks = (unsigned)((rows_all + 7) / 8);
+    const cudaError_t e =
+        fp16 ? launch_dependent(fa_merge_kernel<false>, blocks, 256, 0, st, prm.part_o,
+                                prm.part_lse, o, lse, (long long)rows_all, Dv, prm.kv_split)
+             : launch_dependent(fa_merge_kernel<true>, blocks, 256, 0, st, prm.part_o,
+                                prm.part_lse, o, lse, (long long)rows_all, Dv, prm.kv_split);
+    if (e != cudaSuccess) rc = cuda_fail(e);
+  }
+  if (parts_owned) cudaFreeAsync(parts, st);
+  return rc;
 }
 
 // One warp waits, with the kernels' bounded wait, on an mbarrier that nothing
@@ -394,7 +525,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 
   if (!topk_idx)   // a bf16 V is converted inside the tiled kernel
     return run_tiled(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
-                     kv_block_idx, rescale_threshold, status, st);
+                     kv_block_idx, rescale_threshold, status, st, /*may_alloc=*/true);
   // top-k: an fp16 copy of the bf16 key latent (V is part of it) in
   // stream-ordered scratch, freed on the same stream
   const size_t nv = (size_t)B * Skv * D;
@@ -419,26 +550,6 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
                   rescale_threshold, status, st);
 }
 
-// Device address of g_noalloc_scratch for the current device.  In host code the
-// array's name is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and cached.
-static void* noalloc_scratch_address() {
-  static std::mutex mu;
-  static void* addr[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* ptr = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (e != cudaSuccess) {
-      g_last_cuda.store((int)e);
-      return nullptr;
-    }
-    addr[dev] = ptr;
-  }
-  return addr[dev];
-}
 
 int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                    int Hq, int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
@@ -451,9 +562,10 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* status = status_ptr();
   if (!status) return cuda_fail(cudaGetLastError());
-  if (!topk_idx)   // no scratch: a bf16 V is converted inside the tiled kernel
+  if (!topk_idx)   // a bf16 V is converted inside the tiled kernel; split-KV pieces
+                   // use the fixed scratch (unsplit when they do not fit)
     return run_tiled(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
-                     kv_block_idx, rescale_threshold, status, st);
+                     kv_block_idx, rescale_threshold, status, st, /*may_alloc=*/false);
   const size_t nv = (size_t)B * Skv * D;
   if (!fp16 && nv * 2 > kNoAllocScratchBytes) return FA_ERR_SCRATCH;
   void* k16 = const_cast<void*>(k);
@@ -496,6 +608,12 @@ int fa_check_status(void* stream) {
 }
 
 void fa_set_wait_timeout_ns(int64_t ns) { g_timeout_ns.store(ns > 0 ? ns : 2000000000LL); }
+
+int fa_set_max_kv_split(int n) {
+  if (n < 1 || n > fa::kMaxSplit) return FA_ERR_SHAPE;
+  g_max_kv_split.store(n);
+  return FA_OK;
+}
 
 int fa_wait_probe(void* stream) {
   int* status = status_ptr();

@@ -52,6 +52,7 @@ static_assert(kSoftmaxRegs % 8 == 0 && kCorrRegs % 8 == 0 && kOtherRegs % 8 == 0
 static_assert(kRegsNeeded <= 65536 / kTiledThreads, "register split exceeds the register file");
 constexpr int kMaxSel = 512;      // longest block list a CTA stages in smem
 constexpr int kHiLoKeys = 256;    // rows with fewer valid keys use the hi+lo P split
+constexpr int kMaxSplit = 8;      // most pieces a unit's KV tiles are split into
 // hardware named barriers (0 is __syncthreads): 1-2 scheduler -> issuer release
 // of groups 0 and 1, 3-4 issuer -> scheduler "group issued", 5-6 "P ready" of
 // slot t (its softmax warps and the scheduler -> issuer: P written and the
@@ -76,6 +77,9 @@ struct TiledParams {
   int n_qt;         // ceil(Sq / 128)
   int units_per_q;  // units that share one query position
   int n_qpos;       // query positions (tile pairs or tiles)
+  int kv_split;     // pieces per unit along the KV tiles (1: no split); dense only
+  float* part_o;    // kv_split > 1: O / l of every piece, fp32 [kv_split][B*Hq*Sq][Dv]
+  float* part_lse;  // kv_split > 1: LSE of every piece (-inf: no key) [kv_split][B*Hq*Sq]
   float scale, scale_log2, threshold;
   long long timeout_ns;
   int* status;
@@ -175,6 +179,20 @@ __device__ __forceinline__ int dense_tiles(int qt, int n_qt, int q_len, int kv_l
   return nkv;
 }
 
+// One piece of a unit split along its KV tiles: the slots' ranges [0, n0) and
+// [0, n1) are cut at the same tile boundaries, every ceil(max(n0, n1) /
+// kv_split) tiles; a slot's piece is [lo, min(n, hi)), possibly empty.
+struct Piece {
+  int lo, hi;
+};
+__device__ __forceinline__ Piece piece_range(int n0, int n1, int piece, int kv_split) {
+  const int nmax = n0 > n1 ? n0 : n1;
+  const int chunk = (nmax + kv_split - 1) / kv_split;
+  const int lo = min(piece * chunk, nmax);
+  return Piece{lo, min(lo + chunk, nmax)};
+}
+__device__ __forceinline__ int piece_count(int n, Piece pc) { return max(0, min(n, pc.hi) - pc.lo); }
+
 // The order in which the MMA warp consumes K / V tiles, as a numbered event
 // list: 0 = QK(0,0), 1 = QK(1,0), then per iteration j four events PV(0,j),
 // QK(0,j+1), PV(1,j), QK(1,j+1).  `load` marks the first use of a tile (a
@@ -256,7 +274,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   const int lane = tid & 31;
 
   // ---------------------------------------------------------------- unit
-  const int u = blockIdx.x;
+  const int u = blockIdx.x / p.kv_split;   // pieces of one unit are neighbours
+  const int piece = blockIdx.x - u * p.kv_split;
   const int qpos = p.n_qpos - 1 - u / p.units_per_q;   // heaviest query positions first
   const int bh = u % p.units_per_q;
   int b, h0, h1, qt0, qt1;
@@ -307,9 +326,13 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     tma_prefetch_desc(&p.tm_q);
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
+    s_slot[4] = 0;   // first KV tile of the piece
     if (!sparse) {
-      const int e0 = dense_tiles(qt0, p.n_qt, q_len, kv_len, p.mask);
-      const int e1 = dense_tiles(qt1, p.n_qt, q_len, kv_len, p.mask);
+      const int f0 = dense_tiles(qt0, p.n_qt, q_len, kv_len, p.mask);
+      const int f1 = dense_tiles(qt1, p.n_qt, q_len, kv_len, p.mask);
+      const Piece pc = piece_range(f0, f1, piece, p.kv_split);
+      const int e0 = piece_count(f0, pc), e1 = piece_count(f1, pc);
+      s_slot[4] = pc.lo;
       for (int t = 0; t < 2; ++t) {
         if ((t ? e1 : e0) == 0) continue;
         mbar_arrive_expect_tx(BAR_QFULL(t), SM::kQBytes);
@@ -321,7 +344,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           // the first ring load is K tile 0 for Q.K^T(0,0) in every event order
           mbar_arrive_expect_tx(BAR_FULL(0), SM::kStageBytes);
           for (int bx = 0; bx < kBoxes; ++bx)
-            tma_load_3d(sStage + bx * (kBN * 128), &p.tm_k, BAR_FULL(0), 64 * bx, 0,
+            tma_load_3d(sStage + bx * (kBN * 128), &p.tm_k, BAR_FULL(0), 64 * bx, pc.lo * kBN,
                         b * p.Hkv + kvh);
           early = 1;
         }
@@ -342,12 +365,10 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     int n = 0, hilo = 0;
     const bool live = qt < p.n_qt && q0 < q_len && kv_len > 0;
     if (live && !sparse) {
-      int nkv = (kv_len + kBN - 1) / kBN;
-      if (p.mask == 1) {
-        const int q_last = min(q0 + kBM - 1, q_len - 1);
-        nkv = min(nkv, q_last / kBN + 1);
-      }
-      n = nkv;
+      // this slot's tiles of the piece (both slots' counts fix the cuts)
+      const int f0 = dense_tiles(qt0, p.n_qt, q_len, kv_len, p.mask);
+      const int f1 = dense_tiles(qt1, p.n_qt, q_len, kv_len, p.mask);
+      n = piece_count(t ? f1 : f0, piece_range(f0, f1, piece, p.kv_split));
       const int min_keys = (p.mask == 1) ? min(q0 + 1, kv_len) : kv_len;
       hilo = min_keys < kHiLoKeys;
     } else if (live && sparse) {
@@ -384,6 +405,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
   const int n0 = s_slot[0], n1 = s_slot[1];
+  const int kv_lo = s_slot[4];   // first KV tile of the piece (dense)
   const bool shared_kv = !sparse ? (n0 >= 1 && n0 <= n1) : false;
   const WaitCtx wc{s_abort, p.status, p.timeout_ns};
 
@@ -422,7 +444,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       }
       if (row == 0) FA_TR(1, t, j);
       tc_fence_after();
-      const int kvt = sparse ? s_list[t * kMaxSel + j] : j;
+      const int kvt = sparse ? s_list[t * kMaxSel + j] : kv_lo + j;
       const int kbase = kvt * kBN;
       const bool causal_here = (p.mask == 1) || (p.mask == 2 && kvt == qt);
       const bool need_mask =
@@ -622,6 +644,35 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       const bool write = qi < p.Sq;
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       const uint32_t tO = tmem + 256u + 128u * t + lane_off;
+      if (p.kv_split > 1) {
+        // one piece of a split unit: its O / l in fp32 and its LSE (-inf when
+        // the piece saw no key of the row) for the merge kernel
+        const size_t rows_all = (size_t)p.B * p.Hq * p.Sq;
+        const size_t r = (size_t)(b * p.Hq + h) * p.Sq + (write ? qi : 0);
+        float4* dst = reinterpret_cast<float4*>(p.part_o + ((size_t)piece * rows_all + r) * Dv);
+#pragma unroll 2
+        for (int cc = 0; cc < Dv / 16; ++cc) {
+          uint32_t rr[16];
+          if (acc) {
+            tmem_ld16(tO + 16 * cc, rr);   // warp-collective: all lanes, even rows past Sq
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) rr[i] = 0;
+          }
+          if (write) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[4 * cc + i] = make_float4(
+                  __uint_as_float(rr[4 * i]) * inv_l, __uint_as_float(rr[4 * i + 1]) * inv_l,
+                  __uint_as_float(rr[4 * i + 2]) * inv_l, __uint_as_float(rr[4 * i + 3]) * inv_l);
+          }
+        }
+        if (write)
+          p.part_lse[(size_t)piece * rows_all + r] = (l > 0.f) ? __fmaf_rn(m, p.scale, __logf(l)) : -INFINITY;
+        if (row == 0) FA_TR(11, t, 0);
+        continue;
+      }
       // O / l into the slot's Q buffer (its last Q.K^T finished before the last
       // P.V) in the 128-byte-swizzle layout of the output's tensor map, then one
       // thread stores the tile with TMA (rows past Sq are clipped)
@@ -687,7 +738,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         ++ld;
         if (ld <= early) continue;   // issued before the setup barrier
         if (!wait_bar(BAR_EMPTY(s), (f & 1) ^ 1, wc)) break;
-        const int kvt = sparse ? s_list[ev.t * kMaxSel + ev.j] : ev.j;
+        const int kvt = sparse ? s_list[ev.t * kMaxSel + ev.j] : kv_lo + ev.j;
         FA_TR(5, ev.t, ev.j);
         mbar_arrive_expect_tx(BAR_FULL(s), SM::kStageBytes);
         const CUtensorMap* tm = ev.pv ? &p.tm_v : &p.tm_k;

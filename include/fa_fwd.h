@@ -36,11 +36,18 @@
  *     synchronously and nothing is launched.  Device-side errors are
  *     reported later through fa_check_status().
  *   - The dense / GQA / block-sparse paths allocate nothing (a bf16 V is
- *     converted to fp16 tile by tile inside the kernel).  The top-k path with
- *     a bf16 key latent converts the latent to fp16 into stream-ordered
- *     scratch (cudaMallocAsync from the device's default memory pool,
- *     released on `stream` after use); fa_fwd_noalloc uses a fixed array
- *     instead and allocates nothing at all.
+ *     converted to fp16 tile by tile inside the kernel), except a dense
+ *     problem with too few (batch, head, query-tile) units to fill half the
+ *     GPU: its units' KV tiles are split into up to fa_set_max_kv_split()
+ *     pieces whose partial O / l and LSE (fp32) go to stream-ordered scratch
+ *     and are merged by a second kernel (the blockwise merge of
+ *     "FlashAttention correctness verification", ai6s.net, section "Standard
+ *     Attention vs FlashAttention: mathematical equivalence", in log-sum-exp
+ *     form).  The top-k path with a bf16 key latent converts the latent to
+ *     fp16 into stream-ordered scratch.  Scratch comes from cudaMallocAsync
+ *     on the device's default memory pool and is released on `stream` after
+ *     use; fa_fwd_noalloc uses a fixed array instead and allocates nothing at
+ *     all (a split that does not fit it runs unsplit).
  */
 #ifndef FA_FWD_H_
 #define FA_FWD_H_
@@ -203,6 +210,12 @@ int fa_check_status(void* stream);
 /* Sets the limit of every bounded on-chip wait (nanoseconds, default 2e9);
  * values <= 0 restore the default.  Affects launches made after the call. */
 void fa_set_wait_timeout_ns(int64_t ns);
+
+/* Most pieces a dense unit's KV tiles are split into when the problem has
+ * too few units to fill half the GPU (default 8, the maximum; 1 never
+ * splits).  Pieces have at least two KV tiles.  Returns FA_OK, or
+ * FA_ERR_SHAPE for n outside [1, 8].  Affects calls made after it. */
+int fa_set_max_kv_split(int n);
 
 /* Failure-detection probe: one warp waits, with the same bounded wait as the
  * attention kernels, on an mbarrier that nothing ever arrives at, so that the

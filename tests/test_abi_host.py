@@ -29,6 +29,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("fa_fwd", "fa_check_status", "fa_strerror", "fa_set_wait_timeout_ns",
+              "fa_set_max_kv_split",
               "fa_last_cuda_error", "fa_last_cuda_error_string"):
         assert n in names
 
@@ -94,6 +95,13 @@ def test_topk_without_latent_is_unsupported(lib):
 def test_timeout_setter(lib):
     B.fa_set_wait_timeout_ns(5_000_000)
     B.fa_set_wait_timeout_ns(0)   # back to the default
+
+
+def test_kv_split_setter_range(lib):
+    assert B.fa_set_max_kv_split(0) == -2
+    assert B.fa_set_max_kv_split(9) == -2
+    assert B.fa_set_max_kv_split(1) == 0
+    assert B.fa_set_max_kv_split(8) == 0   # back to the default
 
 
 @pytest.mark.parametrize("args,code", [

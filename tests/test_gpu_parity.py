@@ -115,6 +115,37 @@ def test_repeated_calls_are_deterministic():
     assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
 
 
+SPLIT_CASES = {
+    # (units of (batch, head or head pair, query-tile pair) well under half the SMs)
+    "causal_mha": lambda: W.dense(name="split_causal", B=1, Hq=2, Sq=2048, D=128,
+                                  mask=W.MASK_CAUSAL, seed=51),
+    "fp16_d64_tail": lambda: W.dense(name="split_d64", B=1, Hq=1, Sq=1500, D=64, dtype="fp16",
+                                     mask=W.MASK_NONE, seed=52),
+    "gqa_pairs": lambda: W.dense(name="split_gqa", B=1, Hq=4, Hkv=2, Sq=1024, D=128,
+                                 mask=W.MASK_CAUSAL, seed=53),
+    "seqlens": lambda: W.dense(name="split_ragged", B=2, Hq=2, Sq=2048, D=128,
+                               mask=W.MASK_CAUSAL, seqlens=[2048, 700], seed=54),
+    "cross": lambda: W.dense(name="split_cross", B=1, Hq=2, Sq=300, Skv=3000, D=128,
+                             mask=W.MASK_CAUSAL, seed=55),
+}
+
+
+@pytest.mark.parametrize("max_split", [8, 1])
+@pytest.mark.parametrize("case", sorted(SPLIT_CASES))
+def test_split_kv_small_grids(case, max_split):
+    """Problems with too few units to fill the GPU split each unit's KV tiles
+    into pieces that a second kernel merges (the pages' blockwise merge); with
+    the split turned off (at most 1 piece) they run unsplit.  Both match the
+    oracle."""
+    import attention_forward_fa_gb300 as fa
+    p = SPLIT_CASES[case]()
+    assert fa.fa_set_max_kv_split(max_split) == 0
+    try:
+        full_check(p, threshold=8.0 if case == "gqa_pairs" else 0.0)
+    finally:
+        fa.fa_set_max_kv_split(8)
+
+
 def test_chained_calls_wait_for_the_previous_call():
     """Two calls back to back on one stream, the second taking the first's
     output as its queries.  The second kernel may be scheduled while the first

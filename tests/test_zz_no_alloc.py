@@ -1,10 +1,12 @@
 """fa_fwd_noalloc: the entry point for callers that cannot let a library
 allocate device memory (programs that hand out all device memory from their
 own arena, latency-critical call sites where a driver allocation is not
-acceptable).  The dense, GQA and block-sparse paths allocate nothing anyway
-(a bf16 V is converted inside the kernel); the top-k path's fp16 copy of the
-bf16 key latent goes to a fixed 32 MiB array inside the library instead of
-stream-ordered scratch.  Results must equal fa_fwd's on the same inputs,
+acceptable).  The dense, GQA and block-sparse paths allocate nothing for
+problems that fill the GPU (a bf16 V is converted inside the kernel); a dense
+problem with few units splits its KV tiles into pieces whose partial results
+(and the top-k path's fp16 copy of a bf16 key latent) go to a fixed 32 MiB
+array inside the library instead of stream-ordered scratch.  The dense case
+below has 24 units and runs split into 3 pieces.  Results must equal fa_fwd's on the same inputs,
 including on a second call, which finds the previous call's data still in the
 shared array.
 
