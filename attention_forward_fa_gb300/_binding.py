@@ -55,6 +55,8 @@ def library() -> ctypes.CDLL:
             ctypes.POINTER(fa_topk_t), ctypes.c_float, ctypes.c_void_p]
         lib.fa_fwd_noalloc.restype = ctypes.c_int
         lib.fa_fwd_noalloc.argtypes = lib.fa_fwd.argtypes
+        lib.fa_fwd_o_lo.restype = ctypes.c_int
+        lib.fa_fwd_o_lo.argtypes = lib.fa_fwd.argtypes[:4] + [ctypes.c_void_p] + lib.fa_fwd.argtypes[4:]
         lib.fa_convert_v_fp16.restype = ctypes.c_int
         lib.fa_convert_v_fp16.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                           ctypes.c_void_p]
@@ -116,6 +118,25 @@ def fa_fwd(q, k, v, o, lse, B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int
                       float(rescale_threshold), _stream(stream))
 
 
+def fa_fwd_o_lo(q, k, v, o, o_lo, lse, B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int,
+                Dv: int, scale: float, mask_mode: int, seqlens=None, kv_block_idx=None,
+                topk_idx=None, rescale_threshold: float = 0.0, stream=None) -> int:
+    """fa_fwd that also writes o_lo = fp32(O) - O rounded to o's type (same
+    type and layout as o).  Same arguments as fa_fwd plus o_lo after o."""
+    lib = library()
+    bs = None
+    if kv_block_idx is not None:
+        idx, max_sel, block, sb, sh = kv_block_idx
+        bs = ctypes.pointer(fa_block_sparse_t(_ptr(idx), max_sel, block, sb, sh))
+    tk = None
+    if topk_idx is not None:
+        idx, topk, sb = topk_idx
+        tk = ctypes.pointer(fa_topk_t(_ptr(idx), topk, sb))
+    return lib.fa_fwd_o_lo(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(o_lo), _ptr(lse), B, Hq, Hkv,
+                           Sq, Skv, D, Dv, float(scale), int(mask_mode), _ptr(seqlens), bs, tk,
+                           float(rescale_threshold), _stream(stream))
+
+
 def fa_fwd_noalloc(q, k, v, o, lse, B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int,
                    Dv: int, scale: float, mask_mode: int, seqlens=None, kv_block_idx=None,
                    topk_idx=None, rescale_threshold: float = 0.0, stream=None) -> int:
@@ -170,13 +191,14 @@ def _raise(code: int):
 def flash_attention_forward(q, k, v=None, *, scale: Optional[float] = None, causal: bool = False,
                             mask_mode: Optional[int] = None, seqlens=None, block_idx=None,
                             topk_idx=None, rescale_threshold: float = 0.0, out=None, lse=None,
-                            stream=None):
+                            o_lo=None, stream=None):
     """Allocating convenience wrapper over fa_fwd.
 
     q [B,Hq,Sq,D], k [B,Hkv,Skv,D], v [B,Hkv,Skv,Dv] (or None with top-k and a
     shared latent), bf16 or fp16 CUDA tensors.  block_idx: int32 tensor
     [B, Hq or 1, ceil(Sq/128), max_sel]; topk_idx: int32 [B, Sq, W].
-    Returns (o, lse)."""
+    o_lo: True (allocate) or a tensor like out to also receive the output's
+    rounding residual (fa_fwd_o_lo).  Returns (o, lse), or (o, lse, o_lo)."""
     import torch
     if q.dtype not in (torch.bfloat16, torch.float16):
         raise TypeError("q, k, v must be bf16 or fp16")
@@ -210,7 +232,14 @@ def flash_attention_forward(q, k, v=None, *, scale: Optional[float] = None, caus
         tk = (topk_idx, topk_idx.shape[-1], topk_idx.shape[-2] * topk_idx.shape[-1])
     if seqlens is not None:
         assert seqlens.dtype == torch.int32 and seqlens.is_cuda
-    code = fa_fwd(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens, bs, tk,
-                  rescale_threshold, stream)
+    if o_lo is None or o_lo is False:
+        code = fa_fwd(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens, bs,
+                      tk, rescale_threshold, stream)
+        _raise(code)
+        return out, lse
+    if o_lo is True:
+        o_lo = torch.empty_like(out)
+    code = fa_fwd_o_lo(q, k, v, out, o_lo, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode,
+                       seqlens, bs, tk, rescale_threshold, stream)
     _raise(code)
-    return out, lse
+    return out, lse, o_lo

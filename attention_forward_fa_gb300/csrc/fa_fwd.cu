@@ -176,6 +176,7 @@ template <bool BF16>
 __global__ void __launch_bounds__(256) fa_merge_kernel(const float* __restrict__ part_o,
                                                        const float* __restrict__ part_lse,
                                                        void* __restrict__ o,
+                                                       void* __restrict__ o_lo,
                                                        float* __restrict__ lse, long long rows,
                                                        int Dv, int nsplit) {
   fa::pdl_launch_dependents();
@@ -210,10 +211,14 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const float* __restrict__
       a.z = fmaf(w[s], x.z, a.z);
       a.w = fmaf(w[s], x.w, a.w);
     }
+    const float x0 = a.x * inv, x1 = a.y * inv, x2 = a.z * inv, x3 = a.w * inv;
     uint2 pk;
-    pk.x = BF16 ? fa::pack_bf16x2(a.x * inv, a.y * inv) : fa::pack_f16x2(a.x * inv, a.y * inv);
-    pk.y = BF16 ? fa::pack_bf16x2(a.z * inv, a.w * inv) : fa::pack_f16x2(a.z * inv, a.w * inv);
+    pk.x = BF16 ? fa::pack_bf16x2(x0, x1) : fa::pack_f16x2(x0, x1);
+    pk.y = BF16 ? fa::pack_bf16x2(x2, x3) : fa::pack_f16x2(x2, x3);
     *reinterpret_cast<uint2*>(static_cast<uint8_t*>(o) + ((size_t)row * Dv + c) * 2) = pk;
+    if (o_lo)
+      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(o_lo) + ((size_t)row * Dv + c) * 2) =
+          make_uint2(fa::pack_residual_x2(x0, x1, pk.x, BF16), fa::pack_residual_x2(x2, x3, pk.y, BF16));
   }
   if (lane == 0) lse[row] = empty ? INFINITY : m + logf(L);
 }
@@ -347,9 +352,9 @@ int launch_mla(const fa::MlaParams& prm, long long units, cudaStream_t st) {
 // Top-k sparse MLA forward on validated arguments; `k16` is the key latent
 // [B, Skv, 576] in fp16 (the caller's for fp16 inputs or with FA_V_FP16, a
 // converted copy otherwise).
-int run_topk(const void* q, const void* k16, void* o, float* lse, int B, int Hq, int Sq, int Skv,
-             float scale, int mask_mode, const int32_t* seqlens, const fa_topk_t* tk,
-             float rescale_threshold, int* status, cudaStream_t st) {
+int run_topk(const void* q, const void* k16, void* o, void* o_lo, float* lse, int B, int Hq,
+             int Sq, int Skv, float scale, int mask_mode, const int32_t* seqlens,
+             const fa_topk_t* tk, float rescale_threshold, int* status, cudaStream_t st) {
   const bool fp16 = (mask_mode & FA_DTYPE_FP16) != 0;
   fa::MlaParams prm;
   std::memset(&prm, 0, sizeof(prm));
@@ -359,6 +364,7 @@ int run_topk(const void* q, const void* k16, void* o, float* lse, int B, int Hq,
   prm.kl = static_cast<const uint16_t*>(k16);
   prm.q_rows = (int)q_rows;
   prm.o = o;
+  prm.o_lo = o_lo;
   prm.lse = lse;
   prm.seqlens = seqlens;
   prm.topk = tk->idx;
@@ -381,8 +387,8 @@ int run_topk(const void* q, const void* k16, void* o, float* lse, int B, int Hq,
 
 // Tiled forward on validated arguments.  `v` is fp16 (fp16 inputs, or a bf16
 // call with FA_V_FP16), else bf16, converted tile by tile inside the kernel.
-int run_tiled(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
-              int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
+int run_tiled(const void* q, const void* k, const void* v, void* o, void* o_lo, float* lse, int B,
+              int Hq, int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
               const int32_t* seqlens, const fa_block_sparse_t* kv_block_idx,
               float rescale_threshold, int* status, cudaStream_t st, bool may_alloc) {
   const int mask = mask_mode & 0xF;
@@ -396,6 +402,7 @@ int run_tiled(const void* q, const void* k, const void* v, void* o, float* lse, 
       !encode_3d(&prm.tm_o, o, fp16, Dv, Sq, (uint64_t)B * Hq, fa::kBM))
     return cuda_fail(cudaErrorInvalidValue);
   prm.o = o;
+  prm.o_lo = o_lo;
   prm.lse = lse;
   prm.seqlens = seqlens;
   if (kv_block_idx) {
@@ -482,9 +489,9 @@ int run_tiled(const void* q, const void* k, const void* v, void* o, float* lse, 
     const unsigned blocks = (unsigned)((rows_all + 7) / 8);
     const cudaError_t e =
         fp16 ? launch_dependent(fa_merge_kernel<false>, blocks, 256, 0, st, prm.part_o,
-                                prm.part_lse, o, lse, (long long)rows_all, Dv, prm.kv_split)
+                                prm.part_lse, o, o_lo, lse, (long long)rows_all, Dv, prm.kv_split)
              : launch_dependent(fa_merge_kernel<true>, blocks, 256, 0, st, prm.part_o,
-                                prm.part_lse, o, lse, (long long)rows_all, Dv, prm.kv_split);
+                                prm.part_lse, o, o_lo, lse, (long long)rows_all, Dv, prm.kv_split);
     if (e != cudaSuccess) rc = cuda_fail(e);
   }
   if (parts_owned) cudaFreeAsync(parts, st);
@@ -507,14 +514,11 @@ __global__ void fa_wait_probe_kernel(int* status, long long timeout_ns) {
   (void)fa::wait_bar(fa::smem_u32(&bar), 0, wc);
 }
 
-}  // namespace
-
-extern "C" {
-
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
-           int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
-           const int32_t* seqlens, const fa_block_sparse_t* kv_block_idx,
-           const fa_topk_t* topk_idx, float rescale_threshold, void* stream) {
+// fa_fwd and fa_fwd_o_lo on validated arguments (o_lo: the residual output or null).
+int fwd_impl(const void* q, const void* k, const void* v, void* o, void* o_lo, float* lse, int B,
+             int Hq, int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
+             const int32_t* seqlens, const fa_block_sparse_t* kv_block_idx,
+             const fa_topk_t* topk_idx, float rescale_threshold, void* stream) {
   const int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
                           kv_block_idx, topk_idx, rescale_threshold);
   if (rc != FA_OK) return rc;
@@ -524,8 +528,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   if (!status) return cuda_fail(cudaGetLastError());
 
   if (!topk_idx)   // a bf16 V is converted inside the tiled kernel
-    return run_tiled(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
-                     kv_block_idx, rescale_threshold, status, st, /*may_alloc=*/true);
+    return run_tiled(q, k, v, o, o_lo, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode,
+                     seqlens, kv_block_idx, rescale_threshold, status, st, /*may_alloc=*/true);
   // top-k: an fp16 copy of the bf16 key latent (V is part of it) in
   // stream-ordered scratch, freed on the same stream
   const size_t nv = (size_t)B * Skv * D;
@@ -546,9 +550,32 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
       if (ptr) cudaFreeAsync(ptr, st);
     }
   } guard{fp16 ? nullptr : k16, st};
-  return run_topk(q, k16, o, lse, B, Hq, Sq, Skv, scale, mask_mode, seqlens, topk_idx,
+  return run_topk(q, k16, o, o_lo, lse, B, Hq, Sq, Skv, scale, mask_mode, seqlens, topk_idx,
                   rescale_threshold, status, st);
 }
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+           int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
+           const int32_t* seqlens, const fa_block_sparse_t* kv_block_idx,
+           const fa_topk_t* topk_idx, float rescale_threshold, void* stream) {
+  return fwd_impl(q, k, v, o, nullptr, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
+                  kv_block_idx, topk_idx, rescale_threshold, stream);
+}
+
+int fa_fwd_o_lo(const void* q, const void* k, const void* v, void* o, void* o_lo, float* lse,
+                int B, int Hq, int Hkv, int Sq, int Skv, int D, int Dv, float scale,
+                int mask_mode, const int32_t* seqlens, const fa_block_sparse_t* kv_block_idx,
+                const fa_topk_t* topk_idx, float rescale_threshold, void* stream) {
+  if (!o_lo) return FA_ERR_NULL;
+  if (!aligned(o_lo, 16)) return FA_ERR_ALIGN;
+  return fwd_impl(q, k, v, o, o_lo, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
+                  kv_block_idx, topk_idx, rescale_threshold, stream);
+}
+
 
 
 int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -564,8 +591,8 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* 
   if (!status) return cuda_fail(cudaGetLastError());
   if (!topk_idx)   // a bf16 V is converted inside the tiled kernel; split-KV pieces
                    // use the fixed scratch (unsplit when they do not fit)
-    return run_tiled(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
-                     kv_block_idx, rescale_threshold, status, st, /*may_alloc=*/false);
+    return run_tiled(q, k, v, o, nullptr, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode,
+                     seqlens, kv_block_idx, rescale_threshold, status, st, /*may_alloc=*/false);
   const size_t nv = (size_t)B * Skv * D;
   if (!fp16 && nv * 2 > kNoAllocScratchBytes) return FA_ERR_SCRATCH;
   void* k16 = const_cast<void*>(k);
@@ -577,7 +604,7 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* 
     const int rcv = convert_v(k, k16, nv, status, st);
     if (rcv != FA_OK) return rcv;
   }
-  return run_topk(q, k16, o, lse, B, Hq, Sq, Skv, scale, mask_mode, seqlens, topk_idx,
+  return run_topk(q, k16, o, nullptr, lse, B, Hq, Sq, Skv, scale, mask_mode, seqlens, topk_idx,
                   rescale_threshold, status, st);
 }
 

@@ -67,6 +67,7 @@ struct MlaParams {
   CUtensorMap tm_q;   // 3-D (D, Sq, B*Hq), box 64 x 1 x 128 heads
   const uint16_t* kl; // fp16 key latent [B, Skv, 576]
   void* o;
+  void* o_lo;       // optional: o's rounding residual, same type and layout (or null)
   float* lse;
   const int* seqlens;
   const int* topk;
@@ -469,16 +470,21 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       }
       if (write) {
         uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cc);
+        uint4* dst_lo = p.o_lo ? reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o_lo) +
+                                                          (orow - static_cast<uint16_t*>(p.o)) + 32 * cc)
+                               : nullptr;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          uint32_t w[4];
+          uint32_t w[4], wl[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float a0 = __uint_as_float(o32[8 * i + 2 * e]) * inv_l;
             const float a1 = __uint_as_float(o32[8 * i + 2 * e + 1]) * inv_l;
             w[e] = kBF16 ? pack_bf16x2(a0, a1) : pack_f16x2(a0, a1);
+            wl[e] = pack_residual_x2(a0, a1, w[e], kBF16);
           }
           dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+          if (dst_lo) dst_lo[i] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
         }
       }
     }

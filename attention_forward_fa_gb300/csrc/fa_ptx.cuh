@@ -388,5 +388,13 @@ __device__ __forceinline__ float f16_hi_to_f32(uint32_t h2) {
   asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.f32.f16 %0, h;\n}" : "=f"(f) : "r"(h2));
   return f;
 }
+// Rounding residual of a pair packed as bf16x2 (bf16) or f16x2: x - float(x
+// rounded), for both halves (exact in fp32), itself rounded to the same type.
+__device__ __forceinline__ uint32_t pack_residual_x2(float a0, float a1, uint32_t packed,
+                                                     bool bf16) {
+  const float h0 = bf16 ? __uint_as_float(packed << 16) : f16_lo_to_f32(packed);
+  const float h1 = bf16 ? __uint_as_float(packed & 0xFFFF0000u) : f16_hi_to_f32(packed);
+  return bf16 ? pack_bf16x2(a0 - h0, a1 - h1) : pack_f16x2(a0 - h0, a1 - h1);
+}
 
 }  // namespace fa

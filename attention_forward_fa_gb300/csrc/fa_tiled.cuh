@@ -65,6 +65,7 @@ enum : int { kStatusTimeout = 1, kStatusRange = 2 };
 struct TiledParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_o;
   void* o;
+  void* o_lo;       // optional: o's rounding residual, same type and layout (or null)
   float* lse;
   const int* seqlens;
   const int* blk_idx;
@@ -182,11 +183,13 @@ __device__ __forceinline__ int dense_tiles(int qt, int n_qt, int q_len, int kv_l
 // One piece of a unit split along its KV tiles: the slots' ranges [0, n0) and
 // [0, n1) are cut at the same tile boundaries, every ceil(max(n0, n1) /
 // kv_split) tiles; a slot's piece is [lo, min(n, hi)), possibly empty.
+// (Unsplit launches skip the division: the setup is on every CTA's serial path.)
 struct Piece {
   int lo, hi;
 };
 __device__ __forceinline__ Piece piece_range(int n0, int n1, int piece, int kv_split) {
   const int nmax = n0 > n1 ? n0 : n1;
+  if (kv_split == 1) return Piece{0, nmax};
   const int chunk = (nmax + kv_split - 1) / kv_split;
   const int lo = min(piece * chunk, nmax);
   return Piece{lo, min(lo + chunk, nmax)};
@@ -274,7 +277,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   const int lane = tid & 31;
 
   // ---------------------------------------------------------------- unit
-  const int u = blockIdx.x / p.kv_split;   // pieces of one unit are neighbours
+  // pieces of one unit are neighbours (no division when the launch is unsplit)
+  const int u = p.kv_split == 1 ? (int)blockIdx.x : (int)blockIdx.x / p.kv_split;
   const int piece = blockIdx.x - u * p.kv_split;
   const int qpos = p.n_qpos - 1 - u / p.units_per_q;   // heaviest query positions first
   const int bh = u % p.units_per_q;
@@ -444,7 +448,14 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       }
       if (row == 0) FA_TR(1, t, j);
       tc_fence_after();
-      const int kvt = sparse ? s_list[t * kMaxSel + j] : kv_lo + j;
+      // first KV tile of a split launch's piece, re-read from shared memory
+      // every tile (a register held across this loop would push the softmax
+      // past its budget); unsplit launches skip the load, since shared memory
+      // reads wait behind the tensor core's operand traffic
+      int kv_first = 0;
+      if (p.kv_split > 1)
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(kv_first) : "r"(smem_u32(s_slot + 4)));
+      const int kvt = sparse ? s_list[t * kMaxSel + j] : kv_first + j;
       const int kbase = kvt * kBN;
       const bool causal_here = (p.mask == 1) || (p.mask == 2 && kvt == qt);
       const bool need_mask =
@@ -702,6 +713,34 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
               make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
+      if (p.o_lo) {
+        // o's rounding residual (only when asked for): a second pass over O_t,
+        // so that the epilogue above keeps its register budget
+        uint4* dst_lo = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o_lo) +
+                                                 ((size_t)(b * p.Hq + h) * p.Sq + (write ? qi : 0)) * (Dv * 2));
+#pragma unroll 1
+        for (int cc = 0; cc < Dv / 16; ++cc) {
+          uint32_t r[16];
+          if (acc) {
+            tmem_ld16(tO + 16 * cc, r);   // warp-collective: all lanes, even rows past Sq
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) r[i] = 0;
+          }
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            uint32_t wl[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float a0 = __uint_as_float(r[8 * i + 2 * e]) * inv_l;
+              const float a1 = __uint_as_float(r[8 * i + 2 * e + 1]) * inv_l;
+              wl[e] = pack_residual_x2(a0, a1, kBF16 ? pack_bf16x2(a0, a1) : pack_f16x2(a0, a1), kBF16);
+            }
+            if (write) dst_lo[2 * cc + i] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+          }
+        }
+      }
       fence_proxy_async_smem();
       named_sync(7, kBM);   // the four epilogue warps
       if (warp == 8 && lane == 0) {
@@ -803,7 +842,9 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           ld += (pv_load ? 1 : 0) + (qk_load ? 1 : 0);
         }
         const uint32_t sv_ = (uint32_t)lpv % NS, sk_ = (uint32_t)lqk % NS;
-        if (g >= 2) named_sync(3 + (g & 1), 64);      // issuer finished group g-2
+        // issuer finished group g-2 (a group with work: groups 0 and 1, or a
+        // P.V at tile jpv - 1 < nt; an empty group arrives nowhere)
+        if (g >= 2 && (g < 4 || jpv <= nt)) named_sync(3 + (g & 1), 64);
         if (lane == 0 && !aborted) {
           if (pv_load && !wait_bar(BAR_READY(sv_), (lpv / NS) & 1, wc)) aborted = true;
           if (!aborted && qk_load && !wait_bar(BAR_READY(sk_), (lqk / NS) & 1, wc)) aborted = true;
@@ -819,9 +860,10 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           named_arrive(kBarPReady + t, kPReadyCount);
         }
       }
-      // the issuer's last two "group issued" arrivals
-      if (ngroups >= 2) named_sync(3 + (ngroups & 1), 64);
-      if (ngroups >= 1) named_sync(3 + ((ngroups - 1) & 1), 64);
+      // the issuer's last two "group issued" arrivals: groups (0, nmax - 1)
+      // and (1, nmax - 1), each only if its slot has a P.V there
+      if (nmax > 0 && n0 == nmax) named_sync(3, 64);
+      if (nmax > 0 && n1 == nmax) named_sync(4, 64);
     } else {
       // ---- issuer: the same groups, two per step (slot 0, slot 1) so that
       // everything that depends on the slot is fixed at compile time.  The
@@ -837,6 +879,12 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         const int jqk = jpv + 1;
         const bool pv_valid = jpv >= 0 && jpv < nt;
         const bool qk_valid = jqk < nt;
+        // A group past the slot's last tile has no work (no P.V, hence no
+        // Q.K^T) and hands nothing off: its "group issued" arrival could
+        // otherwise follow the previous one on the same barrier before the
+        // scheduler has consumed that one, completing the barrier's generation
+        // with the wrong pair and leaving the scheduler waiting forever.
+        if (jpv >= 0 && !pv_valid) return;
         int lpv, lqk;
         if (shared_kv) {
           lpv = 2 * jpv + 1;

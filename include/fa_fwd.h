@@ -158,6 +158,20 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            const fa_block_sparse_t* kv_block_idx, const fa_topk_t* topk_idx,
            float rescale_threshold, void* stream);
 
+/* fa_fwd that also writes the output's rounding residual
+ *   o_lo = fp32(O) - O rounded to o's type,
+ * itself rounded to that type, same layout as o (rows past Sq / padded heads
+ * untouched), so that o + o_lo carries O to about twice o's precision for a
+ * backward that recomputes with it ("Sparse-MLA training forward: exact
+ * running max vs lazy rescale" (cf-1.com), section "Tests: order-invariance
+ * verification", the precise-dpsum test).  o_lo: DEVICE memory, 16-byte
+ * aligned; FA_ERR_NULL / FA_ERR_ALIGN otherwise.  Every other argument and
+ * return code as fa_fwd. */
+int fa_fwd_o_lo(const void* q, const void* k, const void* v, void* o, void* o_lo, float* lse,
+                int B, int Hq, int Hkv, int Sq, int Skv, int D, int Dv, float scale,
+                int mask_mode, const int32_t* seqlens, const fa_block_sparse_t* kv_block_idx,
+                const fa_topk_t* topk_idx, float rescale_threshold, void* stream);
+
 /*
  * fa_fwd_noalloc -- fa_fwd without any memory allocation.  (The pages define
  * no counterpart: this is an interface for callers, not part of the method.)

@@ -97,6 +97,14 @@ def test_timeout_setter(lib):
     B.fa_set_wait_timeout_ns(0)   # back to the default
 
 
+def test_o_lo_pointer_checks(lib):
+    """fa_fwd_o_lo refuses a NULL or misaligned residual buffer before anything runs."""
+    args = [P, P, P, P]
+    tail = [P, 1, 2, 2, 128, 128, 128, 128, 0.1, 0, None, None, None, 0.0, None]
+    assert lib.fa_fwd_o_lo(*args, None, *tail) == -1
+    assert lib.fa_fwd_o_lo(*args, P + 2, *tail) == -4
+
+
 def test_kv_split_setter_range(lib):
     assert B.fa_set_max_kv_split(0) == -2
     assert B.fa_set_max_kv_split(9) == -2

@@ -146,6 +146,47 @@ def test_split_kv_small_grids(case, max_split):
         fa.fa_set_max_kv_split(8)
 
 
+O_LO_CASES = {
+    "dense_bf16": lambda: W.dense(name="olo_dense", B=2, Hq=4, Hkv=2, Sq=700, D=128,
+                                  mask=W.MASK_CAUSAL, seqlens=[700, 333], seed=61),
+    "split_fp16": lambda: W.dense(name="olo_split", B=1, Hq=2, Sq=2048, D=64, dtype="fp16",
+                                  mask=W.MASK_CAUSAL, seed=62),
+    "mla_bf16": lambda: W.sparse_mla(name="olo_mla", T=300, W=320, seed=63),
+    # 64 heads: half of the kernel's 128-row head group is padding
+    "mla_padded_heads": lambda: W.sparse_mla(name="olo_mla_h64", T=150, Hq=64, W=160, seed=64),
+}
+
+
+@pytest.mark.parametrize("case", sorted(O_LO_CASES))
+def test_o_lo_residual(case):
+    """fa_fwd_o_lo: o equals fa_fwd's bit for bit, o_lo is within half an ulp
+    of o, and o + o_lo is closer to the fp64 oracle than o (the precise-dpsum
+    forward check of the sparse-MLA page); the split-KV case gets its residual
+    from the merge kernel, the top-k case from its own epilogue."""
+    import torch
+    import attention_forward_fa_gb300 as fa
+    from tests.parity import to_device
+    p = O_LO_CASES[case]()
+    d = to_device(p)
+    kw = dict(scale=p.scale, mask_mode=p.mask_mode, seqlens=d["seqlens"], topk_idx=d["topk_idx"])
+    v = None if p.v_from_k else d["v"]
+    o_ref, l_ref = fa.flash_attention_forward(d["q"], d["k"], v, **kw)
+    o, lse, o_lo = fa.flash_attention_forward(d["q"], d["k"], v, o_lo=True, **kw)
+    torch.cuda.synchronize()
+    assert fa.fa_check_status() == 0
+    assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+    Or, _ = A.attention_problem(p)
+    sel = ~np.isnan(Or)
+    hi = o.float().cpu().double().numpy()
+    lo = o_lo.float().cpu().double().numpy()
+    ulp_half = 2.0 ** -8 if p.dtype == "bf16" else 2.0 ** -11
+    tiny = 1e-30 if p.dtype == "bf16" else 2.0 ** -25
+    assert (np.abs(lo) <= ulp_half * np.abs(hi) + tiny).all()
+    e_hi = np.linalg.norm((hi - Or)[sel]) / np.linalg.norm(Or[sel])
+    e_sum = np.linalg.norm((hi + lo - Or)[sel]) / np.linalg.norm(Or[sel])
+    assert e_sum < (0.5 if p.dtype == "bf16" else 1.0) * e_hi, (e_sum, e_hi)
+
+
 def test_chained_calls_wait_for_the_previous_call():
     """Two calls back to back on one stream, the second taking the first's
     output as its queries.  The second kernel may be scheduled while the first
