@@ -1,0 +1,101 @@
+"""fp64 CPU oracle for the attention backward (dQ, dK, dV), materialising P.
+
+TEST INFRASTRUCTURE.  Only tests/, __graft_entry__.smoke() and bench.py's
+cpu_baseline / reference arm may import or run anything in this package; the
+product path (attention_forward_fa_gb300) never does, and nothing here imports
+the product path.
+
+What it computes is the gradient of the forward's plain definition
+(oracle.attention) for an upstream gradient dO, written out as the BSA PyPTO
+implementation notes describe the backward:
+
+  P[i, j]  = w[i, j] * exp(scale * S[i, j] - LSE[i])   recomputed from the saved
+                                                      LSE, S and P not stored
+                                                      (section 3.2 "Core design
+                                                      strategies", recomputation)
+  d_row[i] = sum_d dO[i, d] * O[i, d]                  (section 8.4, "D_row
+                                                      precompute")
+  dV       = P^T dO                                     (no scale on dV)
+  dP       = dO V^T
+  dS       = P * (dP - d_row)
+  dQ       = scale * dS K,   dK = scale * dS^T Q        (scale on dQ and dK:
+                                                      section 1, data types and
+                                                      precision)
+
+Here S[i, j] = sum_d Q[i, d] K[j, d] (unscaled) and w[i, j] is the number of
+valid slots that list key j for row i (1 for dense, 0 where masked): the same
+valid key sets as the forward, from the same multiplicity rule, so that a key
+listed twice enters P twice, as it does the forward.
+
+  * GQA: dK and dV of a KV head are the sums over the query heads of its group
+    (BSA notes, section 1: GQA compatible).
+  * Padded query rows (i >= seqlens[b]) and rows without a valid key carry
+    LSE = +inf from the forward, so P = 0 there: they contribute nothing and
+    get dQ = 0 (the notes' padded-row defence, section 3.2: such rows must not
+    leak into dK / dV).  Keys j >= seqlens[b] get dK = dV = 0.
+  * Sparse MLA (V is the latent part of K, one KV head): the key latent's
+    gradient is dK plus dV on its first Dv columns; ``latent_grad`` forms it.
+
+Everything is float64; numpy's matmul is the only library step.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+
+from .attention import BLOCK, MASK_NONE, _multiplicity
+
+
+def attention_bwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, o: np.ndarray, lse: np.ndarray,
+                  do: np.ndarray, scale: float, mask: int = MASK_NONE,
+                  seqlens: Optional[np.ndarray] = None,
+                  kv_block_idx: Optional[np.ndarray] = None,
+                  topk_idx: Optional[np.ndarray] = None, block: int = BLOCK):
+    """Reference backward.
+
+    q [B,Hq,Sq,D], k [B,Hkv,Skv,D], v [B,Hkv,Skv,Dv], o / do [B,Hq,Sq,Dv] and
+    lse [B,Hq,Sq] (the forward's outputs; +inf on rows without keys), all
+    float64 values.  Mask arguments as oracle.attention.attention_fwd.
+    Returns dQ [B,Hq,Sq,D], dK [B,Hkv,Skv,D], dV [B,Hkv,Skv,Dv] (float64).
+    """
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Skv, _ = k.shape
+    Dv = v.shape[-1]
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    G = Hq // Hkv
+    nkb = (Skv + block - 1) // block
+    dq = np.zeros((B, Hq, Sq, D))
+    dk = np.zeros((B, Hkv, Skv, D))
+    dv = np.zeros((B, Hkv, Skv, Dv))
+    rows = np.arange(Sq)
+    for b in range(B):
+        qlen = Sq if seqlens is None else int(seqlens[b])
+        kvlen = Skv if seqlens is None else int(seqlens[b])
+        for h in range(Hq):
+            kh = h // G
+            w = _multiplicity(rows, b, h, qlen, kvlen, Skv, nkb, block, mask, kv_block_idx,
+                              topk_idx)
+            s = q[b, h] @ k[b, kh].T
+            lse_h = lse[b, h][:, None]
+            live = np.isfinite(lse_h) & (w > 0)
+            with np.errstate(over="ignore", invalid="ignore"):
+                p = np.where(live, w * np.exp(scale * s - np.where(np.isfinite(lse_h), lse_h, 0.0)),
+                             0.0)
+            d_row = (do[b, h] * o[b, h]).sum(axis=-1)
+            d_row = np.where(np.isfinite(lse[b, h]), d_row, 0.0)
+            dv[b, kh] += p.T @ do[b, h]
+            dp = do[b, h] @ v[b, kh].T
+            ds = p * (dp - d_row[:, None])
+            dq[b, h] = scale * (ds @ k[b, kh])
+            dk[b, kh] += scale * (ds.T @ q[b, h])
+    return dq, dk, dv
+
+
+def latent_grad(dk: np.ndarray, dv: np.ndarray) -> np.ndarray:
+    """Gradient of a shared key latent whose first Dv columns also serve as V
+    (sparse MLA): dK with dV added on those columns."""
+    g = dk.copy()
+    g[..., :dv.shape[-1]] += dv
+    return g
