@@ -11,7 +11,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libfa_fwd.so")
 SOURCES = ["fa_fwd.cu"]
-DEPS = ["fa_fwd.cu", "fa_tiled.cuh", "fa_ptx.cuh"]
+DEPS = ["fa_fwd.cu", "fa_tiled.cuh", "fa_ptx.cuh", "fa_mla.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -255,9 +255,9 @@ cudaError_t launch_dependent(void (*kern)(Params...), unsigned grid, unsigned bl
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-template <int D, bool BF16, int NS, bool CONV>
+template <int D, bool BF16, int NS, bool CONV, bool SPLIT>
 int launch_tiled(const fa::TiledParams& prm, int units, cudaStream_t st) {
-  auto kern = fa::fa_fwd_tiled_kernel<D, BF16, NS, CONV>;
+  auto kern = fa::fa_fwd_tiled_kernel<D, BF16, NS, CONV, SPLIT>;
   constexpr int smem = fa::TiledSmem<D, NS>::kAlloc;
   static std::once_flag once[64];
   int dev = 0;
@@ -278,6 +278,20 @@ int launch_tiled(const fa::TiledParams& prm, int units, cudaStream_t st) {
   cudaError_t e = launch_dependent(kern, (unsigned)units, fa::kTiledThreads, smem, st, prm);
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;
+}
+
+// The dense kernel for (head dim, input type, V conversion), split or not.
+template <bool SPLIT>
+int launch_tiled_variant(const fa::TiledParams& prm, int grid, cudaStream_t st, int D, bool fp16,
+                         bool conv) {
+  if (D == 128) {
+    if (fp16) return launch_tiled<128, false, 4, false, SPLIT>(prm, grid, st);
+    return conv ? launch_tiled<128, true, 4, true, SPLIT>(prm, grid, st)
+                : launch_tiled<128, true, 4, false, SPLIT>(prm, grid, st);
+  }
+  if (fp16) return launch_tiled<64, false, 6, false, SPLIT>(prm, grid, st);
+  return conv ? launch_tiled<64, true, 6, true, SPLIT>(prm, grid, st)
+              : launch_tiled<64, true, 6, false, SPLIT>(prm, grid, st);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -475,16 +489,8 @@ int run_tiled(const void* q, const void* k, const void* v, void* o, void* o_lo, 
     }
   }
   const int grid = (int)std::min<long long>(units * prm.kv_split, 0x7FFFFFFF);
-  int rc;
-  if (D == 128) {
-    if (fp16) rc = launch_tiled<128, false, 4, false>(prm, grid, st);
-    else rc = conv ? launch_tiled<128, true, 4, true>(prm, grid, st)
-                   : launch_tiled<128, true, 4, false>(prm, grid, st);
-  } else {
-    if (fp16) rc = launch_tiled<64, false, 6, false>(prm, grid, st);
-    else rc = conv ? launch_tiled<64, true, 6, true>(prm, grid, st)
-                   : launch_tiled<64, true, 6, false>(prm, grid, st);
-  }
+  int rc = prm.kv_split > 1 ? launch_tiled_variant<true>(prm, grid, st, D, fp16, conv)
+                             : launch_tiled_variant<false>(prm, grid, st, D, fp16, conv);
   if (rc == FA_OK && prm.kv_split > 1) {
     const unsigned blocks = (unsigned)((rows_all + 7) / 8);
     const cudaError_t e =

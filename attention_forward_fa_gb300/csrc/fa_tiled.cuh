@@ -231,7 +231,10 @@ __device__ __forceinline__ Event event_at(int e, int n0, int n1, bool shared) {
 
 // kConvV: V arrives as bf16 and the epilogue warpgroup, idle during the tile
 // loop, converts each V tile to fp16 in shared memory before the MMA reads it.
-template <int D, bool kBF16, int NS, bool kConvV>
+// kSplit: the launch cuts units into KV pieces (p.kv_split > 1); an unsplit
+// launch compiles without the piece bookkeeping, which costs ~1-2 % of the
+// loop's time even when every unit is one piece.
+template <int D, bool kBF16, int NS, bool kConvV, bool kSplit>
 __global__ void __launch_bounds__(kTiledThreads, 1)
     fa_fwd_tiled_kernel(const __grid_constant__ TiledParams p) {
   using SM = TiledSmem<D, NS>;
@@ -277,9 +280,9 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   const int lane = tid & 31;
 
   // ---------------------------------------------------------------- unit
-  // pieces of one unit are neighbours (no division when the launch is unsplit)
-  const int u = p.kv_split == 1 ? (int)blockIdx.x : (int)blockIdx.x / p.kv_split;
-  const int piece = blockIdx.x - u * p.kv_split;
+  const int kv_split = kSplit ? p.kv_split : 1;
+  const int u = kSplit ? (int)blockIdx.x / kv_split : (int)blockIdx.x;   // pieces of one unit are neighbours
+  const int piece = blockIdx.x - u * kv_split;
   const int qpos = p.n_qpos - 1 - u / p.units_per_q;   // heaviest query positions first
   const int bh = u % p.units_per_q;
   int b, h0, h1, qt0, qt1;
@@ -334,7 +337,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     if (!sparse) {
       const int f0 = dense_tiles(qt0, p.n_qt, q_len, kv_len, p.mask);
       const int f1 = dense_tiles(qt1, p.n_qt, q_len, kv_len, p.mask);
-      const Piece pc = piece_range(f0, f1, piece, p.kv_split);
+      const Piece pc = piece_range(f0, f1, piece, kv_split);
       const int e0 = piece_count(f0, pc), e1 = piece_count(f1, pc);
       s_slot[4] = pc.lo;
       for (int t = 0; t < 2; ++t) {
@@ -372,7 +375,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       // this slot's tiles of the piece (both slots' counts fix the cuts)
       const int f0 = dense_tiles(qt0, p.n_qt, q_len, kv_len, p.mask);
       const int f1 = dense_tiles(qt1, p.n_qt, q_len, kv_len, p.mask);
-      n = piece_count(t ? f1 : f0, piece_range(f0, f1, piece, p.kv_split));
+      n = piece_count(t ? f1 : f0, piece_range(f0, f1, piece, kv_split));
       const int min_keys = (p.mask == 1) ? min(q0 + 1, kv_len) : kv_len;
       hilo = min_keys < kHiLoKeys;
     } else if (live && sparse) {
@@ -453,7 +456,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       // past its budget); unsplit launches skip the load, since shared memory
       // reads wait behind the tensor core's operand traffic
       int kv_first = 0;
-      if (p.kv_split > 1)
+      if (kSplit)
         asm volatile("ld.shared.b32 %0, [%1];" : "=r"(kv_first) : "r"(smem_u32(s_slot + 4)));
       const int kvt = sparse ? s_list[t * kMaxSel + j] : kv_first + j;
       const int kbase = kvt * kBN;
@@ -655,7 +658,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       const bool write = qi < p.Sq;
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       const uint32_t tO = tmem + 256u + 128u * t + lane_off;
-      if (p.kv_split > 1) {
+      if (kSplit) {
         // one piece of a split unit: its O / l in fp32 and its LSE (-inf when
         // the piece saw no key of the row) for the merge kernel
         const size_t rows_all = (size_t)p.B * p.Hq * p.Sq;
