@@ -99,3 +99,45 @@ def latent_grad(dk: np.ndarray, dv: np.ndarray) -> np.ndarray:
     g = dk.copy()
     g[..., :dv.shape[-1]] += dv
     return g
+
+
+def backward_emulation(q: np.ndarray, k: np.ndarray, v: np.ndarray, o_out: np.ndarray,
+                       lse: np.ndarray, do: np.ndarray, scale: float, causal: bool,
+                       o_lo: Optional[np.ndarray] = None, op_dtype: str = "fp16",
+                       hilo_keys: int = 256, out_dtype: str = "bf16"):
+    """Emulation of a tensor-core backward's roundings, for one (batch, head).
+
+    q [Sq, D], k [Skv, D], v [Skv, Dv], do [Sq, Dv] hold the exact values of
+    the low-precision inputs; o_out is the forward's rounded output and o_lo
+    its rounding residual (or None); lse the forward's fp32 LSE.  The steps of
+    attention_bwd, with these roundings:
+      * d_row = rowsum(dO * (o_out [+ o_lo])) in fp32 (the backward sees only
+        the forward's stored output, and the residual when given);
+      * P (fp32) and dS = P * (dP - d_row) (fp32) enter the products
+        dV = P^T dO, dQ = dS K and dK = dS^T Q as ``op_dtype`` operands; on
+        query rows with fewer than ``hilo_keys`` valid keys as a pair
+        fp16(x) + fp16(x - fp16(x)) (the forward's hi + lo split), when
+        op_dtype is fp16;
+      * products accumulate exactly (fp32 accumulation over these lengths is
+        far below the operand roundings); outputs rounded to ``out_dtype``.
+    Returns dQ, dK, dV (float64).
+    """
+    from .online import round_bf16, round_fp16, round_fp32
+    rnd = {"bf16": round_bf16, "fp16": round_fp16, "fp32": round_fp32, None: lambda x: x}
+    Sq, Skv = q.shape[0], k.shape[0]
+    masked = (np.arange(Skv)[None, :] > np.arange(Sq)[:, None]) if causal else np.zeros((Sq, Skv), bool)
+    p = round_fp32(np.where(masked, 0.0, np.exp(scale * (q @ k.T) - lse[:, None])))
+    o_seen = o_out if o_lo is None else o_out + o_lo
+    d_row = round_fp32((do * o_seen).sum(-1))
+    ds = p * (round_fp32(do @ v.T) - d_row[:, None])
+    short = ((~masked).sum(1) < hilo_keys)[:, None]
+
+    def operand(x):
+        hi = rnd[op_dtype](x)
+        if op_dtype != "fp16":
+            return hi
+        return hi + np.where(short, round_fp16(x - hi), 0.0)
+
+    p_op, ds_op = operand(p), operand(ds)
+    out = rnd[out_dtype]
+    return (out(scale * (ds_op @ k)), out(scale * (ds_op.T @ q)), out(p_op.T @ do))

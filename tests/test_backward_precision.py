@@ -1,0 +1,75 @@
+"""Precision decisions for a tensor-core backward, from the emulation in
+oracle/backward.py against the fp64 backward oracle, on one causal bf16 head
+(S 1024, D 128, N(0, 1) inputs and dO) under the pages' elementwise bound
+|d| <= 1e-4 + 7.8125e-3 |ref| (BSA implementation notes, section 1).
+
+* With P and dS as fp16 operands, split into hi + lo fp16 pairs on query rows
+  with fewer than 256 keys, and d_row = rowsum(dO * (o + o_lo)) from the
+  forward's output and its rounding residual, dQ, dK and dV meet the bound.
+* Without the residual (d_row from the rounded output alone) dQ and dK miss
+  it by an order of magnitude: the residual output is what the precise-dpsum
+  check of the sparse-MLA page asks the forward for.
+* bf16 dS misses it, and so do fp16 operands without the short-row split.
+"""
+import numpy as np
+import pytest
+
+from oracle import attention as A
+from oracle import backward as BW
+from oracle.online import round_bf16, round_fp32
+
+ATOL, RTOL = 1e-4, 0.0078125
+
+
+@pytest.fixture(scope="module")
+def head():
+    rng = np.random.default_rng(3)
+    S, D = 1024, 128
+    scale = 1 / np.sqrt(D)
+    q, k, v, do = (round_bf16(rng.standard_normal((S, D))) for _ in range(4))
+    o, lse = A.attention_fwd(q[None, None], k[None, None], v[None, None], scale, mask=A.MASK_CAUSAL)
+    ref = [g[0, 0] for g in BW.attention_bwd(q[None, None], k[None, None], v[None, None], o, lse,
+                                             do[None, None], scale, mask=A.MASK_CAUSAL)]
+    o_out = round_bf16(o[0, 0])
+    return dict(q=q, k=k, v=v, do=do, scale=scale, o_out=o_out, o_lo=round_bf16(o[0, 0] - o_out),
+                lse=round_fp32(lse[0, 0]), ref=ref)
+
+
+def worst(h, **kw):
+    got = BW.backward_emulation(h["q"], h["k"], h["v"], h["o_out"], h["lse"], h["do"], h["scale"],
+                                True, **kw)
+    return [float((np.abs(g - r) / (ATOL + RTOL * np.abs(r))).max()) for g, r in zip(got, h["ref"])]
+
+
+def test_fp16_hilo_operands_with_the_residual_meet_the_bound(head):
+    assert max(worst(head, o_lo=head["o_lo"])) < 1.0
+
+
+def test_without_the_residual_dq_and_dk_miss_the_bound(head):
+    rq, rk, _ = worst(head)
+    assert rq > 5 and rk > 5
+
+
+def test_bf16_ds_misses_the_bound(head):
+    rq, rk, rv = worst(head, o_lo=head["o_lo"], op_dtype="bf16")
+    assert max(rq, rk, rv) > 2
+
+
+def test_fp16_without_the_short_row_split_misses_the_bound(head):
+    assert max(worst(head, o_lo=head["o_lo"], hilo_keys=0)) > 1.0
+
+
+def test_emulation_without_roundings_is_the_oracle(head):
+    # exact output in place of the rounded one, no operand or output rounding:
+    # only the fp32 roundings of P, dP and d_row remain
+    rng = np.random.default_rng(4)
+    S, D = 256, 64
+    scale = 1 / np.sqrt(D)
+    q, k, v, do = (rng.standard_normal((S, D)) for _ in range(4))
+    o, lse = A.attention_fwd(q[None, None], k[None, None], v[None, None], scale, mask=A.MASK_CAUSAL)
+    ref = [g[0, 0] for g in BW.attention_bwd(q[None, None], k[None, None], v[None, None], o, lse,
+                                             do[None, None], scale, mask=A.MASK_CAUSAL)]
+    got = BW.backward_emulation(q, k, v, o[0, 0], lse[0, 0], do, scale, True, op_dtype=None,
+                                out_dtype=None)
+    for g, r in zip(got, ref):
+        assert np.linalg.norm(g - r) / np.linalg.norm(r) < 1e-6
