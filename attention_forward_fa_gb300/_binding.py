@@ -57,6 +57,9 @@ def library() -> ctypes.CDLL:
         lib.fa_fwd_noalloc.argtypes = lib.fa_fwd.argtypes
         lib.fa_fwd_o_lo.restype = ctypes.c_int
         lib.fa_fwd_o_lo.argtypes = lib.fa_fwd.argtypes[:4] + [ctypes.c_void_p] + lib.fa_fwd.argtypes[4:]
+        lib.fa_bwd.restype = ctypes.c_int
+        lib.fa_bwd.argtypes = [ctypes.c_void_p] * 10 + [ctypes.c_int] * 7 + [
+            ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
         lib.fa_convert_v_fp16.restype = ctypes.c_int
         lib.fa_convert_v_fp16.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                           ctypes.c_void_p]
@@ -135,6 +138,15 @@ def fa_fwd_o_lo(q, k, v, o, o_lo, lse, B: int, Hq: int, Hkv: int, Sq: int, Skv: 
     return lib.fa_fwd_o_lo(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(o_lo), _ptr(lse), B, Hq, Hkv,
                            Sq, Skv, D, Dv, float(scale), int(mask_mode), _ptr(seqlens), bs, tk,
                            float(rescale_threshold), _stream(stream))
+
+
+def fa_bwd(q, k, v, o, o_lo, lse, dout, dq, dk, dv, B: int, Hq: int, Hkv: int, Sq: int, Skv: int,
+           D: int, Dv: int, scale: float, mask_mode: int, seqlens=None, stream=None) -> int:
+    """Direct call of the backward entry point (see include/fa_fwd.h); o_lo
+    may be None.  Returns the FA_* code."""
+    return library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(o_lo), _ptr(lse), _ptr(dout),
+                            _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Skv, D, Dv, float(scale),
+                            int(mask_mode), _ptr(seqlens), _stream(stream))
 
 
 def fa_fwd_noalloc(q, k, v, o, lse, B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int,
@@ -243,3 +255,30 @@ def flash_attention_forward(q, k, v=None, *, scale: Optional[float] = None, caus
                        seqlens, bs, tk, rescale_threshold, stream)
     _raise(code)
     return out, lse, o_lo
+
+
+def flash_attention_backward(q, k, v, o, lse, dout, *, o_lo=None, scale: Optional[float] = None,
+                             causal: bool = False, seqlens=None, dq=None, dk=None, dv=None,
+                             stream=None):
+    """Allocating wrapper over fa_bwd: q, o, dout [B,Hq,Sq,128], k, v
+    [B,Hkv,Skv,128] (bf16 or fp16 CUDA tensors, contiguous), lse [B,Hq,Sq]
+    fp32 from the forward, o_lo its residual (recommended).  Returns
+    (dq, dk, dv) in the inputs' type."""
+    import torch
+    for t in (q, k, v, o, dout) + ((o_lo,) if o_lo is not None else ()):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype:
+            raise ValueError("q, k, v, o, dout (and o_lo) must be contiguous CUDA tensors of one dtype")
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Skv, _ = k.shape
+    Dv = v.shape[-1]
+    mask_mode = FA_MASK_CAUSAL if causal else FA_MASK_NONE
+    if q.dtype == torch.float16:
+        mask_mode |= FA_DTYPE_FP16
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _raise(fa_bwd(q, k, v, o, o_lo, lse, dout, dq, dk, dv, B, Hq, Hkv, Sq, Skv, D, Dv, scale,
+                  mask_mode, seqlens, stream))
+    return dq, dk, dv

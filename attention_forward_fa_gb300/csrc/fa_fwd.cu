@@ -15,6 +15,7 @@
 #include "../../include/fa_fwd.h"
 #include "fa_tiled.cuh"
 #include "fa_mla.cuh"
+#include "fa_bwd.cuh"
 
 namespace {
 
@@ -560,9 +561,132 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, void* o_lo, f
                   rescale_threshold, status, st);
 }
 
+// ------------------------------------------------------------------ backward
+template <bool BF16>
+int launch_bwd(const fa::BwdParams& prm, int grid_kv, int grid_q, cudaStream_t st) {
+  auto k_kv = fa::fa_bwd_dkdv_kernel<BF16>;
+  auto k_q = fa::fa_bwd_dq_kernel<BF16>;
+  constexpr int smem = fa::BwdSmem::kAlloc;
+  static std::once_flag once[64];
+  static cudaError_t attr_err[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::call_once(once[dev & 63], [&] {
+    cudaError_t e = cudaFuncSetAttribute(k_kv, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_q, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    attr_err[dev & 63] = e;
+  });
+  if (attr_err[dev & 63] != cudaSuccess) return cuda_fail(attr_err[dev & 63]);
+  if (grid_kv > 0) k_kv<<<grid_kv, fa::kBwdThreads, smem, st>>>(prm);
+  if (grid_q > 0) k_q<<<grid_q, fa::kBwdThreads, smem, st>>>(prm);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* o_lo,
+             const float* lse, const void* dout, void* dq, void* dk, void* dv, int B, int Hq,
+             int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
+             const int32_t* seqlens, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_NULL;
+  if (mask_mode & ~(0xF | FA_DTYPE_FP16)) return FA_ERR_SHAPE;
+  const int mask = mask_mode & 0xF;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || D <= 0 || Dv <= 0 || Hq % Hkv)
+    return FA_ERR_SHAPE;
+  if (mask > FA_MASK_CAUSAL || !std::isfinite(scale)) return FA_ERR_SHAPE;
+  if ((long long)B * Hq > (1LL << 30) || (long long)Sq * 128 > (1LL << 31) ||
+      (long long)Skv * 128 > (1LL << 31))
+    return FA_ERR_SHAPE;
+  if (D != 128 || Dv != 128) return FA_ERR_UNSUPPORTED;
+  for (const void* t : {q, k, v, o, dout, static_cast<const void*>(dq), static_cast<const void*>(dk),
+                        static_cast<const void*>(dv)})
+    if (!aligned(t, 16)) return FA_ERR_ALIGN;
+  if ((o_lo && !aligned(o_lo, 16)) || !aligned(lse, 4) || (seqlens && !aligned(seqlens, 4)))
+    return FA_ERR_ALIGN;
+  const bool fp16 = (mask_mode & FA_DTYPE_FP16) != 0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* status = status_ptr();
+  if (!status) return cuda_fail(cudaGetLastError());
+
+  // scratch: d_row, and fp16 copies of bf16 Q, K, V, dO (every product runs on fp16)
+  const size_t nq = (size_t)B * Hq * Sq * 128, nk = (size_t)B * Hkv * Skv * 128;
+  const size_t rows = (size_t)B * Hq * Sq;
+  const size_t drow_bytes = (rows * 4 + 255) & ~size_t(255);
+  const size_t bytes = drow_bytes + (fp16 ? 0 : 2 * (nq + nk) * 2);
+  uint8_t* scratch = static_cast<uint8_t*>(scratch_alloc(bytes, st));
+  if (!scratch) return cuda_fail(cudaGetLastError());
+  float* d_row = reinterpret_cast<float*>(scratch);
+  const void *q16 = q, *k16 = k, *v16 = v, *do16 = dout;
+  int rc = FA_OK;
+  if (!fp16) {
+    uint8_t* c = scratch + drow_bytes;
+    q16 = c;
+    do16 = c + nq * 2;
+    k16 = c + 2 * nq * 2;
+    v16 = c + 2 * nq * 2 + nk * 2;
+    rc = convert_v(q, const_cast<void*>(q16), nq, status, st);
+    if (rc == FA_OK) rc = convert_v(dout, const_cast<void*>(do16), nq, status, st);
+    if (rc == FA_OK) rc = convert_v(k, const_cast<void*>(k16), nk, status, st);
+    if (rc == FA_OK) rc = convert_v(v, const_cast<void*>(v16), nk, status, st);
+  }
+  if (rc == FA_OK) {
+    const unsigned blocks = (unsigned)((rows + 7) / 8);
+    const auto* o16 = static_cast<const uint16_t*>(o);
+    const auto* lo16 = static_cast<const uint16_t*>(o_lo);
+    const auto* d16 = static_cast<const uint16_t*>(dout);
+    if (fp16) fa::fa_bwd_drow_kernel<false><<<blocks, 256, 0, st>>>(o16, lo16, d16, d_row, (long long)rows);
+    else fa::fa_bwd_drow_kernel<true><<<blocks, 256, 0, st>>>(o16, lo16, d16, d_row, (long long)rows);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) rc = cuda_fail(e);
+  }
+  if (rc == FA_OK) {
+    fa::BwdParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    if (!encode_3d(&prm.tm_q, q16, true, 128, Sq, (uint64_t)B * Hq, 128) ||
+        !encode_3d(&prm.tm_do, do16, true, 128, Sq, (uint64_t)B * Hq, 128) ||
+        !encode_3d(&prm.tm_k, k16, true, 128, Skv, (uint64_t)B * Hkv, 128) ||
+        !encode_3d(&prm.tm_v, v16, true, 128, Skv, (uint64_t)B * Hkv, 128)) {
+      rc = cuda_fail(cudaErrorInvalidValue);
+    } else {
+      prm.lse = lse;
+      prm.d_row = d_row;
+      prm.dq = dq;
+      prm.dk = dk;
+      prm.dv = dv;
+      prm.seqlens = seqlens;
+      prm.B = B;
+      prm.Hq = Hq;
+      prm.Hkv = Hkv;
+      prm.Sq = Sq;
+      prm.Skv = Skv;
+      prm.G = Hq / Hkv;
+      prm.n_qt = (Sq + 127) / 128;
+      prm.n_kt = (Skv + 127) / 128;
+      prm.causal = mask == FA_MASK_CAUSAL;
+      prm.scale = scale;
+      prm.scale_log2 = scale * 1.4426950408889634f;
+      prm.timeout_ns = g_timeout_ns.load();
+      prm.status = status;
+      const long long grid_kv = (long long)prm.n_kt * B * Hkv, grid_q = (long long)prm.n_qt * B * Hq;
+      if (grid_kv > 0x7FFFFFFF || grid_q > 0x7FFFFFFF) rc = FA_ERR_SHAPE;
+      else rc = fp16 ? launch_bwd<false>(prm, (int)grid_kv, (int)grid_q, st)
+                     : launch_bwd<true>(prm, (int)grid_kv, (int)grid_q, st);
+    }
+  }
+  cudaFreeAsync(scratch, st);
+  return rc;
+}
+
 }  // namespace
 
 extern "C" {
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* o_lo,
+           const float* lse, const void* dout, void* dq, void* dk, void* dv, int B, int Hq,
+           int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
+           const int32_t* seqlens, void* stream) {
+  return bwd_impl(q, k, v, o, o_lo, lse, dout, dq, dk, dv, B, Hq, Hkv, Sq, Skv, D, Dv, scale,
+                  mask_mode, seqlens, stream);
+}
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
            int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,

@@ -172,6 +172,29 @@ int fa_fwd_o_lo(const void* q, const void* k, const void* v, void* o, void* o_lo
                 int mask_mode, const int32_t* seqlens, const fa_block_sparse_t* kv_block_idx,
                 const fa_topk_t* topk_idx, float rescale_threshold, void* stream);
 
+/* fa_bwd -- gradients of the dense forward for an upstream gradient dout:
+ *   P = exp(scale * Q K^T - LSE) recomputed from the forward's LSE,
+ *   d_row = rowsum(dout * (o + o_lo)),   dV = P^T dout,
+ *   dS = P * (dout V^T - d_row),   dQ = scale dS K,   dK = scale dS^T Q
+ * ("BSA PyPTO implementation notes" (gitcode pypto-gym), sections 3.2
+ * "Core design strategies" (recomputation), 8.4 (d_row precomputed) and 1
+ * (dV unscaled, dQ / dK scaled)).  GQA: dK / dV sum over the heads of a group.
+ * q, o, dout, dq: [B, Hq, Sq, 128]; k, v, dk, dv: [B, Hkv, Skv, 128]; lse:
+ * [B, Hq, Sq] fp32 as fa_fwd wrote it; all DEVICE memory, bf16 (or fp16 with
+ * FA_DTYPE_FP16 in mask_mode), 16-byte aligned (lse 4).  o_lo: the residual
+ * from fa_fwd_o_lo, or NULL; without it the dpsum uses the rounded output, and
+ * on causal problems dQ / dK then lose about an order of magnitude in
+ * accuracy.  mask_mode: FA_MASK_NONE or FA_MASK_CAUSAL (top-left), plus
+ * FA_DTYPE_FP16; seqlens as fa_fwd.  D = Dv = 128 only (FA_ERR_UNSUPPORTED
+ * otherwise).  Rows past a batch's length get zero gradients.  Stream-ordered
+ * scratch: d_row, and fp16 copies of bf16 inputs (FA_ERR_RANGE, reported by
+ * fa_check_status, when a bf16 value exceeds the fp16 range).  Returns FA_OK
+ * or a negative FA_ERR_* code (nothing launched on an argument error). */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* o_lo,
+           const float* lse, const void* dout, void* dq, void* dk, void* dv, int B, int Hq,
+           int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
+           const int32_t* seqlens, void* stream);
+
 /*
  * fa_fwd_noalloc -- fa_fwd without any memory allocation.  (The pages define
  * no counterpart: this is an interface for callers, not part of the method.)

@@ -105,6 +105,20 @@ def test_o_lo_pointer_checks(lib):
     assert lib.fa_fwd_o_lo(*args, P + 2, *tail) == -4
 
 
+@pytest.mark.parametrize("change, code", [
+    (dict(q=None), -1), (dict(dout=None), -1), (dict(lse=None), -1),
+    (dict(D=64, Dv=64), -3), (dict(Dv=64), -3),
+    (dict(Hq=3, Hkv=2), -2), (dict(Sq=0), -2), (dict(mask_mode=2), -2), (dict(mask_mode=0x200), -2),
+    (dict(dk=P + 8), -4), (dict(o_lo=P + 2), -4),
+])
+def test_bwd_argument_errors(lib, change, code):
+    """fa_bwd checks its arguments before anything runs (no GPU needed)."""
+    a = dict(q=P, k=P, v=P, o=P, o_lo=None, lse=P, dout=P, dq=P, dk=P, dv=P, B=1, Hq=2, Hkv=1,
+             Sq=256, Skv=256, D=128, Dv=128, scale=0.1, mask_mode=1, seqlens=None, stream=0)
+    a.update(change)
+    assert B.fa_bwd(**a) == code
+
+
 def test_kv_split_setter_range(lib):
     assert B.fa_set_max_kv_split(0) == -2
     assert B.fa_set_max_kv_split(9) == -2
