@@ -46,6 +46,7 @@ the only library step.
 """
 from __future__ import annotations
 
+from dataclasses import dataclass
 from typing import Optional
 
 import numpy as np
@@ -80,7 +81,7 @@ def attention_fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
                   topk_idx: Optional[np.ndarray] = None,
                   block: int = BLOCK, rows: Optional[np.ndarray] = None,
                   heads: Optional[np.ndarray] = None, batches: Optional[np.ndarray] = None,
-                  return_p: bool = False):
+                  return_p: bool = False, extras: Optional["Extras"] = None):
     """Reference forward.
 
     q [B,Hq,Sq,D], k [B,Hkv,Skv,D], v [B,Hkv,Skv,Dv] (float64 values).
@@ -89,6 +90,8 @@ def attention_fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
     computed (for sampling large problems); skipped outputs stay NaN.
     Returns O [B,Hq,Sq,Dv] and LSE [B,Hq,Sq] (float64); with return_p also a
     dict (b, h) -> (P over the full key axis with multiplicity folded in).
+    ``extras`` adds the operator doc's mask, position-bias, window and dropout
+    terms (class Extras); LSE stays the softmax's (dropout comes after it).
     """
     B, Hq, Sq, D = q.shape
     _, Hkv, Skv, _ = k.shape
@@ -112,8 +115,14 @@ def attention_fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
                 ri = row_set[r0:r0 + 256]
                 w = _multiplicity(ri, b, h, qlen, kvlen, Skv, nkb, block, mask,
                                   kv_block_idx, topk_idx)
-                s = scale * (q[b, h, ri, :] @ k[b, kh].T)
+                if extras is None:
+                    s = scale * (q[b, h, ri, :] @ k[b, kh].T)
+                else:
+                    s = extras.scores(q[b, h, ri, :] @ k[b, kh].T, scale, b, h, ri, Hq, Sq, Skv)
+                    w = w * extras.visible(b, h, ri, Sq, Skv)
                 p, lse = _softmax_rows(s, w)
+                if extras is not None:
+                    p = p * extras.keep(b, h, ri, Skv)
                 O[b, h, ri, :] = p @ v[b, kh]
                 LSE[b, h, ri] = lse
                 if return_p:
@@ -190,3 +199,87 @@ def attention_problem(p, **kw):
     q()/k()/v(), scale, mask, seqlens, kv_block_idx, topk_idx)."""
     return attention_fwd(p.q(), p.k(), p.v(), p.scale, mask=p.mask, seqlens=p.seqlens,
                          kv_block_idx=p.kv_block_idx, topk_idx=p.topk_idx, **kw)
+
+
+@dataclass
+class Extras:
+    """The FlashAttentionScore operator doc's optional terms (gitcode
+    ops-transformer, section "Function description", the forward formula and
+    the parameter table), with the test-framework write-up of
+    FlashAttentionScoreGrad (section 5, CPU golden) for how each is built:
+
+      s = (Q K^T + pse) * scale         pse_type 1 (add, then multiply)
+      s = Q K^T * scale + pse           pse_type 0, 2, 3 (multiply, then add)
+      s masked where atten_mask is 1, outside the sparse_mode window
+      P = softmax(s),  O = (P * drop_mask / keep_prob) V
+
+    * atten_mask: 0/1 array broadcastable to [B, Hq, Sq, Skv] (1 = masked).
+    * pse: array broadcastable to [B, Hq, Sq, Skv]; pse_type 2 / 3 build it
+      instead as ALiBi, -slope_h * d and -slope_h * sqrt(d) with d = |i - j|
+      and slope_h = 2^(-8 (h + 1) / Hq), the geometric series of ratio
+      2^(-8/n) (Sq == Skv only, as the doc requires).
+    * sparse_mode 0: key j visible from query i when
+      i - pre_tokens <= j <= i + next_tokens; 2: j <= i (top-left causal);
+      3: j <= i + Skv - Sq (bottom-right causal); None: no window.
+    * drop_mask: 0/1 array broadcastable to [B, Hq, Sq, Skv] (1 = kept), with
+      keep_prob in (0, 1]; philox_dropout_mask draws one as the write-up does.
+    Masked scores take no part in the softmax (the write-up's golden fills
+    -40000; the oracle's reading is -inf, as for every other mask).
+    """
+    atten_mask: Optional[np.ndarray] = None
+    pse: Optional[np.ndarray] = None
+    pse_type: int = 1
+    sparse_mode: Optional[int] = None
+    pre_tokens: int = 2 ** 31 - 1
+    next_tokens: int = 2 ** 31 - 1
+    drop_mask: Optional[np.ndarray] = None
+    keep_prob: float = 1.0
+
+    def bias(self, b, h, ri, Hq, Sq, Skv):
+        if self.pse_type in (2, 3):
+            if Sq != Skv:
+                raise ValueError("ALiBi position bias needs Sq == Skv")
+            slope = 2.0 ** (-8.0 * (h + 1) / Hq)
+            d = np.abs(ri[:, None] - np.arange(Skv)[None, :]).astype(np.float64)
+            return -slope * (np.sqrt(d) if self.pse_type == 3 else d)
+        if self.pse is None:
+            return None
+        return _pick(self.pse, b, h, ri, Skv)
+
+    def scores(self, qk, scale, b, h, ri, Hq, Sq, Skv):
+        bias = self.bias(b, h, ri, Hq, Sq, Skv)
+        if bias is None:
+            return scale * qk
+        if self.pse_type == 1:
+            return (qk + bias) * scale
+        return qk * scale + bias
+
+    def visible(self, b, h, ri, Sq, Skv):
+        i = ri[:, None]
+        j = np.arange(Skv)[None, :]
+        vis = np.ones((len(ri), Skv))
+        if self.sparse_mode == 0:
+            vis *= (j >= i - self.pre_tokens) & (j <= i + self.next_tokens)
+        elif self.sparse_mode == 2:
+            vis *= j <= i
+        elif self.sparse_mode == 3:
+            vis *= j <= i + (Skv - Sq)
+        elif self.sparse_mode is not None:
+            raise ValueError("sparse_mode must be None, 0, 2 or 3")
+        if self.atten_mask is not None:
+            vis *= 1.0 - _pick(self.atten_mask, b, h, ri, Skv)
+        return vis
+
+    def keep(self, b, h, ri, Skv):
+        if self.drop_mask is None:
+            return 1.0 if self.keep_prob == 1.0 else 1.0 / self.keep_prob
+        return _pick(self.drop_mask, b, h, ri, Skv) / self.keep_prob
+
+
+def _pick(x, b, h, ri, Skv):
+    """Rows ri of (b, h) of an array broadcastable to [B, H, S, Skv]."""
+    x = np.asarray(x, dtype=np.float64)
+    while x.ndim < 4:
+        x = x[None]
+    xb = x[b if x.shape[0] > 1 else 0, h if x.shape[1] > 1 else 0]
+    return np.broadcast_to(xb[ri] if xb.shape[0] > 1 else xb, (len(ri), Skv))

@@ -51,8 +51,11 @@ def attention_bwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, o: np.ndarray, ls
                   do: np.ndarray, scale: float, mask: int = MASK_NONE,
                   seqlens: Optional[np.ndarray] = None,
                   kv_block_idx: Optional[np.ndarray] = None,
-                  topk_idx: Optional[np.ndarray] = None, block: int = BLOCK):
-    """Reference backward.
+                  topk_idx: Optional[np.ndarray] = None, block: int = BLOCK, extras=None):
+    """Reference backward.  ``extras`` (oracle.attention.Extras): masks and
+    position bias change P only; dropout enters as the FlashAttentionScoreGrad
+    write-up gives it (section 5.2): dV = (P * M / keep_prob)^T dO and
+    dS = P * (dP * M / keep_prob - d_row).
 
     q [B,Hq,Sq,D], k [B,Hkv,Skv,D], v [B,Hkv,Skv,Dv], o / do [B,Hq,Sq,Dv] and
     lse [B,Hq,Sq] (the forward's outputs; +inf on rows without keys), all
@@ -78,15 +81,21 @@ def attention_bwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, o: np.ndarray, ls
             w = _multiplicity(rows, b, h, qlen, kvlen, Skv, nkb, block, mask, kv_block_idx,
                               topk_idx)
             s = q[b, h] @ k[b, kh].T
+            keep = 1.0
+            if extras is None:
+                st = scale * s
+            else:
+                st = extras.scores(s, scale, b, h, rows, Hq, Sq, Skv)
+                w = w * extras.visible(b, h, rows, Sq, Skv)
+                keep = extras.keep(b, h, rows, Skv)
             lse_h = lse[b, h][:, None]
             live = np.isfinite(lse_h) & (w > 0)
             with np.errstate(over="ignore", invalid="ignore"):
-                p = np.where(live, w * np.exp(scale * s - np.where(np.isfinite(lse_h), lse_h, 0.0)),
-                             0.0)
+                p = np.where(live, w * np.exp(st - np.where(np.isfinite(lse_h), lse_h, 0.0)), 0.0)
             d_row = (do[b, h] * o[b, h]).sum(axis=-1)
             d_row = np.where(np.isfinite(lse[b, h]), d_row, 0.0)
-            dv[b, kh] += p.T @ do[b, h]
-            dp = do[b, h] @ v[b, kh].T
+            dv[b, kh] += (p * keep).T @ do[b, h]
+            dp = (do[b, h] @ v[b, kh].T) * keep
             ds = p * (dp - d_row[:, None])
             dq[b, h] = scale * (ds @ k[b, kh])
             dk[b, kh] += scale * (ds.T @ q[b, h])
@@ -141,3 +150,44 @@ def backward_emulation(q: np.ndarray, k: np.ndarray, v: np.ndarray, o_out: np.nd
     p_op, ds_op = operand(p), operand(ds)
     out = rnd[out_dtype]
     return (out(scale * (ds_op @ k)), out(scale * (ds_op.T @ q)), out(p_op.T @ do))
+
+
+
+# ------------------------------------------------------------------ dropout masks
+_M0, _M1 = 0xD2511F53, 0xCD9E8D57      # Philox4x32 round multipliers
+_W0, _W1 = 0x9E3779B9, 0xBB67AE85      # key schedule increments (Weyl)
+
+
+def philox4x32(counter, key, rounds: int = 10):
+    """Philox4x32-R (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+    easy as 1, 2, 3", SC 2011): 4 x 32-bit counter, 2 x 32-bit key.  Each
+    round maps (c0, c1, c2, c3) to (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2),
+    hi(M0 c0) ^ c3 ^ k1, lo(M0 c0)); the key grows by the Weyl constants
+    between rounds."""
+    c = [int(x) & 0xFFFFFFFF for x in counter]
+    k0, k1 = (int(x) & 0xFFFFFFFF for x in key)
+    for r in range(rounds):
+        p0 = _M0 * c[0]
+        p1 = _M1 * c[2]
+        c = [((p1 >> 32) ^ c[1] ^ k0) & 0xFFFFFFFF, p1 & 0xFFFFFFFF,
+             ((p0 >> 32) ^ c[3] ^ k1) & 0xFFFFFFFF, p0 & 0xFFFFFFFF]
+        if r + 1 < rounds:
+            k0 = (k0 + _W0) & 0xFFFFFFFF
+            k1 = (k1 + _W1) & 0xFFFFFFFF
+    return c
+
+
+def philox_dropout_mask(seed: int, offset: int, n: int, keep_prob: float) -> np.ndarray:
+    """0/1 keep mask of n elements as the FlashAttentionScoreGrad write-up
+    draws it (section 5.3): the seed's low and high 32 bits are the key, the
+    counter starts at offset / 16, every Philox output gives 16 bytes (words
+    in order, bytes of a word low first; the pages leave the order open), and
+    an element is kept when its byte is below keep_prob * 255."""
+    key = (seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF)
+    ctr0 = offset // 16
+    out = np.empty(((n + 15) // 16) * 16, dtype=np.uint8)
+    for t in range(len(out) // 16):
+        c = ctr0 + t
+        words = philox4x32((c & 0xFFFFFFFF, (c >> 32) & 0xFFFFFFFF, 0, 0), key)
+        out[16 * t:16 * t + 16] = np.array(words, dtype="<u4").view(np.uint8)
+    return (out[:n] < keep_prob * 255).astype(np.uint8)
