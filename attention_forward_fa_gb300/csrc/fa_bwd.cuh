@@ -18,7 +18,7 @@
 // Every hand-off is an mbarrier with a bounded wait.
 //
 // Precision: every MMA runs on fp16 operands (bf16 inputs arrive as fp16
-// copies); P and dS are fp16, and on query rows with fewer than kHiLoKeys
+// copies); P and dS are fp16, and on query rows with fewer than kBwdHiLoKeys
 // valid keys a second fp16 term x - fp16(x) doubles the product (the
 // forward's hi + lo split).  d_row should come from O + o_lo, the forward's
 // output and its rounding residual: from the rounded output alone the dpsum
@@ -29,6 +29,10 @@
 namespace fa {
 
 constexpr int kBwdThreads = 192;
+// query rows with fewer keys than this take the hi + lo split of P and dS
+// (twice the forward's threshold: the backward's fp16 dS rounding reaches
+// the rows just above the threshold, and 512 keeps about half the bound free)
+constexpr int kBwdHiLoKeys = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct BwdParams {
@@ -85,9 +89,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, WaitCtx
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
-// Rows of a query tile with fewer than kHiLoKeys valid keys take the hi + lo split.
+// Rows of a query tile with fewer than kBwdHiLoKeys valid keys take the hi + lo split.
 __device__ __forceinline__ bool bwd_hilo(int q0, int kv_len, int causal) {
-  return (causal ? min(q0 + 1, kv_len) : kv_len) < kHiLoKeys;
+  return (causal ? min(q0 + 1, kv_len) : kv_len) < kBwdHiLoKeys;
 }
 
 // P (fp32, 128 values of one row) into TMEM as fp16 at `t`, and the

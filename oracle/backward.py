@@ -113,7 +113,7 @@ def latent_grad(dk: np.ndarray, dv: np.ndarray) -> np.ndarray:
 def backward_emulation(q: np.ndarray, k: np.ndarray, v: np.ndarray, o_out: np.ndarray,
                        lse: np.ndarray, do: np.ndarray, scale: float, causal: bool,
                        o_lo: Optional[np.ndarray] = None, op_dtype: str = "fp16",
-                       hilo_keys: int = 256, out_dtype: str = "bf16"):
+                       hilo_keys: int = 512, out_dtype: str = "bf16"):
     """Emulation of a tensor-core backward's roundings, for one (batch, head).
 
     q [Sq, D], k [Skv, D], v [Skv, Dv], do [Sq, Dv] hold the exact values of

@@ -4,7 +4,7 @@ oracle/backward.py against the fp64 backward oracle, on one causal bf16 head
 |d| <= 1e-4 + 7.8125e-3 |ref| (BSA implementation notes, section 1).
 
 * With P and dS as fp16 operands, split into hi + lo fp16 pairs on query rows
-  with fewer than 256 keys, and d_row = rowsum(dO * (o + o_lo)) from the
+  with fewer than 512 keys (the backward kernels' threshold), and d_row = rowsum(dO * (o + o_lo)) from the
   forward's output and its rounding residual, dQ, dK and dV meet the bound.
 * Without the residual (d_row from the rounded output alone) dQ and dK miss
   it by an order of magnitude: the residual output is what the precise-dpsum
