@@ -173,6 +173,9 @@ __device__ __forceinline__ void bwd_store_row(uint32_t t, bool have, float mul, 
 // ---------------------------------------------------------------------------
 // dK and dV of one 128-key tile.  TMEM: S^T / P^T at column 0, dP^T / dS^T at
 // 128, dV at 256, dK at 384 (rows = keys).
+// With GQA (G > 1) every step takes the hi + lo split: dK and dV then sum the
+// fp16 roundings of P and dS over the group's heads, and long rows' terms
+// alone pass the elementwise bound where the result nearly cancels.
 template <bool kBF16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
@@ -255,7 +258,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!dead && !__all_sync(0xffffffffu, wait_bar(BAR_S, n & 1, wc))) dead = true;
       if (!dead) {
         tc_fence_after();
-        const bool hilo = bwd_hilo(q0, kv_len, p.causal);
+        const bool hilo = p.G > 1 || bwd_hilo(q0, kv_len, p.causal);   // GQA: every row (see above)
         const int lim = p.causal ? kj - q0 : -1;   // query column i sees the key iff i >= lim
         float pr[128];
         {
@@ -346,7 +349,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       const int g = n / nq, qt = qt_lo + n - g * nq;
       (void)g;
-      const bool hilo = bwd_hilo(qt * 128, kv_len, p.causal);
+      const bool hilo = p.G > 1 || bwd_hilo(qt * 128, kv_len, p.causal);
       const uint64_t m_q = sw128_desc(sq, 128 * 128, 1024), m_do = sw128_desc(sdo, 128 * 128, 1024);
       // dV += P^T dO, dK += dS^T Q (K = the step's 128 queries)
 #pragma unroll

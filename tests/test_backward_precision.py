@@ -10,6 +10,9 @@ oracle/backward.py against the fp64 backward oracle, on one causal bf16 head
   it by an order of magnitude: the residual output is what the precise-dpsum
   check of the sparse-MLA page asks the forward for.
 * bf16 dS misses it, and so do fp16 operands without the short-row split.
+* A GQA group (4 heads, S 1024): dK and dV sum the group's roundings, and
+  the short-row split alone misses the bound; the split on every row (the
+  dK / dV kernel's rule when G > 1) meets it.
 """
 import numpy as np
 import pytest
@@ -73,3 +76,28 @@ def test_emulation_without_roundings_is_the_oracle(head):
                                 out_dtype=None)
     for g, r in zip(got, ref):
         assert np.linalg.norm(g - r) / np.linalg.norm(r) < 1e-6
+
+
+def test_gqa_group_needs_the_split_on_every_row():
+    rng = np.random.default_rng(9)
+    S, D, G = 1024, 128, 4
+    scale = 1 / np.sqrt(D)
+    k, v = (round_bf16(rng.standard_normal((S, D))) for _ in range(2))
+    qs = [round_bf16(rng.standard_normal((S, D))) for _ in range(G)]
+    dos = [round_bf16(rng.standard_normal((S, D))) for _ in range(G)]
+    q4, do4 = np.stack(qs)[None], np.stack(dos)[None]
+    o, lse = A.attention_fwd(q4, k[None, None], v[None, None], scale, mask=A.MASK_CAUSAL)
+    _, rk, rv = BW.attention_bwd(q4, k[None, None], v[None, None], o, lse, do4, scale, mask=A.MASK_CAUSAL)
+
+    def group(hilo_keys):
+        dk, dv = np.zeros((S, D)), np.zeros((S, D))
+        for g in range(G):
+            o_out = round_bf16(o[0, g])
+            _, dk_g, dv_g = BW.backward_emulation(qs[g], k, v, o_out, round_fp32(lse[0, g]), dos[g], scale,
+                                                  True, o_lo=round_bf16(o[0, g] - o_out), out_dtype=None,
+                                                  hilo_keys=hilo_keys)
+            dk, dv = dk + dk_g, dv + dv_g      # fp32 accumulators in the kernel: exact here
+        return [float((np.abs(round_bf16(x) - r) / (ATOL + RTOL * np.abs(r))).max())
+                for x, r in ((dk, rk[0, 0]), (dv, rv[0, 0]))]
+    assert max(group(512)) > 1.0
+    assert max(group(S + 1)) < 1.0

@@ -59,7 +59,7 @@ def dkdv_model(B, Hq, Hkv, Sq, Skv, causal, seqlens):
             qi = q0 + rows[None, :]             # query column i
             lim = kj - q0 if causal else -1
             mask = (kj < kv_len) & (rows[None, :] >= lim) & (qi < q_len)   # LSE +inf past q_len
-            hilo = (min(q0 + 1, kv_len) if causal else kv_len) < 512
+            hilo = G > 1 or (min(q0 + 1, kv_len) if causal else kv_len) < 512
             steps.append((h, qt, mask, hilo))
         written = [k0 + r for r in range(T) if k0 + r < Skv]
         yield b, kvh, kt, steps, written
