@@ -596,6 +596,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   if ((long long)B * Hq > (1LL << 30) || (long long)Sq * 128 > (1LL << 31) ||
       (long long)Skv * 128 > (1LL << 31))
     return FA_ERR_SHAPE;
+  if (((long long)B * Hq * Sq + 7) / 8 > 0x7FFFFFFF) return FA_ERR_SHAPE;   // the d_row launch's grid
   if (D != 128 || Dv != 128) return FA_ERR_UNSUPPORTED;
   for (const void* t : {q, k, v, o, dout, static_cast<const void*>(dq), static_cast<const void*>(dk),
                         static_cast<const void*>(dv)})
@@ -610,7 +611,6 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   // scratch: d_row, and fp16 copies of bf16 Q, K, V, dO (every product runs on fp16)
   const size_t nq = (size_t)B * Hq * Sq * 128, nk = (size_t)B * Hkv * Skv * 128;
   const size_t rows = (size_t)B * Hq * Sq;
-  if ((rows + 7) / 8 > 0x7FFFFFFF) return FA_ERR_SHAPE;   // the d_row launch's grid
   const size_t drow_bytes = (rows * 4 + 255) & ~size_t(255);
   const size_t bytes = drow_bytes + (fp16 ? 0 : 2 * (nq + nk) * 2);
   uint8_t* scratch = static_cast<uint8_t*>(scratch_alloc(bytes, st));
