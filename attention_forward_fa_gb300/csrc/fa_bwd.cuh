@@ -170,6 +170,65 @@ __device__ __forceinline__ void bwd_store_row(uint32_t t, bool have, float mul, 
   }
 }
 
+// The CTA's shared-memory base, barriers and flags (the same plan in both
+// kernels): resident, full[2], empty[2], s_ready, p_ready, acc, drain.
+struct BwdCta {
+  uint8_t* smem;
+  uint32_t sbase;
+  uint32_t bar0;
+  uint32_t* s_tmem;
+  volatile int* s_abort;
+  __device__ uint32_t res() const { return bar0; }
+  __device__ uint32_t full(int s) const { return bar0 + 8u + 8u * s; }
+  __device__ uint32_t empty(int s) const { return bar0 + 24u + 8u * s; }
+  __device__ uint32_t s_ready() const { return bar0 + 40u; }
+  __device__ uint32_t p_ready() const { return bar0 + 48u; }
+  __device__ uint32_t acc() const { return bar0 + 56u; }
+  __device__ uint32_t drain() const { return bar0 + 64u; }
+};
+
+// Setup common to both kernels: barriers (warp 4, lane 0), the 512 TMEM
+// columns (warp 5), then a CTA barrier.  Returns the TMEM base.
+__device__ __forceinline__ uint32_t bwd_setup(BwdCta& c, uint8_t* smem_raw) {
+  c.smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                      ~uintptr_t(1023));
+  c.sbase = smem_u32(c.smem);
+  c.bar0 = c.sbase + BwdSmem::kBarOff;
+  c.s_tmem = reinterpret_cast<uint32_t*>(c.smem + BwdSmem::kMiscOff);
+  c.s_abort = reinterpret_cast<volatile int*>(c.smem + BwdSmem::kMiscOff + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 4 && lane == 0) {
+    mbar_init(c.res(), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(c.full(s), 1);
+      mbar_init(c.empty(s), 1);
+    }
+    mbar_init(c.s_ready(), 1);
+    mbar_init(c.p_ready(), 4);   // lane 0 of each elementwise warp
+    mbar_init(c.acc(), 1);
+    mbar_init(c.drain(), 1);
+    *c.s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(c.s_tmem), 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  return *c.s_tmem;
+}
+
+// Teardown: every role done (the MMA warp drained its products), TMEM freed.
+__device__ __forceinline__ void bwd_teardown(uint32_t tmem) {
+  tc_fence_before();
+  __syncthreads();
+  if ((threadIdx.x >> 5) == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // dK and dV of one 128-key tile.  TMEM: S^T / P^T at column 0, dP^T / dS^T at
 // 128, dV at 256, dK at 384 (rows = keys).
@@ -181,17 +240,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   using SM = BwdSmem;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar0 = sbase + SM::kBarOff;
-  const uint32_t BAR_RES = bar0, BAR_S = bar0 + 40, BAR_P = bar0 + 48, BAR_ACC = bar0 + 56,
-                 BAR_DRAIN = bar0 + 64;
-  auto BAR_FULL = [=](int s) { return bar0 + 8u + 8u * s; };
-  auto BAR_EMPTY = [=](int s) { return bar0 + 24u + 8u * s; };
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + SM::kMiscOff);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + SM::kMiscOff + 4);
-  float* s_rows = reinterpret_cast<float*>(smem + SM::kRowOff);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // heaviest key tiles (the first ones, under a causal mask) first
@@ -208,26 +256,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int nq = (k0 < kv_len && qt_hi > qt_lo) ? qt_hi - qt_lo : 0;
   const int nsteps = nq * p.G;   // step n: head kvh * G + n / nq, query tile qt_lo + n % nq
 
-  if (warp == 4 && lane == 0) {
-    mbar_init(BAR_RES, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(BAR_FULL(s), 1);
-      mbar_init(BAR_EMPTY(s), 1);
-    }
-    mbar_init(BAR_S, 1);
-    mbar_init(BAR_P, 4);   // lane 0 of each elementwise warp
-    mbar_init(BAR_ACC, 1);
-    mbar_init(BAR_DRAIN, 1);
-    *s_abort = 0;
-    fence_mbar_init();
-  }
-  if (warp == 5) {
-    tmem_alloc(smem_u32(s_tmem), 512);
-    tmem_relinquish();
-  }
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *s_tmem;
+  BwdCta cta;
+  const uint32_t tmem = bwd_setup(cta, smem_raw);
+  const uint32_t sbase = cta.sbase;
+  const uint32_t BAR_RES = cta.res(), BAR_S = cta.s_ready(), BAR_P = cta.p_ready(),
+                 BAR_ACC = cta.acc(), BAR_DRAIN = cta.drain();
+  auto BAR_FULL = [=](int s) { return cta.full(s); };
+  auto BAR_EMPTY = [=](int s) { return cta.empty(s); };
+  volatile int* s_abort = cta.s_abort;
   const WaitCtx wc{s_abort, p.status, p.timeout_ns};
 
   if (warp < 4) {
@@ -245,7 +281,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int q0 = qt * 128;
       // this step's per-query values: LSE in log2 units (+inf past the rows)
       // and d_row (0 past the rows), one per thread, read by all
-      float* buf = s_rows + (n & 1) * 256;
+      float* buf = reinterpret_cast<float*>(cta.smem + SM::kRowOff) + (n & 1) * 256;
       {
         const int qi = q0 + row;
         const bool live = qi < q_len;
@@ -382,12 +418,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   }
 
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 5) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
+  bwd_teardown(tmem);
 }
 
 // ---------------------------------------------------------------------------
@@ -398,16 +429,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using SM = BwdSmem;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar0 = sbase + SM::kBarOff;
-  const uint32_t BAR_RES = bar0, BAR_S = bar0 + 40, BAR_P = bar0 + 48, BAR_ACC = bar0 + 56,
-                 BAR_DRAIN = bar0 + 64;
-  auto BAR_FULL = [=](int s) { return bar0 + 8u + 8u * s; };
-  auto BAR_EMPTY = [=](int s) { return bar0 + 24u + 8u * s; };
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + SM::kMiscOff);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + SM::kMiscOff + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // heaviest query tiles (the last ones, under a causal mask) first
@@ -421,26 +442,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int q0 = qt * 128;
   const int nsteps = dense_tiles(qt, p.n_qt, q_len, kv_len, p.causal ? 1 : 0);   // key tiles [0, n)
 
-  if (warp == 4 && lane == 0) {
-    mbar_init(BAR_RES, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(BAR_FULL(s), 1);
-      mbar_init(BAR_EMPTY(s), 1);
-    }
-    mbar_init(BAR_S, 1);
-    mbar_init(BAR_P, 4);
-    mbar_init(BAR_ACC, 1);
-    mbar_init(BAR_DRAIN, 1);
-    *s_abort = 0;
-    fence_mbar_init();
-  }
-  if (warp == 5) {
-    tmem_alloc(smem_u32(s_tmem), 512);
-    tmem_relinquish();
-  }
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *s_tmem;
+  BwdCta cta;
+  const uint32_t tmem = bwd_setup(cta, smem_raw);
+  const uint32_t sbase = cta.sbase;
+  const uint32_t BAR_RES = cta.res(), BAR_S = cta.s_ready(), BAR_P = cta.p_ready(),
+                 BAR_ACC = cta.acc(), BAR_DRAIN = cta.drain();
+  auto BAR_FULL = [=](int s) { return cta.full(s); };
+  auto BAR_EMPTY = [=](int s) { return cta.empty(s); };
+  volatile int* s_abort = cta.s_abort;
   const WaitCtx wc{s_abort, p.status, p.timeout_ns};
 
   if (warp < 4) {
@@ -568,12 +577,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   }
 
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 5) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
+  bwd_teardown(tmem);
 }
 
 // d_row = rowsum(dO * (O + O_lo)) in fp32, one warp per row of 128 values.
