@@ -11,7 +11,6 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libfa_fwd.so")
 SOURCES = ["fa_fwd.cu"]
-DEPS = ["fa_fwd.cu", "fa_tiled.cuh", "fa_ptx.cuh", "fa_mla.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -29,7 +28,9 @@ def up_to_date() -> bool:
     if not os.path.exists(LIB):
         return False
     t = os.path.getmtime(LIB)
-    files = [os.path.join(CSRC, f) for f in DEPS] + [os.path.join(ROOT, "include", "fa_fwd.h")]
+    # every source and header under csrc/ (the translation unit includes them all)
+    files = [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC)) if f.endswith((".cu", ".cuh"))]
+    files.append(os.path.join(ROOT, "include", "fa_fwd.h"))
     return all(os.path.getmtime(f) <= t for f in files)
 
 
