@@ -132,3 +132,14 @@ def test_kv_split_setter_range(lib):
 ])
 def test_convert_v_argument_errors(lib, args, code):
     assert B.fa_convert_v_fp16(*args, stream=0) == code
+
+
+def test_backward_wrapper_rejects_host_or_mixed_tensors():
+    torch = pytest.importorskip("torch")
+    import attention_forward_fa_gb300 as fa
+    q = torch.zeros(1, 2, 8, 128, dtype=torch.bfloat16)
+    lse = torch.zeros(1, 2, 8)
+    with pytest.raises(ValueError):
+        fa.flash_attention_backward(q, q, q, q, lse, q)                  # host tensors
+    with pytest.raises(ValueError):
+        fa.flash_attention_backward(q, q.half(), q, q, lse, q)           # mixed types
