@@ -135,6 +135,23 @@ WORKLOADS = {
 }
 
 
+def max_over_ranks(dist, values, device):
+    """Element-wise maximum of per-rank values over all ranks (the whole job
+    is as slow as its slowest rank); values unchanged without a process group."""
+    if dist is None:
+        return [float(x) for x in values]
+    import torch
+    t = torch.tensor([float(x) for x in values], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def whole_job_tflops(world, flops_per_rank_step, ms_per_step):
+    """Throughput of all ranks together: every rank runs one step's work in
+    ms_per_step (replicas, weak scaling)."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def workload_problem(name="c2", mla_tokens=4096):
     from attention_forward_fa_gb300 import workloads as W
     if name == "c5" and mla_tokens != 4096:
@@ -381,12 +398,9 @@ def run_ours(args, world, rank, local):
         conv_ms = [e[0].elapsed_time(e[1]) for e in evs]
         kern_avg_ms = sum(kern_ms) / len(kern_ms)
         conv_avg_ms = sum(conv_ms) / len(conv_ms)
-    if dist:
-        t = torch.tensor([total_ms, kern_avg_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, kern_avg_ms = float(t[0]), float(t[1])
+    total_ms, kern_avg_ms = max_over_ranks(dist, [total_ms, kern_avg_ms], dev)
     ms_per_step = total_ms / args.steps
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops, ms_per_step)
 
     # end to end through the public entry point with host buffers
     pin = lambda x: x.cpu().pin_memory()  # noqa: E731
@@ -451,11 +465,8 @@ def run_ours(args, world, rank, local):
     e1.record(s_out)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / n_e2e
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
-    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(dist, [e2e_ms], dev)[0]
+    e2e_value = whole_job_tflops(world, flops, e2e_ms)
 
     if rank != 0:
         if dist:
