@@ -23,9 +23,12 @@ namespace {
 // bit 0 = a bounded wait expired, bit 1 = a bf16 V value overflowed fp16.
 __device__ int g_fa_status;
 
-// Fixed scratch of fa_fwd_noalloc: room for the fp16 copy of a bf16 V of up
-// to kNoAllocScratchBytes.  It is part of the module image, so every device
-// that loads this library holds it until the process exits.
+// Fixed scratch of fa_fwd_noalloc, kNoAllocScratchBytes long.  It holds either
+// the fp16 copy of a bf16 key latent (top-k calls) or the fp32 O / l and LSE
+// pieces of a dense call split along its KV tiles; any two fa_fwd_noalloc calls
+// that overlap on the GPU therefore race on it, whatever their kinds.  It is
+// part of the module image, so every device that loads this library holds it
+// until the process exits.
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;   // 32 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -717,6 +720,9 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* 
                           kv_block_idx, topk_idx, rescale_threshold);
   if (rc != FA_OK) return rc;
   const bool fp16 = (mask_mode & (FA_DTYPE_FP16 | FA_V_FP16)) != 0;   // latent already fp16
+  // the latent's size is checked with the other arguments, before any CUDA call
+  const size_t nv = (size_t)B * Skv * D;
+  if (topk_idx && !fp16 && nv * 2 > kNoAllocScratchBytes) return FA_ERR_SCRATCH;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* status = status_ptr();
   if (!status) return cuda_fail(cudaGetLastError());
@@ -724,8 +730,6 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* 
                    // use the fixed scratch (unsplit when they do not fit)
     return run_tiled(q, k, v, o, nullptr, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode,
                      seqlens, kv_block_idx, rescale_threshold, status, st, /*may_alloc=*/false);
-  const size_t nv = (size_t)B * Skv * D;
-  if (!fp16 && nv * 2 > kNoAllocScratchBytes) return FA_ERR_SCRATCH;
   void* k16 = const_cast<void*>(k);
   if (!fp16) {
     // bf16 key latent -> fp16 into the fixed scratch (every element is

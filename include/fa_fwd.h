@@ -47,7 +47,11 @@
  *     fp16 into stream-ordered scratch.  Scratch comes from cudaMallocAsync
  *     on the device's default memory pool and is released on `stream` after
  *     use; fa_fwd_noalloc uses a fixed array instead and allocates nothing at
- *     all (a split that does not fit it runs unsplit).
+ *     all (a split that does not fit it runs unsplit).  Why scratch at all:
+ *     the split's partial results must outlive the kernel that writes them
+ *     until the merge kernel reads them, and the top-k kernel reads each
+ *     latent row many times (once per token that lists it), so converting
+ *     it once per call is cheaper than converting it at every gather.
  */
 #ifndef FA_FWD_H_
 #define FA_FWD_H_
@@ -202,16 +206,23 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
  * For callers that cannot let a library allocate device memory: programs that
  * hand out all device memory from their own fixed arena and account for every
  * byte, and latency-critical call sites where a driver allocation (and the
- * synchronisation it may imply) is not acceptable.  fa_fwd's top-k path
- * converts a bf16 key latent to fp16 in stream-ordered scratch taken from the
- * device's memory pool; this entry point uses a fixed array inside the
- * library's device image instead (32 MiB, held by every device that loads the
- * library until the process exits) and calls no cudaMalloc, cudaFree or other
- * allocating routine.  (The other paths allocate nothing in either entry.)
+ * synchronisation it may imply) is not acceptable.  fa_fwd takes
+ * stream-ordered scratch from the device's memory pool in two cases: the fp16
+ * copy of a bf16 key latent (top-k path) and the fp32 partial results of a
+ * dense problem split along its KV tiles (too few units to fill half the
+ * GPU).  This entry point puts either into one fixed array inside the
+ * library's device image instead (32 MiB, held by every device that loads
+ * the library until the process exits) and calls no cudaMalloc, cudaFree or
+ * other allocating routine.  Every other call allocates nothing in either
+ * entry point.
  *
- * Same arguments, layouts and results as fa_fwd.  Differences:
+ * Same arguments, layouts and results as fa_fwd (bit for bit, whenever the
+ * split pieces fit the array).  Differences:
  *   - top-k calls with a bf16 key latent of B*Skv*D*2 bytes > 32 MiB are
- *     rejected with FA_ERR_SCRATCH (fp16 latents need no scratch);
+ *     rejected with FA_ERR_SCRATCH before any CUDA call (fp16 latents need
+ *     no scratch);
+ *   - a split dense problem whose pieces, kv_split * B*Hq*Sq * (4*Dv + 4)
+ *     bytes, exceed 32 MiB runs unsplit (same result, slower);
  *   - the first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
  *     stream capture;

@@ -272,7 +272,12 @@ class Extras:
 
     def keep(self, b, h, ri, Skv):
         if self.drop_mask is None:
-            return 1.0 if self.keep_prob == 1.0 else 1.0 / self.keep_prob
+            # dropout draws which elements it drops: a keep_prob below 1 with
+            # no mask would only rescale P, which is not the formula
+            if self.keep_prob != 1.0:
+                raise ValueError("keep_prob < 1 needs a drop_mask "
+                                 "(draw one with oracle.backward.philox_dropout_mask)")
+            return 1.0
         return _pick(self.drop_mask, b, h, ri, Skv) / self.keep_prob
 
 

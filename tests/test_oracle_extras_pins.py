@@ -116,6 +116,40 @@ def test_dropout_from_the_oracles_own_p():
     assert _same(ones, (o0, l0))
 
 
+def test_dropout_without_a_mask_is_refused():
+    """keep_prob < 1 names a dropout, which drops elements: without the mask
+    that says which, the oracle refuses rather than rescale every element by
+    1 / keep_prob (the formula's O = (P * M / keep_prob) V has no such case)."""
+    q, k, v = _qkv(6, Hq=2, Sq=6, Skv=7)
+    with pytest.raises(ValueError):
+        A.attention_fwd(q, k, v, SCALE, extras=Extras(keep_prob=0.5))
+    with pytest.raises(ValueError):
+        BW.attention_bwd(q, k, v, *A.attention_fwd(q, k, v, SCALE), np.ones_like(q), SCALE,
+                         extras=Extras(keep_prob=0.5))
+    # keep_prob 1 without a mask is no dropout at all
+    assert _same(A.attention_fwd(q, k, v, SCALE, extras=Extras(keep_prob=1.0)),
+                 A.attention_fwd(q, k, v, SCALE))
+
+
+def test_philox_dropout_mask_byte_order_worked_example():
+    """One Philox block worked by hand from the authors' published answer for
+    counter (0, 0, 0, 0) and key (0, 0): words 0x6627E8D5, 0xE169C58D,
+    0xBC57AC4C, 0x9B00DBD8.  Seed 0 and offset 0 select exactly that block;
+    taken word by word, low byte first, its 16 bytes are
+    D5 E8 27 66 | 8D C5 69 E1 | 4C AC 57 BC | D8 DB 00 9B, and with
+    keep_prob 0.5 an element is kept when its byte is below 127.5."""
+    bytes_ = [0xD5, 0xE8, 0x27, 0x66, 0x8D, 0xC5, 0x69, 0xE1,
+              0x4C, 0xAC, 0x57, 0xBC, 0xD8, 0xDB, 0x00, 0x9B]
+    want = [1 if b < 127.5 else 0 for b in bytes_]
+    assert want == [0, 0, 1, 1, 0, 0, 1, 0, 1, 0, 1, 0, 0, 0, 1, 0]
+    assert BW.philox_dropout_mask(seed=0, offset=0, n=16, keep_prob=0.5).tolist() == want
+    # keep_prob 0.9: only the bytes above 229.5 (E8 = 232) are dropped
+    assert BW.philox_dropout_mask(seed=0, offset=0, n=16, keep_prob=0.9).tolist() == \
+        [1 if b < 229.5 else 0 for b in bytes_]
+    # n not a multiple of 16 takes the block's first bytes
+    assert BW.philox_dropout_mask(seed=0, offset=0, n=5, keep_prob=0.5).tolist() == want[:5]
+
+
 def test_philox_known_answers():
     assert BW.philox4x32((0, 0, 0, 0), (0, 0)) == [0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8]
     assert BW.philox4x32((0xFFFFFFFF,) * 4, (0xFFFFFFFF, 0xFFFFFFFF)) == \
