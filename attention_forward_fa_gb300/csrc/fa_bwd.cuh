@@ -337,6 +337,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int n = 0;
       for (; n < nsteps; ++n) {
         const int s = n & 1;
+        // (the MMA warp releases a stage only after it saw the stage's copy
+        // land: it stops at a wait that gave up, so a stage is never reused
+        // with a copy in flight)
         if (!wait_bar(BAR_EMPTY(s), ((n >> 1) & 1) ^ 1, wc)) break;
         const int g = n / nq, qt = qt_lo + n - g * nq;
         const int plane = b * p.Hq + kvh * p.G + g;
@@ -345,10 +348,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bwd_load_tile(st, &p.tm_q, BAR_FULL(s), qt * 128, plane);
         bwd_load_tile(st + SM::kTile, &p.tm_do, BAR_FULL(s), qt * 128, plane);
       }
-      if (*s_abort) {   // copies in flight land before the shared memory goes away
-        drain_bar(BAR_RES, 0, wc.timeout);
-        for (int i = n > 2 ? n - 2 : 0; i < n; ++i) drain_bar(BAR_FULL(i & 1), (i >> 1) & 1, wc.timeout);
-      }
+      // copies in flight land before the shared memory goes away (whether or
+      // not a role gave up: one may give up after this point); each of these
+      // phases is its barrier's last, so on the normal path they pass at once
+      drain_bar(BAR_RES, 0, wc.timeout);
+      for (int i = n > 2 ? n - 2 : 0; i < n; ++i) drain_bar(BAR_FULL(i & 1), (i >> 1) & 1, wc.timeout);
     }
     __syncwarp();
   } else {
@@ -510,16 +514,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int n = 0;
       for (; n < nsteps; ++n) {
         const int s = n & 1;
-        if (!wait_bar(BAR_EMPTY(s), ((n >> 1) & 1) ^ 1, wc)) break;
+        if (!wait_bar(BAR_EMPTY(s), ((n >> 1) & 1) ^ 1, wc)) break;   // (as in the dK / dV kernel)
         const uint32_t st = sbase + SM::kStage + s * 2 * SM::kTile;
         mbar_arrive_expect_tx(BAR_FULL(s), 2 * SM::kTile);
         bwd_load_tile(st, &p.tm_k, BAR_FULL(s), n * 128, b * p.Hkv + kvh);
         bwd_load_tile(st + SM::kTile, &p.tm_v, BAR_FULL(s), n * 128, b * p.Hkv + kvh);
       }
-      if (*s_abort) {
-        drain_bar(BAR_RES, 0, wc.timeout);
-        for (int i = n > 2 ? n - 2 : 0; i < n; ++i) drain_bar(BAR_FULL(i & 1), (i >> 1) & 1, wc.timeout);
-      }
+      drain_bar(BAR_RES, 0, wc.timeout);   // as in the dK / dV kernel
+      for (int i = n > 2 ? n - 2 : 0; i < n; ++i) drain_bar(BAR_FULL(i & 1), (i >> 1) & 1, wc.timeout);
     }
     __syncwarp();
   } else {

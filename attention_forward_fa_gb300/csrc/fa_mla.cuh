@@ -59,7 +59,12 @@ constexpr int kMlaThreads = 32 * (kMlaMmaWarp + 1);
 constexpr int kMlaMaxTopk = 2048;            // longest slot list
 constexpr int kMlaBoxes = kMlaD / 64;        // 128-byte column boxes per key row
 constexpr int kMlaQtBoxes = 5;               // query boxes kept in TMEM (columns 0-319)
-constexpr int kMlaHiLoKeys = 256;
+// Tokens with fewer keys than this take the hi + lo split on every tile.  The
+// sparse-MLA rows are peaked (a few keys carry most of the weight), so fp16
+// P alone leaves less margin than on the dense kernel's rows: in an fp16-P
+// emulation of the kernel, rows of 256-300 keys reach 1.15x the elementwise
+// bound, rows of 512 keys and more stay at or below 0.65x.
+constexpr int kMlaHiLoKeys = 512;
 constexpr uint32_t kMlaColO = 0, kMlaColS = 256, kMlaColP = 320, kMlaColQ = 352;
 static_assert(kMlaColQ + 32 * kMlaQtBoxes == 512, "TMEM plan");
 

@@ -435,17 +435,16 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     float m = -INFINITY, l = 0.f;
     bool dead = false;   // a bounded wait expired: keep the hand-offs, skip the work
     for (int j = 0; j < nt; ++j) {
-      if (!dead && !__all_sync(0xffffffffu, wait_bar(BAR_SFULL(t), j & 1, wc))) {
-        dead = true;
-      } else if (dead) {
-        // Paced by the issuer's S commits (a bounded wait past the abort
-        // flag): the issuer commits S of tile j only after its "P ready" wait
-        // for tile j - 1, so these arrivals never run two generations ahead
-        // of it (which would leave it waiting on the hardware barrier).
-        drain_bar(BAR_SFULL(t), j & 1, wc.timeout);
-      }
+      if (!dead && !__all_sync(0xffffffffu, wait_bar(BAR_SFULL(t), j & 1, wc))) dead = true;
       if (dead) {
-        // the MMA issuer waits for one arrival per tile on a hardware barrier
+        // The MMA issuer waits for one arrival per tile on a hardware barrier.
+        // Each arrival, also the one for the tile this warp gave up on, is
+        // paced by the issuer's S commit of that tile (a bounded wait past the
+        // abort flag): the issuer commits S of tile j only after its "P ready"
+        // wait for tile j - 1 completed, so the arrival lands in tile j's
+        // generation.  Arriving at once could land it in tile j - 1's, still
+        // open, and complete that generation with the wrong set of warps.
+        drain_bar(BAR_SFULL(t), j & 1, wc.timeout);
         named_arrive(kBarPReady + t, kPReadyCount);
         continue;
       }
@@ -779,7 +778,15 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         const uint32_t f = ld / NS;
         ++ld;
         if (ld <= early) continue;   // issued before the setup barrier
-        if (!wait_bar(BAR_EMPTY(s), (f & 1) ^ 1, wc)) break;
+        // the stage's readers are done, and its previous copy has landed (its
+        // readers waited for it on the normal path, but after a give-up they
+        // release the stage without waiting): at most one copy is ever in
+        // flight per stage, so each phase of its barrier belongs to one copy
+        if (!wait_bar(BAR_EMPTY(s), (f & 1) ^ 1, wc) ||
+            (f > 0 && !wait_bar(BAR_FULL(s), (f - 1) & 1, wc))) {
+          --ld;   // not issued: ld counts the loads in flight or landed
+          break;
+        }
         const int kvt = sparse ? s_list[ev.t * kMaxSel + ev.j] : kv_lo + ev.j;
         FA_TR(5, ev.t, ev.j);
         mbar_arrive_expect_tx(BAR_FULL(s), SM::kStageBytes);
@@ -788,13 +795,15 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           tma_load_3d(sStage + s * SM::kStageBytes + bx * (kBN * 128), tm, BAR_FULL(s), 64 * bx,
                       kvt * kBN, b * p.Hkv + kvh);
       }
-      if (*s_abort) {
-        // let every copy in flight land before the CTA's shared memory goes away
-        for (int i = (ld > NS ? ld - NS : 0); i < ld; ++i)
-          drain_bar(BAR_FULL(i % NS), (i / NS) & 1, wc.timeout);
-        for (int t = 0; t < 2; ++t)
-          if ((t ? n1 : n0) > 0) drain_bar(BAR_QFULL(t), 0, wc.timeout);
-      }
+      // Every copy lands before the CTA's shared memory goes away: the last
+      // load of each stage and the Q tiles, whether or not some role gave up
+      // (a role may give up after this point, with a copy still in flight).
+      // On the normal path these phases completed long ago (each is its
+      // stage's last), so the waits pass at once.
+      for (int i = (ld > NS ? ld - NS : 0); i < ld; ++i)
+        drain_bar(BAR_FULL(i % NS), (i / NS) & 1, wc.timeout);
+      for (int t = 0; t < 2; ++t)
+        if ((t ? n1 : n0) > 0) drain_bar(BAR_QFULL(t), 0, wc.timeout);
     }
     __syncwarp();
   } else if (warp == 13 || warp == 14) {

@@ -8,6 +8,10 @@ the measured dense bf16 tensor peak.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+With the default workload (c2) the line also carries a "workloads" entry for
+the other workloads (c3 GQA causal ragged, c4 block-sparse, c5 top-k sparse
+MLA), each timed the same way after the benchmark line's own timed region.
+
 N > 1 runs one process per GPU (torchrun); every rank runs its own replica of
 the workload (the forward shards over (b, h) with no exchange), so the
 scaling is weak and the whole-job value is the sum over ranks.
@@ -250,6 +254,202 @@ def run_reference(args, world, rank):
     return 0
 
 
+class Prepared:
+    """Device buffers of one workload: rotating input / output sets larger than
+    L2 together, and the fa_fwd arguments."""
+
+    def __init__(self, p, dev):
+        import torch
+        import attention_forward_fa_gb300 as fa
+        self.p = p
+        bf16 = p.dtype == "bf16"
+        self.bf16 = bf16
+        dt = torch.bfloat16 if bf16 else torch.float16
+        self.dt = dt
+
+        def up(bits):
+            return torch.from_numpy(bits.view(np.int16).copy()).to(dev).view(dt)
+
+        def up_i32(a):
+            return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+        self.q0, self.k0 = up(p.q_bits), up(p.k_bits)
+        self.v0 = None if p.v_from_k else up(p.v_bits)
+        self.seqlens = up_i32(p.seqlens)
+        self.blk = self.tk = None
+        if p.kv_block_idx is not None:
+            bi = up_i32(p.kv_block_idx)
+            nb, hh, nqb, ms = bi.shape
+            self.blk = (bi, ms, 128, hh * nqb * ms, nqb * ms if hh > 1 else 0)
+        if p.topk_idx is not None:
+            ti = up_i32(p.topk_idx)
+            self.tk = (ti, ti.shape[-1], ti.shape[-2] * ti.shape[-1])
+        # top-k with a bf16 key latent: the latent (V is part of it) is
+        # converted to fp16 by a separate pass; a bf16 V of the other paths is
+        # converted inside the attention kernel
+        self.conv_pass = bf16 and p.v_from_k
+        self.n_conv = self.k0.numel() if self.conv_pass else 0
+        mode = p.mask | (fa.FA_V_FROM_K if p.v_from_k else 0)
+        if not bf16:
+            mode |= fa.FA_DTYPE_FP16
+        elif self.conv_pass:
+            mode |= fa.FA_V_FP16
+        self.mode = mode
+        o_bytes = 2 * p.B * p.Hq * p.Sq * p.Dv + 4 * p.B * p.Hq * p.Sq
+        v_n = 0 if self.v0 is None else self.v0.numel()
+        self.per_set = 2 * (self.q0.numel() + self.k0.numel() + v_n) + 2 * self.n_conv + o_bytes
+        self.n_sets = max(2, int(np.ceil(2.5 * L2_BYTES / self.per_set)))
+        self.sets = []
+        for _ in range(self.n_sets):
+            o = torch.empty((p.B, p.Hq, p.Sq, p.Dv), dtype=dt, device=dev)
+            lse = torch.empty((p.B, p.Hq, p.Sq), dtype=torch.float32, device=dev)
+            q, k = self.q0.clone(), self.k0.clone()
+            v = None if self.v0 is None else self.v0.clone()
+            c16 = torch.empty(k.shape, dtype=torch.float16, device=dev) if self.conv_pass else None
+            self.sets.append((q, k, v, c16, o, lse))
+
+    def step(self, i, strm, ev=None):
+        """One step = the whole hot path: one fa_fwd launch, plus for a bf16
+        top-k latent the conversion pass before it (issued through the C ABI on
+        its own so that the attention kernel can be timed alone)."""
+        import attention_forward_fa_gb300 as fa
+        p = self.p
+        ssp = strm.cuda_stream
+        q, k, v, c16, o, lse = self.sets[i % self.n_sets]
+        if ev:
+            ev[0].record(strm)
+        if self.conv_pass:
+            code = fa.fa_convert_v_fp16(k, c16, self.n_conv, ssp)
+            if code != 0:
+                raise RuntimeError(fa.fa_strerror(code))
+        if ev:
+            ev[1].record(strm)
+        code = fa.fa_fwd(q, c16 if self.conv_pass else k, v, o, lse, p.B, p.Hq, p.Hkv, p.Sq,
+                         p.Skv, p.D, p.Dv, p.scale, self.mode, self.seqlens, self.blk, self.tk,
+                         0.0, ssp)
+        if code != 0:
+            raise RuntimeError(fa.fa_strerror(code))
+        if ev:
+            ev[2].record(strm)
+
+
+def timed_steps(prep, steps, warmup, soak, dist, local, no_graph=False):
+    """Warm-up, an untimed soak (clocks sampled under load from its start),
+    then exactly `steps` steps between a barrier + synchronize on both sides.
+    Returns (total ms, mean attention-kernel ms, mean conversion ms, clocks,
+    graph used)."""
+    import torch
+    import attention_forward_fa_gb300 as fa
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        prep.step(i, stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else local)
+    sampler.start()
+    t_soak = time.perf_counter()
+    i = 0
+    while time.perf_counter() - t_soak < soak:
+        for _ in range(20):
+            prep.step(i, stream)
+            i += 1
+        torch.cuda.synchronize()
+    # A step that is one launch (every workload but a bf16 top-k latent) runs
+    # as a CUDA graph of the K launches, captured beforehand: the events around
+    # the replay then time K launches of that one kernel, so its average launch
+    # duration is the step time.  A two-launch step runs eagerly with events
+    # around each launch.
+    use_graph = not prep.conv_pass and not no_graph
+    evs = None
+    graph = None
+    if use_graph:
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            prep.step(0, cap)
+            cap.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=cap):
+                for s_ in range(steps):
+                    prep.step(s_, cap)
+        torch.cuda.synchronize()
+    else:
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    t_all0.record(stream)
+    if use_graph:
+        graph.replay()
+    else:
+        for s_ in range(steps):
+            prep.step(s_, stream, evs[s_])
+    t_all1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    status = fa.fa_check_status()
+    if status != 0:
+        raise RuntimeError("device status after timed region: " + fa.fa_strerror(status))
+    total_ms = t_all0.elapsed_time(t_all1)
+    if use_graph:
+        kern_avg_ms = total_ms / steps
+        conv_avg_ms = 0.0
+    else:
+        kern_ms = [e[1].elapsed_time(e[2]) for e in evs]
+        conv_ms = [e[0].elapsed_time(e[1]) for e in evs]
+        kern_avg_ms = sum(kern_ms) / len(kern_ms)
+        conv_avg_ms = sum(conv_ms) / len(conv_ms)
+    del graph
+    return total_ms, kern_avg_ms, conv_avg_ms, clocks, use_graph
+
+
+def kernel_name(p):
+    bf16 = p.dtype == "bf16"
+    if p.topk_idx is not None:
+        return f"fa_mla_topk_kernel<{'bf16' if bf16 else 'fp16'}>"
+    return (f"fa_fwd_tiled_kernel<{p.D},{'bf16' if bf16 else 'fp16'},{4 if p.D == 128 else 6}"
+            f"{',convert-V' if bf16 else ''}>")
+
+
+def other_workloads(args, dev, dist, world, local, peak):
+    """The same path on the other workloads (one fa_fwd call per step, threshold
+    0, the given slot order), each timed like the benchmark line with its own
+    clock record: ms per call, algorithmic TFLOP/s, fraction of the peak, and
+    the DRAM bytes per launch of the latest ncu capture of that kernel (null
+    when its sources changed since)."""
+    import torch
+    from attention_forward_fa_gb300 import workloads as W
+    out = {}
+    for name in ("c3", "c4", "c5"):
+        p = workload_problem(name)
+        flops = W.algorithmic_flops(p)
+        prep = Prepared(p, dev)
+        total_ms, kern_ms, conv_ms, clocks, graph = timed_steps(
+            prep, args.workload_steps, 5, args.workload_soak, dist, local)
+        total_ms, kern_ms = max_over_ranks(dist, [total_ms, kern_ms], dev)
+        ms = total_ms / args.workload_steps
+        achieved = flops / (kern_ms * 1e-3) / 1e12
+        e = {"config": workload_desc(p, name), "algorithmic_gflop": flops / 1e9,
+             "ms_per_call": ms, "tflops": whole_job_tflops(world, flops, ms),
+             "kernel": kernel_name(p), "kernel_ms": kern_ms,
+             "kernel_tflops": achieved, "frac": achieved / peak, "steps": args.workload_steps,
+             "timing": "CUDA graph of the steps" if graph else "eager, events around each launch",
+             "clocks": clocks, "traffic": dram_traffic(name)}
+        if e["traffic"] is not None:
+            e["dram_gbs"] = e["traffic"] / (kern_ms * 1e-3) / 1e9
+        if prep.conv_pass:
+            e["other_kernel"] = {"name": "fa_convert_v_kernel (bf16 -> fp16 copy of the key latent)",
+                                 "avg_ms": conv_ms}
+        out[name] = e
+        del prep
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, world, rank, local):
     import torch
     import attention_forward_fa_gb300 as fa
@@ -269,138 +469,18 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     p = workload_problem(args.workload, args.mla_tokens)
     flops = W.algorithmic_flops(p)
-    bf16 = p.dtype == "bf16"
-    dt = torch.bfloat16 if bf16 else torch.float16
+    prep = Prepared(p, dev)
+    bf16, dt = prep.bf16, prep.dt
+    q0, k0, v0 = prep.q0, prep.k0, prep.v0
+    seqlens, blk, tk = prep.seqlens, prep.blk, prep.tk
+    sets, n_sets, per_set, conv_pass = prep.sets, prep.n_sets, prep.per_set, prep.conv_pass
 
-    def up(bits):
-        return torch.from_numpy(bits.view(np.int16).copy()).to(dev).view(dt)
-
-    def up_i32(a):
-        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-
-    q0, k0 = up(p.q_bits), up(p.k_bits)
-    v0 = None if p.v_from_k else up(p.v_bits)
-    seqlens = up_i32(p.seqlens)
-    blk = tk = None
-    if p.kv_block_idx is not None:
-        bi = up_i32(p.kv_block_idx)
-        nb, hh, nqb, ms = bi.shape
-        blk = (bi, ms, 128, hh * nqb * ms, nqb * ms if hh > 1 else 0)
-    if p.topk_idx is not None:
-        ti = up_i32(p.topk_idx)
-        tk = (ti, ti.shape[-1], ti.shape[-2] * ti.shape[-1])
-    # top-k with a bf16 key latent: the latent (V is part of it) is converted to
-    # fp16 by a separate pass; a bf16 V of the other paths is converted inside
-    # the attention kernel
-    conv_pass = bf16 and p.v_from_k
-    n_conv = k0.numel() if conv_pass else 0
-    mode = p.mask | (fa.FA_V_FROM_K if p.v_from_k else 0)
-    if not bf16:
-        mode |= fa.FA_DTYPE_FP16
-    elif conv_pass:
-        mode |= fa.FA_V_FP16
-    o_bytes = 2 * p.B * p.Hq * p.Sq * p.Dv + 4 * p.B * p.Hq * p.Sq
-    per_set = 2 * (q0.numel() + k0.numel() + (0 if v0 is None else v0.numel())) + 2 * n_conv + o_bytes
-    n_sets = max(2, int(np.ceil(2.5 * L2_BYTES / per_set)))
-    sets = []
-    for i in range(n_sets):
-        o = torch.empty((p.B, p.Hq, p.Sq, p.Dv), dtype=dt, device=dev)
-        lse = torch.empty((p.B, p.Hq, p.Sq), dtype=torch.float32, device=dev)
-        q, k = q0.clone(), k0.clone()
-        v = None if v0 is None else v0.clone()
-        c16 = torch.empty(k.shape, dtype=torch.float16, device=dev) if conv_pass else None
-        sets.append((q, k, v, c16, o, lse))
-    stream = torch.cuda.current_stream()
-    sp = stream.cuda_stream
-
-    # One step = the whole hot path: one fa_fwd launch, plus for a bf16 top-k
-    # latent the conversion pass before it (issued through the C ABI on its own
-    # so that the attention kernel can be timed alone).
-    def step(i, ev=None, strm=None):
-        strm = strm or stream
-        ssp = strm.cuda_stream
-        q, k, v, c16, o, lse = sets[i % n_sets]
-        if ev:
-            ev[0].record(strm)
-        if conv_pass:
-            code = fa.fa_convert_v_fp16(k, c16, n_conv, ssp)
-            if code != 0:
-                raise RuntimeError(fa.fa_strerror(code))
-        if ev:
-            ev[1].record(strm)
-        code = fa.fa_fwd(q, c16 if conv_pass else k, v, o, lse, p.B, p.Hq, p.Hkv, p.Sq, p.Skv,
-                         p.D, p.Dv, p.scale, mode, seqlens, blk, tk, 0.0, ssp)
-        if code != 0:
-            raise RuntimeError(fa.fa_strerror(code))
-        if ev:
-            ev[2].record(strm)
-
-    # warm-up, then an untimed soak so that clocks are sampled under load
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
-                           else local)
-    sampler.start()
-    t_soak = time.perf_counter()
-    i = 0
-    while time.perf_counter() - t_soak < args.soak:
-        for _ in range(20):
-            step(i)
-            i += 1
-        torch.cuda.synchronize()
-    # Timed region: exactly K steps.  A step that is one launch (every workload
-    # but a bf16 top-k latent) runs as a CUDA graph of the K launches, captured
-    # beforehand: the events around the replay then time K launches of that one
-    # kernel, so its average launch duration is the step time.  A two-launch
-    # step runs eagerly with events around each launch.
-    use_graph = not conv_pass and not args.no_graph
-    evs = None
-    graph = None
-    if use_graph:
-        cap = torch.cuda.Stream()
-        cap.wait_stream(stream)
-        with torch.cuda.stream(cap):
-            step(0, strm=cap)
-            cap.synchronize()
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=cap):
-                for s_ in range(args.steps):
-                    step(s_, strm=cap)
-        torch.cuda.synchronize()
-    else:
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_all0 = torch.cuda.Event(enable_timing=True)
-    t_all1 = torch.cuda.Event(enable_timing=True)
-    t_all0.record(stream)
-    if use_graph:
-        graph.replay()
-    else:
-        for s_ in range(args.steps):
-            step(s_, evs[s_])
-    t_all1.record(stream)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    clocks = sampler.stop()
-    status = fa.fa_check_status()
-    if status != 0:
-        raise RuntimeError("device status after timed region: " + fa.fa_strerror(status))
-    total_ms = t_all0.elapsed_time(t_all1)
-    if use_graph:
-        kern_avg_ms = total_ms / args.steps
-        conv_avg_ms = 0.0
-    else:
-        kern_ms = [e[1].elapsed_time(e[2]) for e in evs]
-        conv_ms = [e[0].elapsed_time(e[1]) for e in evs]
-        kern_avg_ms = sum(kern_ms) / len(kern_ms)
-        conv_avg_ms = sum(conv_ms) / len(conv_ms)
+    total_ms, kern_avg_ms, conv_avg_ms, clocks, use_graph = timed_steps(
+        prep, args.steps, args.warmup, args.soak, dist, local, args.no_graph)
     total_ms, kern_avg_ms = max_over_ranks(dist, [total_ms, kern_avg_ms], dev)
     ms_per_step = total_ms / args.steps
     value = whole_job_tflops(world, flops, ms_per_step)
+    stream = torch.cuda.current_stream()
 
     # end to end through the public entry point with host buffers
     pin = lambda x: x.cpu().pin_memory()  # noqa: E731
@@ -468,12 +548,18 @@ def run_ours(args, world, rank, local):
     e2e_ms = max_over_ranks(dist, [e2e_ms], dev)[0]
     e2e_value = whole_job_tflops(world, flops, e2e_ms)
 
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    # the other workloads, timed after the benchmark line's own region (every
+    # rank takes part: their barriers and max over ranks are the same)
+    del prep, sets
+    others = None
+    if args.workload == "c2" and not args.no_workloads:
+        others = other_workloads(args, dev, dist, world, local, peak)
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return 0
-    peaks, peak_src = measured_peaks()
-    peak = float(peaks["bf16_tflops"])
     achieved = flops / (kern_avg_ms * 1e-3) / 1e12
     cfg = workload_desc(p, args.workload)
     cfg.update({"timing": ("CUDA graph of the K steps (captured before the timed region), "
@@ -483,11 +569,7 @@ def run_ours(args, world, rank, local):
                 "l2": f"{n_sets} rotating input/output sets of {per_set / 2**20:.0f} MiB "
                       f"(> 2 x 129 MiB L2), no flush",
                 "algorithmic_gflop_per_step": flops / 1e9})
-    if p.topk_idx is not None:
-        kernel = f"fa_mla_topk_kernel<{'bf16' if bf16 else 'fp16'}>"
-    else:
-        kernel = (f"fa_fwd_tiled_kernel<{p.D},{'bf16' if bf16 else 'fp16'},{4 if p.D == 128 else 6}"
-                  f"{',convert-V' if bf16 else ''}>")
+    kernel = kernel_name(p)
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak,
             "peak_source": f"{peak_src} bf16_tflops (burst); the fp16 products run at the same "
@@ -506,6 +588,8 @@ def run_ours(args, world, rank, local):
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": (2 if conv_pass else 1) * args.steps}
+    if others is not None:
+        line["workloads"] = others
     if world == 1 and not args.no_cpu_baseline and args.workload == "c2":
         f, t, n = oracle_timed(p, args.cpu_seconds)
         line["cpu_baseline"] = {
@@ -532,6 +616,12 @@ def main():
                     help="tokens of the top-k workload (c5); smaller values for profiling captures")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps eagerly with events around each launch")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the entries of the other workloads (c3, c4, c5) in the c2 line")
+    ap.add_argument("--workload-steps", type=int, default=100,
+                    help="timed steps of each other workload")
+    ap.add_argument("--workload-soak", type=float, default=1.0,
+                    help="seconds of untimed load before each other workload's timing")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c2",
                     help="c2 (default) is the benchmark line; the others time the same path "
                          "on the other workloads")

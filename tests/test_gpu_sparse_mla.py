@@ -45,6 +45,15 @@ def test_fp16_inputs():
     full_check(p)
 
 
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_rows_just_above_256_keys(dtype):
+    """Peaked rows of 256-300 keys: with fp16 P alone the fp16 case exceeded the
+    elementwise bound (1.16x at token 298), so every token below 512 keys takes
+    the hi + lo split."""
+    p = W.sparse_mla(name=f"mla_T300_{dtype}", T=300, W=320, seed=36, dtype=dtype)
+    full_check(p)
+
+
 @pytest.mark.parametrize("Hq", [64, 192])
 def test_partial_head_groups(Hq):
     p = W.sparse_mla(name=f"mla_H{Hq}", T=150, Hq=Hq, W=160, seed=43)
