@@ -119,7 +119,7 @@ def attention_fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
                     s = scale * (q[b, h, ri, :] @ k[b, kh].T)
                 else:
                     s = extras.scores(q[b, h, ri, :] @ k[b, kh].T, scale, b, h, ri, Hq, Sq, Skv)
-                    w = w * extras.visible(b, h, ri, Sq, Skv)
+                    w = w * extras.visible(b, h, ri, Sq, Skv, qlen, kvlen)
                 p, lse = _softmax_rows(s, w)
                 if extras is not None:
                     p = p * extras.keep(b, h, ri, Skv)
@@ -220,7 +220,9 @@ class Extras:
       2^(-8/n) (Sq == Skv only, as the doc requires).
     * sparse_mode 0: key j visible from query i when
       i - pre_tokens <= j <= i + next_tokens; 2: j <= i (top-left causal);
-      3: j <= i + Skv - Sq (bottom-right causal); None: no window.
+      3: j <= i + kv_len - q_len (bottom-right causal: the last query of a
+      sequence sees up to its last key, by the batch's actual lengths when
+      they are given, else Skv - Sq); None: no window.
     * drop_mask: 0/1 array broadcastable to [B, Hq, Sq, Skv] (1 = kept), with
       keep_prob in (0, 1]; philox_dropout_mask draws one as the write-up does.
     Masked scores take no part in the softmax (the write-up's golden fills
@@ -254,7 +256,12 @@ class Extras:
             return (qk + bias) * scale
         return qk * scale + bias
 
-    def visible(self, b, h, ri, Sq, Skv):
+    def visible(self, b, h, ri, Sq, Skv, qlen=None, kvlen=None):
+        """qlen / kvlen: the batch's actual lengths (default Sq, Skv); the
+        bottom-right causal mask aligns the last query of the sequence with
+        its last key, so it is offset by kvlen - qlen."""
+        qlen = Sq if qlen is None else min(qlen, Sq)
+        kvlen = Skv if kvlen is None else min(kvlen, Skv)
         i = ri[:, None]
         j = np.arange(Skv)[None, :]
         vis = np.ones((len(ri), Skv))
@@ -263,7 +270,7 @@ class Extras:
         elif self.sparse_mode == 2:
             vis *= j <= i
         elif self.sparse_mode == 3:
-            vis *= j <= i + (Skv - Sq)
+            vis *= j <= i + (kvlen - qlen)
         elif self.sparse_mode is not None:
             raise ValueError("sparse_mode must be None, 0, 2 or 3")
         if self.atten_mask is not None:

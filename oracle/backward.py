@@ -86,7 +86,7 @@ def attention_bwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, o: np.ndarray, ls
                 st = scale * s
             else:
                 st = extras.scores(s, scale, b, h, rows, Hq, Sq, Skv)
-                w = w * extras.visible(b, h, rows, Sq, Skv)
+                w = w * extras.visible(b, h, rows, Sq, Skv, qlen, kvlen)
                 keep = extras.keep(b, h, rows, Skv)
             lse_h = lse[b, h][:, None]
             live = np.isfinite(lse_h) & (w > 0)

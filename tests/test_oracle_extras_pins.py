@@ -60,6 +60,23 @@ def test_masks_and_windows():
                  A.attention_fwd(q, k, v, SCALE, extras=Extras(atten_mask=rd)))
 
 
+def test_bottom_right_causal_follows_each_batchs_lengths():
+    """With per-batch lengths the bottom-right mask aligns each sequence's
+    last query with its last key: batch b is the oracle on its own cropped
+    problem, whose mask is built element by element."""
+    q, k, v = _qkv(3, B=2, Sq=4, Skv=9)
+    seq = np.array([9, 3])       # a length applies to queries and keys, up to Sq and Skv
+    o, l = A.attention_fwd(q, k, v, SCALE, seqlens=seq, extras=Extras(sparse_mode=3))
+    for b, n in enumerate(seq):
+        ql, kl = min(n, 4), min(n, 9)
+        m = _mask_py(ql, kl, lambda i, j: j <= i + (kl - ql))   # offsets 5 and 0
+        oc, lc = A.attention_fwd(q[b:b + 1, :, :ql], k[b:b + 1, :, :kl], v[b:b + 1, :, :kl],
+                                 SCALE, extras=Extras(atten_mask=m))
+        assert np.allclose(o[b, :, :ql], oc[0], rtol=1e-12, atol=1e-14)
+        assert np.allclose(l[b, :, :ql], lc[0], rtol=1e-12, atol=1e-14)
+        assert np.all(np.isinf(l[b, :, ql:]))
+
+
 @pytest.mark.parametrize("pse_type, moved", [(0, 1.0), (1, SCALE)])
 def test_row_constant_bias(pse_type, moved):
     q, k, v = _qkv(3)
