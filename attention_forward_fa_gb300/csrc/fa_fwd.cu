@@ -416,8 +416,7 @@ int run_tiled(const void* q, const void* k, const void* v, void* o, void* o_lo, 
   std::memset(&prm, 0, sizeof(prm));
   if (!encode_3d(&prm.tm_q, q, fp16, D, Sq, (uint64_t)B * Hq, fa::kBM) ||
       !encode_3d(&prm.tm_k, k, fp16, D, Skv, (uint64_t)B * Hkv, fa::kBN) ||
-      !encode_3d(&prm.tm_v, v, /*fp16=*/!conv, Dv, Skv, (uint64_t)B * Hkv, fa::kBN) ||
-      !encode_3d(&prm.tm_o, o, fp16, Dv, Sq, (uint64_t)B * Hq, fa::kBM))
+      !encode_3d(&prm.tm_v, v, /*fp16=*/!conv, Dv, Skv, (uint64_t)B * Hkv, fa::kBN))
     return cuda_fail(cudaErrorInvalidValue);
   prm.o = o;
   prm.o_lo = o_lo;

@@ -56,14 +56,15 @@ constexpr int kMaxSplit = 8;      // most pieces a unit's KV tiles are split int
 // hardware named barriers (0 is __syncthreads): 1-2 scheduler -> issuer release
 // of groups 0 and 1, 3-4 issuer -> scheduler "group issued", 5-6 "P ready" of
 // slot t (its softmax warps and the scheduler -> issuer: P written and the
-// group's copies landed)
+// group's copies landed), 7-8 the epilogue of slot t (its softmax warps)
 constexpr int kBarPReady = 5;
+constexpr int kBarEpi = 7;
 constexpr int kPReadyCount = kBM + 64;   // slot's softmax threads, scheduler, issuer
 
 enum : int { kStatusTimeout = 1, kStatusRange = 2 };
 
 struct TiledParams {
-  CUtensorMap tm_q, tm_k, tm_v, tm_o;
+  CUtensorMap tm_q, tm_k, tm_v;
   void* o;
   void* o_lo;       // optional: o's rounding residual, same type and layout (or null)
   float* lse;
@@ -125,11 +126,10 @@ struct TiledSmem {
   static constexpr int kQOff = 0;
   static constexpr int kStageOff = 2 * kQBytes;
   static constexpr int kListOff = kStageOff + NS * kStageBytes;
-  static constexpr int kRowOff = kListOff + 2 * kMaxSel * 4;   // m[2][128], l[2][128]
-  static constexpr int kBarOff = kRowOff + 2 * 2 * kBM * 4;
-  // barriers: q_full[2], full[NS], empty[NS], s_full[2], p_full[2], o_ready[2],
-  // drain, sm_done[2], ready[NS] (a load passed the V converter)
-  static constexpr int kNumBars = 2 + 2 * NS + 6 + 1 + 2 + NS;
+  static constexpr int kBarOff = kListOff + 2 * kMaxSel * 4;
+  // barriers: q_full[2], full[NS], empty[NS], s_full[2], o_ready[2], drain,
+  // ready[NS] (a load passed the V converter)
+  static constexpr int kNumBars = 2 + 2 * NS + 4 + 1 + NS;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;   // tmem base, abort flag, slot info
   static constexpr int kBytes = kMiscOff + 64;
   static constexpr int kAlloc = kBytes + 1024;              // slack for 1024-byte alignment
@@ -196,6 +196,61 @@ __device__ __forceinline__ Piece piece_range(int n0, int n1, int piece, int kv_s
 }
 __device__ __forceinline__ int piece_count(int n, Piece pc) { return max(0, min(n, pc.hi) - pc.lo); }
 
+// Number of SMs of this GPU.
+__device__ __forceinline__ uint32_t sm_count() {
+  uint32_t n;
+  asm("mov.u32 %0, %%nsmid;" : "=r"(n));
+  return n;
+}
+
+// L2 prefetch of a unit's first tiles (its query tiles, the first two K and V
+// tiles of a dense unit), computed from the kernel's arguments alone.
+template <int D, bool kSplit>
+__device__ __noinline__ void prefetch_unit_l2(const TiledParams& p) {
+  constexpr int kBoxes = D / 64;
+  const int kv_split = kSplit ? p.kv_split : 1;
+  const int u = kSplit ? (int)blockIdx.x / kv_split : (int)blockIdx.x;
+  const int piece = blockIdx.x - u * kv_split;
+  const int qpos = p.n_qpos - 1 - u / p.units_per_q;
+  const int bh = u % p.units_per_q;
+  int b, h0, h1, qt0, qt1;
+  if (p.pair_mode == 0) {
+    b = bh / p.Hq;
+    h0 = h1 = bh % p.Hq;
+    qt0 = 2 * qpos;
+    qt1 = 2 * qpos + 1;
+  } else {
+    const int hpairs = p.Hq / 2;
+    b = bh / hpairs;
+    h0 = 2 * (bh % hpairs);
+    h1 = h0 + 1;
+    qt0 = qt1 = qpos;
+  }
+  tma_prefetch_desc(&p.tm_q);
+  tma_prefetch_desc(&p.tm_k);
+  tma_prefetch_desc(&p.tm_v);
+  for (int t = 0; t < 2; ++t) {
+    const int qt = t ? qt1 : qt0;
+    if (qt >= p.n_qt) continue;
+    for (int bx = 0; bx < kBoxes; ++bx)
+      tma_prefetch_l2_3d(&p.tm_q, 64 * bx, qt * kBM, b * p.Hq + (t ? h1 : h0));
+  }
+  if (p.blk_idx == nullptr) {
+    // the per-batch lengths are read only after the wait: a prefetched tile
+    // that turns out unused costs only bandwidth
+    const int f0 = dense_tiles(qt0, p.n_qt, p.Sq, p.Skv, p.mask);
+    const int f1 = dense_tiles(qt1, p.n_qt, p.Sq, p.Skv, p.mask);
+    const Piece pc = piece_range(f0, f1, piece, kv_split);
+    const int nf = min(2, pc.hi - pc.lo);
+    const int kvh = h0 / p.G;
+    for (int j = 0; j < nf; ++j)
+      for (int bx = 0; bx < kBoxes; ++bx) {
+        tma_prefetch_l2_3d(&p.tm_k, 64 * bx, (pc.lo + j) * kBN, b * p.Hkv + kvh);
+        tma_prefetch_l2_3d(&p.tm_v, 64 * bx, (pc.lo + j) * kBN, b * p.Hkv + kvh);
+      }
+  }
+}
+
 // The order in which the MMA warp consumes K / V tiles, as a numbered event
 // list: 0 = QK(0,0), 1 = QK(1,0), then per iteration j four events PV(0,j),
 // QK(0,j+1), PV(1,j), QK(1,j+1).  `load` marks the first use of a tile (a
@@ -251,20 +306,16 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   const uint32_t sQ = sbase + SM::kQOff;
   const uint32_t sStage = sbase + SM::kStageOff;
   int* s_list = reinterpret_cast<int*>(smem + SM::kListOff);
-  float* s_m = reinterpret_cast<float*>(smem + SM::kRowOff);   // [2][128]
-  float* s_l = s_m + 2 * kBM;                                   // [2][128]
   const uint32_t bar0 = sbase + SM::kBarOff;
   auto BAR_QFULL = [=](int t) { return bar0 + 8u * t; };
   auto BAR_FULL = [=](int s) { return bar0 + 8u * (2 + s); };
   auto BAR_EMPTY = [=](int s) { return bar0 + 8u * (2 + NS + s); };
   auto BAR_SFULL = [=](int t) { return bar0 + 8u * (2 + 2 * NS + t); };
-  auto BAR_PFULL = [=](int t) { return bar0 + 8u * (4 + 2 * NS + t); };
-  auto BAR_OREADY = [=](int t) { return bar0 + 8u * (6 + 2 * NS + t); };
-  const uint32_t BAR_DRAIN = bar0 + 8u * (8 + 2 * NS);
-  auto BAR_SMDONE = [=](int t) { return bar0 + 8u * (9 + 2 * NS + t); };
+  auto BAR_OREADY = [=](int t) { return bar0 + 8u * (4 + 2 * NS + t); };
+  const uint32_t BAR_DRAIN = bar0 + 8u * (6 + 2 * NS);
   // with kConvV every ring load passes the converter (V tiles converted, K
   // tiles untouched) and the MMA side waits here instead of on BAR_FULL
-  auto BAR_READY = [=](int s) { return kConvV ? bar0 + 8u * (11 + 2 * NS + s) : bar0 + 8u * (2 + s); };
+  auto BAR_READY = [=](int s) { return kConvV ? bar0 + 8u * (7 + 2 * NS + s) : bar0 + 8u * (2 + s); };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + SM::kMiscOff);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + SM::kMiscOff + 4);
   int* s_slot = reinterpret_cast<int*>(smem + SM::kMiscOff + 8);   // [2] n, [2] hilo
@@ -273,6 +324,13 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   // has started (its CTAs then wait here for this grid to finish); nothing
   // below touches global memory before the previous kernel has completed.
   pdl_launch_dependents();
+  // While the previous kernel on the stream may still run, one thread warms L2
+  // with the first tiles of this CTA's unit (a prefetch only reads into the
+  // cache, which stays coherent with that kernel's later writes): the first
+  // wave of CTAs is scheduled during the previous kernel's tail, and its first
+  // loads then come from L2 instead of every CTA reading HBM at once.  Later
+  // CTAs start after that kernel has finished and load at once instead.
+  if (threadIdx.x == 32 * 15 && blockIdx.x < sm_count()) prefetch_unit_l2<D, kSplit>(p);
   pdl_wait_prior();
 
   const int tid = threadIdx.x;
@@ -318,8 +376,6 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(BAR_QFULL(t), 1);
       mbar_init(BAR_SFULL(t), 1);
-      mbar_init(BAR_SMDONE(t), kBM);     // softmax threads, once, after their last tile
-      mbar_init(BAR_PFULL(t), kBM);      // softmax threads, per tile
       mbar_init(BAR_OREADY(t), 1);
     }
     for (int s = 0; s < NS; ++s) {
@@ -406,6 +462,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     if (lane == 0) {
       s_slot[t] = n;
       s_slot[2 + t] = hilo;
+      s_slot[5 + t] = b * p.Hq + (t ? h1 : h0);   // the slot's output plane (for its epilogue)
     }
   }
   __syncthreads();
@@ -588,12 +645,137 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       // P_t (and the rescaled O_t) ready: hardware barrier to the MMA issuer
       named_arrive(kBarPReady + t, kPReadyCount);
     }
-    // final row statistics for the epilogue warpgroup
-    s_m[t * kBM + row] = m;
-    s_l[t * kBM + row] = l;
-    mbar_arrive(BAR_SMDONE(t));
+    // ---- epilogue of slot t, by its own threads (m and l are in registers):
+    // O / l and the LSE.  O_t is complete once the slot's last P.V has
+    // finished; the slot's Q buffer (its last reader, Q.K^T, finished before
+    // that P.V) stages the output tile, which the slot's threads then copy to
+    // memory row by row (each warp store covers 512 contiguous bytes).  Plain
+    // stores let the CTA retire without waiting for them to drain.
+    if (qt < p.n_qt) {
+      bool skip = false;
+      if (nt > 0) {
+        const bool ok = !dead && __all_sync(0xffffffffu, wait_bar(BAR_OREADY(t), 0, wc));
+        // one decision for the slot's four warps, so that none waits at the
+        // staging barrier below for a warp that gave up
+        skip = named_or(kBarEpi + t, kBM, !ok);
+        if (!skip) tc_fence_after();
+      }
+      if (!skip) {
+        // the slot's (batch, head) plane, re-read here rather than held in a
+        // register across the tile loop
+        int plane;
+        asm volatile("ld.shared.b32 %0, [%1];"
+                     : "=r"(plane)
+                     : "r"(((smem_u32(smem_raw) + 1023u) & ~1023u) + SM::kMiscOff + 8 + 4 * (5 + t)));
+        const bool write = qi < p.Sq;
+        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        const uint32_t tO = tmem + 256u + 128u * t + lane_off;
+        const uint32_t stage = ((smem_u32(smem_raw) + 1023u) & ~1023u) + SM::kQOff + t * SM::kQBytes;
+        const size_t rows_all = (size_t)p.B * p.Hq * p.Sq;
+        const size_t rr = (size_t)plane * p.Sq + (write ? qi : 0);
+        // this CTA's piece of a split unit (recomputed: nothing held across the loop)
+        const int my_piece = kSplit ? (int)(blockIdx.x % (unsigned)p.kv_split) : 0;
+        // O in halves of 64 columns: TMEM -> registers, O / l, out
+#pragma unroll 1
+        for (int hh = 0; hh < Dv / 64; ++hh) {
+          uint32_t r[64];
+          if (nt > 0) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc)   // warp-collective: all lanes, even rows past Sq
+              tmem_ld32(tO + 64 * hh + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * cc]));
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) r[i] = 0;
+          }
+          const uint64_t il2 = f2_pack(inv_l, inv_l);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float x0, x1;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), il2), x0, x1);
+            r[2 * i] = __float_as_uint(x0);
+            r[2 * i + 1] = __float_as_uint(x1);
+          }
+          if (kSplit) {
+            // one piece of a split unit: its O / l in fp32 for the merge kernel
+            float4* dst = reinterpret_cast<float4*>(p.part_o + ((size_t)my_piece * rows_all + rr) * Dv + 64 * hh);
+            if (write) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                     __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+            }
+          } else {
+            // O / l rounded to o's type, staged in the slot's Q buffer: row-major,
+            // 16-byte chunk c of row i at i * 2 Dv + ((c ^ i) & 15) * 16 (the XOR
+            // spreads the 32 rows of one warp store over the banks)
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {   // 16-byte chunks of eight outputs
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float a0 = __uint_as_float(r[8 * c8 + 2 * e]);
+                const float a1 = __uint_as_float(r[8 * c8 + 2 * e + 1]);
+                w[e] = kBF16 ? pack_bf16x2(a0, a1) : pack_f16x2(a0, a1);
+              }
+              const int c = 8 * hh + c8;
+              st_shared_v4(stage + row * (2 * Dv) + (((c ^ row) & (Dv / 8 - 1)) << 4),
+                           make_uint4(w[0], w[1], w[2], w[3]));
+            }
+            if (p.o_lo && write) {
+              // o's rounding residual (only when asked for), straight to memory
+              uint4* dst_lo = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o_lo) + (rr * Dv + 64 * hh) * 2);
+#pragma unroll
+              for (int c8 = 0; c8 < 8; ++c8) {
+                uint32_t wl[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float a0 = __uint_as_float(r[8 * c8 + 2 * e]);
+                  const float a1 = __uint_as_float(r[8 * c8 + 2 * e + 1]);
+                  wl[e] = pack_residual_x2(a0, a1, kBF16 ? pack_bf16x2(a0, a1) : pack_f16x2(a0, a1), kBF16);
+                }
+                dst_lo[c8] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+              }
+            }
+          }
+        }
+        if (kSplit) {
+          if (write)
+            p.part_lse[(size_t)my_piece * rows_all + rr] = (l > 0.f) ? __fmaf_rn(m, p.scale, __logf(l)) : -INFINITY;
+        } else {
+          if (write)
+            p.lse[rr] = (l > 0.f) ? __fmaf_rn(m, p.scale, __logf(l)) : INFINITY;
+          named_sync(kBarEpi + t, kBM);   // the slot's four warps staged their rows
+          // copy-out: the slot's 128 threads walk the tile in 16-byte chunks,
+          // consecutive threads on consecutive chunks of a row
+          constexpr int kChunks = Dv / 8;                // per row
+          constexpr int kRowsPerPass = kBM * 16 / (2 * Dv);
+          const int c = row % kChunks;
+          const int i0 = row / kChunks;
+          const int rows_left = p.Sq - q0;               // rows past Sq are not written
+          uint8_t* out = static_cast<uint8_t*>(p.o) + ((size_t)plane * p.Sq + q0) * (2 * Dv) + c * 16;
+#pragma unroll
+          for (int k = 0; k < kBM / kRowsPerPass; k += 4) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int i = i0 + (k + u) * kRowsPerPass;
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(v[u].x), "=r"(v[u].y), "=r"(v[u].z), "=r"(v[u].w)
+                           : "r"(stage + i * (2 * Dv) + (((c ^ i) & (kChunks - 1)) << 4)));
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int i = i0 + (k + u) * kRowsPerPass;
+              if (i < rows_left) *reinterpret_cast<uint4*>(out + (size_t)i * (2 * Dv)) = v[u];
+            }
+          }
+        }
+        if (row == 0) FA_TR(11, t, 0);
+      }
+    }
   } else if (warp < 12) {
-    // ============================================================ V converter, then epilogue
+    // ============================================================ V converter
     regs_dec<kCorrRegs>();
     FA_TR_ROLE(2);
     if constexpr (kConvV) {
@@ -632,131 +814,6 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       }
       if ((vmax & 0xFFFFu) > 0x477Fu || (vmax >> 16) > 0x477Fu) atomicOr(p.status, kStatusRange);
     }
-    const int row = (warp & 3) * 32 + lane;
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-#pragma unroll 1
-    for (int t = 0; t < 2; ++t) {
-      const int qt = t ? qt1 : qt0;
-      if (qt >= p.n_qt) continue;
-      const int nt = t ? n1 : n0;
-      const int h = t ? h1 : h0;
-      const int qi = qt * kBM + row;
-      bool acc = false;
-      if (nt > 0) {
-        acc = __all_sync(0xffffffffu, wait_bar(BAR_SMDONE(t), 0, wc)) &&
-              __all_sync(0xffffffffu, wait_bar(BAR_OREADY(t), 0, wc));   // the last P.V
-        // one decision for the four epilogue warps (each reaches this barrier
-        // once per slot), so that none waits at the staging barrier below for
-        // a warp that gave up
-        if (named_or(7, kBM, !acc)) break;
-        tc_fence_after();
-      }
-      if (row == 0) FA_TR(10, t, 0);
-      const float l = acc ? s_l[t * kBM + row] : 0.f;
-      const float m = acc ? s_m[t * kBM + row] : 0.f;
-      const bool write = qi < p.Sq;
-      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-      const uint32_t tO = tmem + 256u + 128u * t + lane_off;
-      if (kSplit) {
-        // one piece of a split unit: its O / l in fp32 and its LSE (-inf when
-        // the piece saw no key of the row) for the merge kernel
-        const size_t rows_all = (size_t)p.B * p.Hq * p.Sq;
-        const size_t r = (size_t)(b * p.Hq + h) * p.Sq + (write ? qi : 0);
-        float4* dst = reinterpret_cast<float4*>(p.part_o + ((size_t)piece * rows_all + r) * Dv);
-#pragma unroll 2
-        for (int cc = 0; cc < Dv / 16; ++cc) {
-          uint32_t rr[16];
-          if (acc) {
-            tmem_ld16(tO + 16 * cc, rr);   // warp-collective: all lanes, even rows past Sq
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) rr[i] = 0;
-          }
-          if (write) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[4 * cc + i] = make_float4(
-                  __uint_as_float(rr[4 * i]) * inv_l, __uint_as_float(rr[4 * i + 1]) * inv_l,
-                  __uint_as_float(rr[4 * i + 2]) * inv_l, __uint_as_float(rr[4 * i + 3]) * inv_l);
-          }
-        }
-        if (write)
-          p.part_lse[(size_t)piece * rows_all + r] = (l > 0.f) ? __fmaf_rn(m, p.scale, __logf(l)) : -INFINITY;
-        if (row == 0) FA_TR(11, t, 0);
-        continue;
-      }
-      // O / l into the slot's Q buffer (its last Q.K^T finished before the last
-      // P.V) in the 128-byte-swizzle layout of the output's tensor map, then one
-      // thread stores the tile with TMA (rows past Sq are clipped)
-      uint8_t* stage_o = smem + SM::kQOff + t * SM::kQBytes + row * 128;
-      const int sw = row & 7;
-#pragma unroll 2
-      for (int cc = 0; cc < Dv / 16; ++cc) {
-        uint32_t r[16];
-        if (acc) {
-          tmem_ld16(tO + 16 * cc, r);   // warp-collective: all lanes, even rows past Sq
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) r[i] = 0;
-        }
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float a0 = __uint_as_float(r[8 * i + 2 * e]) * inv_l;
-            const float a1 = __uint_as_float(r[8 * i + 2 * e + 1]) * inv_l;
-            w[e] = kBF16 ? pack_bf16x2(a0, a1) : pack_f16x2(a0, a1);
-          }
-          const int chunk = (cc & 3) * 2 + i;   // 16-byte chunk within the 64-column box
-          *reinterpret_cast<uint4*>(stage_o + (cc >> 2) * (kBM * 128) + ((chunk ^ sw) << 4)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      }
-      if (p.o_lo) {
-        // o's rounding residual (only when asked for): a second pass over O_t,
-        // so that the epilogue above keeps its register budget
-        uint4* dst_lo = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o_lo) +
-                                                 ((size_t)(b * p.Hq + h) * p.Sq + (write ? qi : 0)) * (Dv * 2));
-#pragma unroll 1
-        for (int cc = 0; cc < Dv / 16; ++cc) {
-          uint32_t r[16];
-          if (acc) {
-            tmem_ld16(tO + 16 * cc, r);   // warp-collective: all lanes, even rows past Sq
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) r[i] = 0;
-          }
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            uint32_t wl[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float a0 = __uint_as_float(r[8 * i + 2 * e]) * inv_l;
-              const float a1 = __uint_as_float(r[8 * i + 2 * e + 1]) * inv_l;
-              wl[e] = pack_residual_x2(a0, a1, kBF16 ? pack_bf16x2(a0, a1) : pack_f16x2(a0, a1), kBF16);
-            }
-            if (write) dst_lo[2 * cc + i] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-          }
-        }
-      }
-      fence_proxy_async_smem();
-      named_sync(7, kBM);   // the four epilogue warps
-      if (warp == 8 && lane == 0) {
-        for (int bx = 0; bx < kBoxes; ++bx)
-          tma_store_3d(&p.tm_o, sQ + t * SM::kQBytes + bx * (kBM * 128), 64 * bx, qt * kBM,
-                       b * p.Hq + h);
-        bulk_commit();
-      }
-      if (write)
-        p.lse[(size_t)(b * p.Hq + h) * p.Sq + qi] = (l > 0.f) ? __fmaf_rn(m, p.scale, __logf(l)) : INFINITY;
-      if (row == 0) FA_TR(11, t, 0);
-    }
-    // the tiles' shared memory must outlive the stores' reads
-    if (warp == 8 && lane == 0) bulk_wait_read();
   } else if (warp == 12) {
     // ============================================================ producer
     regs_dec<kOtherRegs>();

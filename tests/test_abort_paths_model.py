@@ -26,9 +26,9 @@ happen, and counts that.
 
 The roles' programs are written down from the kernels' loops:
 attention_forward_fa_gb300/csrc/fa_tiled.cuh (the dense forward: TMA producer,
-V converter + epilogue, MMA scheduler, MMA issuer, the softmax warps of two
-query tiles) and csrc/fa_bwd.cuh (the backward's dK/dV kernel: producer, MMA
-issuer, four elementwise warps).  Planted mistakes show that each property is
+V converter, MMA scheduler, MMA issuer, the softmax warps of two query
+tiles, which also write their tile's epilogue) and csrc/fa_bwd.cuh (the
+backward's dK/dV kernel: producer, MMA issuer, four elementwise warps).  Planted mistakes show that each property is
 seen.  Host-side model: it reads no file and runs no kernel.
 """
 import pytest
@@ -314,6 +314,8 @@ def forward_handoff_roles(n0, n1, NS=2, planted=None):
         if jpv >= 0 and not pv_valid:
             continue
         iss["main"].append(("nbsync", 1 + t) if jpv < 0 else ("nbsync", PREADY + t))
+        if pv_valid and jpv == ntt - 1:
+            iss["main"].append(("commit", f"oready{t}"))   # the slot's last P.V
         if qk_valid:
             iss["main"].append(("commit", f"sfull{t}"))
         iss["main"].append(("nbarrive", 3 + t))
@@ -322,8 +324,12 @@ def forward_handoff_roles(n0, n1, NS=2, planted=None):
     iss["main"].append(("syncall",))
 
     def softmax(t):
-        pr = {"main": []}
-        tail = [("arrive", f"smdone{t}"), ("syncall",)]
+        # after its last tile the slot's warps write its epilogue once its
+        # last P.V has completed (a bounded wait; on a give-up the slot's
+        # warps agree to skip the writes); the warps of one slot move as one
+        # agent here, so their own staging barrier is not modelled
+        pr = {"main": [], "epi_skip": [("syncall",)]}
+        tail = ([("bwait", f"oready{t}", 0, "epi_skip")] if nt[t] > 0 else []) + [("syncall",)]
         for j in range(nt[t]):
             alt = f"dead{j}"
             dead = []
@@ -336,23 +342,22 @@ def forward_handoff_roles(n0, n1, NS=2, planted=None):
                 if paced:
                     dead.append(("drain", f"sfull{t}", j2))
                 dead.append(("nbarrive", PREADY + t))
-            pr[alt] = dead + tail
+            pr[alt] = dead + [("syncall",)]   # a warp that gave up skips the epilogue
             pr["main"] += [("bwait", f"sfull{t}", j, alt), ("nbarrive", PREADY + t)]
         pr["main"] += tail
         return pr
 
     roles = [("scheduler", 1, sched), ("issuer", 1, iss), ("softmax0", 4, softmax(0)),
              ("softmax1", 4, softmax(1))]
-    mcounts = {"sfull0": 1, "sfull1": 1, "smdone0": 1, "smdone1": 1, "drain": 1}
+    mcounts = {"sfull0": 1, "sfull1": 1, "oready0": 1, "oready1": 1, "drain": 1}
     return roles, mcounts, {1: 2, 2: 2, 3: 2, 4: 2, 5: 6, 6: 6}
 
 
 def forward_ring_roles(n0, n1, NS=2, planted=None):
     """Model B: the ring of fa_tiled.cuh and the teardown.  The TMA producer,
-    the V converter with the epilogue (its waits for the softmax and the last
-    P.V are events outside this model), and the MMA side as one consumer: the
-    scheduler's waits for each group's copies, then the issuer's commits that
-    release the group's stages."""
+    the V converter, and the MMA side as one consumer: the scheduler's waits
+    for each group's copies, then the issuer's commits that release the
+    group's stages."""
     nt, nmax, shared, loads, groups = _forward_plan(n0, n1, NS)
 
     def drains(issued):
@@ -373,16 +378,12 @@ def forward_ring_roles(n0, n1, NS=2, planted=None):
         prod["main"] += drains(len(loads))
     prod["main"].append(("syncall",))
 
-    epi = []
-    for t in range(2):
-        if nt[t] > 0:
-            epi += [("ext_wait", "epi_gaveup"), ("ext_wait", "epi_gaveup")]   # smdone, oready
-    conv = {"main": [], "epi_gaveup": [("syncall",)]}
+    conv = {"main": []}
     for L, s, f in loads:
         alt = f"dead{L}"
-        conv[alt] = [("arrive", f"ready{s2}") for _, s2, _ in loads[L:]] + epi + [("syncall",)]
+        conv[alt] = [("arrive", f"ready{s2}") for _, s2, _ in loads[L:]] + [("syncall",)]
         conv["main"] += [("bwait", f"full{s}", f, alt), ("arrive", f"ready{s}")]
-    conv["main"] += epi + [("syncall",)]
+    conv["main"] += [("syncall",)]
 
     cons_ops = []
     for g, t, jpv, jqk, ntt, pv_valid, qk_valid, pv_load, qk_load, lpv, lqk in groups:
