@@ -34,6 +34,13 @@ class fa_topk_t(ctypes.Structure):
     _fields_ = [("idx", ctypes.c_void_p), ("topk", ctypes.c_int32), ("stride_b", ctypes.c_int64)]
 
 
+class fa_extras_t(ctypes.Structure):
+    _fields_ = [("window", ctypes.c_int32), ("pre_tokens", ctypes.c_int32),
+                ("next_tokens", ctypes.c_int32), ("alibi", ctypes.c_int32),
+                ("atten_mask", ctypes.c_void_p), ("mask_stride_b", ctypes.c_int64),
+                ("mask_stride_h", ctypes.c_int64), ("mask_stride_q", ctypes.c_int64)]
+
+
 _lib = None
 
 
@@ -55,6 +62,10 @@ def library() -> ctypes.CDLL:
             ctypes.POINTER(fa_topk_t), ctypes.c_float, ctypes.c_void_p]
         lib.fa_fwd_noalloc.restype = ctypes.c_int
         lib.fa_fwd_noalloc.argtypes = lib.fa_fwd.argtypes
+        lib.fa_fwd_ext.restype = ctypes.c_int
+        lib.fa_fwd_ext.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 7 + [
+            ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(fa_extras_t),
+            ctypes.c_float, ctypes.c_void_p]
         lib.fa_fwd_o_lo.restype = ctypes.c_int
         lib.fa_fwd_o_lo.argtypes = lib.fa_fwd.argtypes[:4] + [ctypes.c_void_p] + lib.fa_fwd.argtypes[4:]
         lib.fa_bwd.restype = ctypes.c_int
@@ -149,6 +160,17 @@ def fa_bwd(q, k, v, o, o_lo, lse, dout, dq, dk, dv, B: int, Hq: int, Hkv: int, S
                             int(mask_mode), _ptr(seqlens), _stream(stream))
 
 
+def fa_fwd_ext(q, k, v, o, lse, B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int, Dv: int,
+               scale: float, mask_mode: int, seqlens, extras, rescale_threshold: float = 0.0,
+               stream=None) -> int:
+    """Direct call of fa_fwd_ext (see include/fa_fwd.h).  extras: an
+    fa_extras_t (or None, which the library rejects).  Returns the FA_* code."""
+    return library().fa_fwd_ext(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv,
+                                D, Dv, float(scale), int(mask_mode), _ptr(seqlens),
+                                ctypes.byref(extras) if extras is not None else None,
+                                float(rescale_threshold), _stream(stream))
+
+
 def fa_fwd_noalloc(q, k, v, o, lse, B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int,
                    Dv: int, scale: float, mask_mode: int, seqlens=None, kv_block_idx=None,
                    topk_idx=None, rescale_threshold: float = 0.0, stream=None) -> int:
@@ -203,14 +225,21 @@ def _raise(code: int):
 def flash_attention_forward(q, k, v=None, *, scale: Optional[float] = None, causal: bool = False,
                             mask_mode: Optional[int] = None, seqlens=None, block_idx=None,
                             topk_idx=None, rescale_threshold: float = 0.0, out=None, lse=None,
-                            o_lo=None, stream=None):
+                            o_lo=None, window=None, bottom_right_causal: bool = False,
+                            atten_mask=None, alibi: bool = False, stream=None):
     """Allocating convenience wrapper over fa_fwd.
 
     q [B,Hq,Sq,D], k [B,Hkv,Skv,D], v [B,Hkv,Skv,Dv] (or None with top-k and a
     shared latent), bf16 or fp16 CUDA tensors.  block_idx: int32 tensor
     [B, Hq or 1, ceil(Sq/128), max_sel]; topk_idx: int32 [B, Sq, W].
     o_lo: True (allocate) or a tensor like out to also receive the output's
-    rounding residual (fa_fwd_o_lo).  Returns (o, lse), or (o, lse, o_lo)."""
+    rounding residual (fa_fwd_o_lo).  Returns (o, lse), or (o, lse, o_lo).
+
+    The operator's optional terms go through fa_fwd_ext: window=(pre_tokens,
+    next_tokens) (sparse_mode 0), bottom_right_causal (sparse_mode 3),
+    atten_mask (bool or uint8 CUDA tensor [..., Sq, Skv] broadcastable to
+    [B, Hq, Sq, Skv], True / nonzero = masked; its last dimension contiguous),
+    alibi (pse_type 2)."""
     import torch
     if q.dtype not in (torch.bfloat16, torch.float16):
         raise TypeError("q, k, v must be bf16 or fp16")
@@ -244,6 +273,34 @@ def flash_attention_forward(q, k, v=None, *, scale: Optional[float] = None, caus
         tk = (topk_idx, topk_idx.shape[-1], topk_idx.shape[-2] * topk_idx.shape[-1])
     if seqlens is not None:
         assert seqlens.dtype == torch.int32 and seqlens.is_cuda
+    if window is not None or bottom_right_causal or atten_mask is not None or alibi:
+        if o_lo not in (None, False) or bs is not None or tk is not None:
+            raise ValueError("the optional terms apply to dense problems without o_lo")
+        ex = fa_extras_t()
+        ex.window = 1 if window is not None else (2 if bottom_right_causal else 0)
+        if window is not None and bottom_right_causal:
+            raise ValueError("window and bottom_right_causal are exclusive")
+        ex.pre_tokens, ex.next_tokens = (int(window[0]), int(window[1])) if window is not None else (0, 0)
+        ex.alibi = 1 if alibi else 0
+        keep = None
+        if atten_mask is not None:
+            m = atten_mask
+            if m.dtype == torch.bool:
+                m = m.view(torch.uint8)
+            if m.dtype != torch.uint8 or not m.is_cuda or m.stride(-1) != 1:
+                raise ValueError("atten_mask must be a bool / uint8 CUDA tensor with a contiguous last dim")
+            while m.dim() < 4:
+                m = m.unsqueeze(0)
+            def st(d):
+                return 0 if m.shape[d] == 1 else m.stride(d)
+            ex.atten_mask = m.data_ptr()
+            ex.mask_stride_b, ex.mask_stride_h, ex.mask_stride_q = st(0), st(1), st(2)
+            keep = m
+        code = fa_fwd_ext(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
+                          ex, rescale_threshold, stream)
+        del keep
+        _raise(code)
+        return out, lse
     if o_lo is None or o_lo is False:
         code = fa_fwd(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens, bs,
                       tk, rescale_threshold, stream)

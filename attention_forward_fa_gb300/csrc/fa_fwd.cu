@@ -259,9 +259,9 @@ cudaError_t launch_dependent(void (*kern)(Params...), unsigned grid, unsigned bl
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-template <int D, bool BF16, int NS, bool CONV, bool SPLIT>
+template <int D, bool BF16, int NS, bool CONV, bool SPLIT, bool EXTRAS = false>
 int launch_tiled(const fa::TiledParams& prm, int units, cudaStream_t st) {
-  auto kern = fa::fa_fwd_tiled_kernel<D, BF16, NS, CONV, SPLIT>;
+  auto kern = fa::fa_fwd_tiled_kernel<D, BF16, NS, CONV, SPLIT, EXTRAS>;
   constexpr int smem = fa::TiledSmem<D, NS>::kAlloc;
   static std::once_flag once[64];
   int dev = 0;
@@ -284,18 +284,19 @@ int launch_tiled(const fa::TiledParams& prm, int units, cudaStream_t st) {
   return FA_OK;
 }
 
-// The dense kernel for (head dim, input type, V conversion), split or not.
-template <bool SPLIT>
+// The dense kernel for (head dim, input type, V conversion), split or not,
+// with the optional terms or not.
+template <bool SPLIT, bool EXTRAS = false>
 int launch_tiled_variant(const fa::TiledParams& prm, int grid, cudaStream_t st, int D, bool fp16,
                          bool conv) {
   if (D == 128) {
-    if (fp16) return launch_tiled<128, false, 4, false, SPLIT>(prm, grid, st);
-    return conv ? launch_tiled<128, true, 4, true, SPLIT>(prm, grid, st)
-                : launch_tiled<128, true, 4, false, SPLIT>(prm, grid, st);
+    if (fp16) return launch_tiled<128, false, 4, false, SPLIT, EXTRAS>(prm, grid, st);
+    return conv ? launch_tiled<128, true, 4, true, SPLIT, EXTRAS>(prm, grid, st)
+                : launch_tiled<128, true, 4, false, SPLIT, EXTRAS>(prm, grid, st);
   }
-  if (fp16) return launch_tiled<64, false, 6, false, SPLIT>(prm, grid, st);
-  return conv ? launch_tiled<64, true, 6, true, SPLIT>(prm, grid, st)
-              : launch_tiled<64, true, 6, false, SPLIT>(prm, grid, st);
+  if (fp16) return launch_tiled<64, false, 6, false, SPLIT, EXTRAS>(prm, grid, st);
+  return conv ? launch_tiled<64, true, 6, true, SPLIT, EXTRAS>(prm, grid, st)
+              : launch_tiled<64, true, 6, false, SPLIT, EXTRAS>(prm, grid, st);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -408,7 +409,8 @@ int run_topk(const void* q, const void* k16, void* o, void* o_lo, float* lse, in
 int run_tiled(const void* q, const void* k, const void* v, void* o, void* o_lo, float* lse, int B,
               int Hq, int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
               const int32_t* seqlens, const fa_block_sparse_t* kv_block_idx,
-              float rescale_threshold, int* status, cudaStream_t st, bool may_alloc) {
+              float rescale_threshold, int* status, cudaStream_t st, bool may_alloc,
+              const fa_extras_t* ex = nullptr) {
   const int mask = mask_mode & 0xF;
   const bool fp16 = (mask_mode & FA_DTYPE_FP16) != 0;
   const bool conv = !fp16 && !(mask_mode & FA_V_FP16);   // V arrives as bf16
@@ -457,6 +459,19 @@ int run_tiled(const void* q, const void* k, const void* v, void* o, void* o_lo, 
 #ifdef FA_TRACE
   prm.trace = g_trace;
 #endif
+  if (ex) {
+    // window bounds beyond +-(Sq + Skv) cannot change a row's key range
+    const long long lim = (long long)Sq + Skv;
+    auto clampw = [lim](int32_t v) { return (int)std::max(-lim, std::min(lim, (long long)v)); };
+    prm.win_mode = ex->window;
+    prm.pre_tokens = clampw(ex->pre_tokens);
+    prm.next_tokens = clampw(ex->next_tokens);
+    prm.amask = ex->atten_mask;
+    prm.am_sb = ex->mask_stride_b;
+    prm.am_sh = ex->mask_stride_h;
+    prm.am_sq = ex->mask_stride_q;
+    prm.alibi = ex->alibi;
+  }
   const long long units = (long long)prm.units_per_q * prm.n_qpos;
   if (units > 0x7FFFFFFF) return FA_ERR_SHAPE;
 
@@ -467,7 +482,7 @@ int run_tiled(const void* q, const void* k, const void* v, void* o, void* o_lo, 
   prm.kv_split = 1;
   const int sms = sm_count();
   const int n_kb = (Skv + fa::kBN - 1) / fa::kBN;
-  if (!kv_block_idx && sms > 0 && units * 2 <= sms) {
+  if (!kv_block_idx && !ex && sms > 0 && units * 2 <= sms) {
     int ks = std::min(g_max_kv_split.load(), (int)((sms + units - 1) / units));
     ks = std::min(ks, n_kb / 2);
     if (ks >= 2) prm.kv_split = ks;
@@ -492,8 +507,9 @@ int run_tiled(const void* q, const void* k, const void* v, void* o, void* o_lo, 
     }
   }
   const int grid = (int)std::min<long long>(units * prm.kv_split, 0x7FFFFFFF);
-  int rc = prm.kv_split > 1 ? launch_tiled_variant<true>(prm, grid, st, D, fp16, conv)
-                             : launch_tiled_variant<false>(prm, grid, st, D, fp16, conv);
+  int rc = ex ? launch_tiled_variant<false, true>(prm, grid, st, D, fp16, conv)
+           : prm.kv_split > 1 ? launch_tiled_variant<true>(prm, grid, st, D, fp16, conv)
+                              : launch_tiled_variant<false>(prm, grid, st, D, fp16, conv);
   if (rc == FA_OK && prm.kv_split > 1) {
     const unsigned blocks = (unsigned)((rows_all + 7) / 8);
     const cudaError_t e =
@@ -697,6 +713,32 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            const fa_topk_t* topk_idx, float rescale_threshold, void* stream) {
   return fwd_impl(q, k, v, o, nullptr, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
                   kv_block_idx, topk_idx, rescale_threshold, stream);
+}
+
+int fa_fwd_ext(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+               int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
+               const int32_t* seqlens, const fa_extras_t* extras, float rescale_threshold,
+               void* stream) {
+  if (!extras) return FA_ERR_NULL;
+  const int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
+                          nullptr, nullptr, rescale_threshold);
+  if (rc != FA_OK) return rc;
+  if ((mask_mode & FA_V_FROM_K) || (mask_mode & 0xF) > FA_MASK_CAUSAL) return FA_ERR_SHAPE;
+  if (extras->window < 0 || extras->window > 2 || extras->alibi < 0 || extras->alibi > 1)
+    return FA_ERR_SHAPE;
+  if ((Skv + fa::kBN - 1) / fa::kBN > fa::kMaxSel) return FA_ERR_SHAPE;
+  if (extras->atten_mask) {
+    if (extras->mask_stride_b < 0 || extras->mask_stride_h < 0 || extras->mask_stride_q < 0)
+      return FA_ERR_SHAPE;
+    if (!aligned(extras->atten_mask, 16) || extras->mask_stride_q % 16 ||
+        extras->mask_stride_h % 16 || extras->mask_stride_b % 16 || Skv % 16)
+      return FA_ERR_ALIGN;
+  }
+  int* status = status_ptr();
+  if (!status) return cuda_fail(cudaGetLastError());
+  return run_tiled(q, k, v, o, nullptr, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
+                   nullptr, rescale_threshold, status, reinterpret_cast<cudaStream_t>(stream),
+                   /*may_alloc=*/false, extras);
 }
 
 int fa_fwd_o_lo(const void* q, const void* k, const void* v, void* o, void* o_lo, float* lse,

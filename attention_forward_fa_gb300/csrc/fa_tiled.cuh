@@ -86,6 +86,13 @@ struct TiledParams {
   long long timeout_ns;
   int* status;
   unsigned long long* trace;   // cycle-stamped events of the first CTAs (trace builds only)
+  // The operator doc's optional terms (kExtras launches only):
+  int win_mode;                // 0: none; 1: keys i - pre_tokens <= j <= i + next_tokens;
+                               // 2: bottom-right causal, j <= i + kv_len - q_len
+  int pre_tokens, next_tokens; // win_mode 1 (clamped by the host to +-(Sq + Skv))
+  const uint8_t* amask;        // explicit mask or null: nonzero byte = key masked
+  long long am_sb, am_sh, am_sq;   // its strides (elements) over batch, head, query row
+  int alibi;                   // 1: score bias -slope_h |i - j|, slope_h = 2^(-8 (h + 1) / Hq)
 };
 
 // Trace points: compiled only with -DFA_TRACE (a profiling build); otherwise
@@ -235,9 +242,10 @@ __device__ __noinline__ void prefetch_unit_l2(const TiledParams& p) {
     for (int bx = 0; bx < kBoxes; ++bx)
       tma_prefetch_l2_3d(&p.tm_q, 64 * bx, qt * kBM, b * p.Hq + (t ? h1 : h0));
   }
-  if (p.blk_idx == nullptr) {
-    // the per-batch lengths are read only after the wait: a prefetched tile
-    // that turns out unused costs only bandwidth
+  if (p.blk_idx == nullptr && p.win_mode != 1) {
+    // (a key window starts elsewhere) the per-batch lengths are read only
+    // after the wait: a prefetched tile that turns out unused costs only
+    // bandwidth
     const int f0 = dense_tiles(qt0, p.n_qt, p.Sq, p.Skv, p.mask);
     const int f1 = dense_tiles(qt1, p.n_qt, p.Sq, p.Skv, p.mask);
     const Piece pc = piece_range(f0, f1, piece, kv_split);
@@ -249,6 +257,21 @@ __device__ __noinline__ void prefetch_unit_l2(const TiledParams& p) {
         tma_prefetch_l2_3d(&p.tm_v, 64 * bx, (pc.lo + j) * kBN, b * p.Hkv + kvh);
       }
   }
+}
+
+// Keys visible from query row i under the optional terms, before the explicit
+// mask: [ext_key_lo(i), ext_key_hi(i)] (empty when hi < lo; hi = -1 for a row
+// past the batch's length).
+__device__ __forceinline__ int ext_key_lo(const TiledParams& p, int i) {
+  return p.win_mode == 1 ? max(0, i - p.pre_tokens) : 0;
+}
+__device__ __forceinline__ int ext_key_hi(const TiledParams& p, int i, int q_len, int kv_len) {
+  if (i >= q_len) return -1;
+  int hi = kv_len - 1;
+  if (p.mask == 1) hi = min(hi, i);                       // top-left causal
+  if (p.win_mode == 1) hi = min(hi, i + p.next_tokens);
+  if (p.win_mode == 2) hi = min(hi, i + kv_len - q_len);  // bottom-right causal
+  return hi;
 }
 
 // The order in which the MMA warp consumes K / V tiles, as a numbered event
@@ -289,7 +312,10 @@ __device__ __forceinline__ Event event_at(int e, int n0, int n1, bool shared) {
 // kSplit: the launch cuts units into KV pieces (p.kv_split > 1); an unsplit
 // launch compiles without the piece bookkeeping, which costs ~1-2 % of the
 // loop's time even when every unit is one piece.
-template <int D, bool kBF16, int NS, bool kConvV, bool kSplit>
+// kExtras: the operator doc's optional terms (p.win_mode, p.amask, p.alibi);
+// each slot walks its own list of KV tiles (its window), scores are scaled to
+// log2 units before the mask and the row max.
+template <int D, bool kBF16, int NS, bool kConvV, bool kSplit, bool kExtras = false>
 __global__ void __launch_bounds__(kTiledThreads, 1)
     fa_fwd_tiled_kernel(const __grid_constant__ TiledParams p) {
   using SM = TiledSmem<D, NS>;
@@ -361,6 +387,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   const int kv_len = p.seqlens ? min(p.seqlens[b], p.Skv) : p.Skv;
   const int nkb = (p.Skv + kBN - 1) / kBN;
   const bool sparse = p.blk_idx != nullptr;
+  // slots that walk a list of KV tiles (block lists, or the extras' windows)
+  const bool listed = sparse || kExtras;
 
   // ---------------------------------------------------------------- setup
   {
@@ -390,7 +418,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
     s_slot[4] = 0;   // first KV tile of the piece
-    if (!sparse) {
+    if (!listed) {
       const int f0 = dense_tiles(qt0, p.n_qt, q_len, kv_len, p.mask);
       const int f1 = dense_tiles(qt1, p.n_qt, q_len, kv_len, p.mask);
       const Piece pc = piece_range(f0, f1, piece, kv_split);
@@ -427,13 +455,30 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     const int q0 = qt * kBM;
     int n = 0, hilo = 0;
     const bool live = qt < p.n_qt && q0 < q_len && kv_len > 0;
-    if (live && !sparse) {
+    if (live && !listed) {
       // this slot's tiles of the piece (both slots' counts fix the cuts)
       const int f0 = dense_tiles(qt0, p.n_qt, q_len, kv_len, p.mask);
       const int f1 = dense_tiles(qt1, p.n_qt, q_len, kv_len, p.mask);
       n = piece_count(t ? f1 : f0, piece_range(f0, f1, piece, kv_split));
       const int min_keys = (p.mask == 1) ? min(q0 + 1, kv_len) : kv_len;
       hilo = min_keys < kHiLoKeys;
+    } else if (live && kExtras) {
+      // the rows' key ranges grow with the row: tiles from the first row's
+      // lowest key to the last row's highest
+      const int qa = q0, qb = min(q0 + kBM, q_len) - 1;
+      const int lo_a = ext_key_lo(p, qa), hi_b = ext_key_hi(p, qb, q_len, kv_len);
+      const int t_lo = lo_a / kBN, t_hi = min(nkb, hi_b >= 0 ? hi_b / kBN + 1 : 0);
+      n = max(0, t_hi - t_lo);
+      for (int e = lane; e < n; e += 32) s_list[t * kMaxSel + e] = t_lo + e;
+      // the fewest keys of a row (the count is concave in the row, so at an
+      // end).  The cut is twice the plain kernel's: a window gives every row
+      // of a tile about the same short length, and with the lazy threshold a
+      // 300-key band reached 1.13x the elementwise bound on fp16 P alone.
+      // Any row may be short under an explicit mask, and the ALiBi decay
+      // leaves few keys that matter (head 0 of 8 at 512 keys: 1.67x)
+      const int ka = ext_key_hi(p, qa, q_len, kv_len) - lo_a + 1;
+      const int kb = hi_b - ext_key_lo(p, qb) + 1;
+      hilo = p.amask != nullptr || p.alibi || min(ka, kb) < 2 * kHiLoKeys;
     } else if (live && sparse) {
       const int* lst = p.blk_idx + (long long)b * p.blk_stride_b +
                        (long long)(t ? h1 : h0) * p.blk_stride_h + (long long)qt * p.max_sel;
@@ -470,7 +515,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
   const uint32_t tmem = *s_tmem;
   const int n0 = s_slot[0], n1 = s_slot[1];
   const int kv_lo = s_slot[4];   // first KV tile of the piece (dense)
-  const bool shared_kv = !sparse ? (n0 >= 1 && n0 <= n1) : false;
+  const bool shared_kv = !listed ? (n0 >= 1 && n0 <= n1) : false;
   const WaitCtx wc{s_abort, p.status, p.timeout_ns};
 
   if (warp < 8) {
@@ -487,11 +532,37 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     const bool row_valid = qi < q_len;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + 128u * t + lane_off;
-    const float c = p.scale_log2;
+    // scores enter the exponential as s * c - m * c; the extras path scales
+    // them to log2 units first (c = 1 there, and m is in log2 units)
+    const float c = kExtras ? 1.f : p.scale_log2;
     const uint64_t c2 = f2_pack(c, c);
+    // extras: the row's key range, its mask row and the ALiBi slope (log2 units)
+    int ek_lo = 0, ek_hi = 0;
+    const uint8_t* mrow = nullptr;
+    float slope2 = 0.f;
+    if constexpr (kExtras) {
+      ek_lo = ext_key_lo(p, qi);
+      ek_hi = ext_key_hi(p, qi, q_len, kv_len);
+      const int h = t ? h1 : h0;
+      if (p.amask)
+        mrow = p.amask + b * p.am_sb + h * p.am_sh + (long long)min(qi, p.Sq - 1) * p.am_sq;
+      if (p.alibi) slope2 = -exp2f(-8.f * (float)(h + 1) / (float)p.Hq) * 1.4426950408889634f;
+    }
     float m = -INFINITY, l = 0.f;
     bool dead = false;   // a bounded wait expired: keep the hand-offs, skip the work
     for (int j = 0; j < nt; ++j) {
+      // extras: this tile's bytes of the explicit mask, loaded before the S
+      // wait (128 keys per row, 16 bytes per load; keys past Skv read none)
+      uint4 mbytes[kBN / 16];
+      if constexpr (kExtras) {
+        if (mrow) {
+          const int kb0 = s_list[t * kMaxSel + j] * kBN;
+#pragma unroll
+          for (int q = 0; q < kBN / 16; ++q)
+            mbytes[q] = kb0 + 16 * q < p.Skv ? __ldg(reinterpret_cast<const uint4*>(mrow + kb0 + 16 * q))
+                                         : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
       if (!dead && !__all_sync(0xffffffffu, wait_bar(BAR_SFULL(t), j & 1, wc))) dead = true;
       if (dead) {
         // The MMA issuer waits for one arrival per tile on a hardware barrier.
@@ -514,7 +585,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       int kv_first = 0;
       if (kSplit)
         asm volatile("ld.shared.b32 %0, [%1];" : "=r"(kv_first) : "r"(smem_u32(s_slot + 4)));
-      const int kvt = sparse ? s_list[t * kMaxSel + j] : kv_first + j;
+      const int kvt = listed ? s_list[t * kMaxSel + j] : kv_first + j;
       const int kbase = kvt * kBN;
       const bool causal_here = (p.mask == 1) || (p.mask == 2 && kvt == qt);
       const bool need_mask =
@@ -530,7 +601,39 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       float sv[kBN];
 #pragma unroll
       for (int i = 0; i < kBN; ++i) sv[i] = __uint_as_float(su[i]);
-      if (__any_sync(0xffffffffu, need_mask)) {
+      if constexpr (kExtras) {
+        // scores in log2 units, s * scale * log2(e), plus the ALiBi bias
+        // -slope_h |i - j| log2(e) (exact integer distances in fp32)
+        const float dq = (float)(qi - kbase);
+        if (p.alibi) {
+#pragma unroll
+          for (int i = 0; i < kBN; ++i) sv[i] = fmaf(sv[i], p.scale_log2, slope2 * fabsf(dq - (float)i));
+        } else {
+#pragma unroll
+          for (int i = 0; i < kBN; ++i) sv[i] *= p.scale_log2;
+        }
+        // the mask bytes as bits (a nonzero byte masks its key)
+        uint32_t mbits[kBN / 32] = {0u, 0u, 0u, 0u};
+        if (mrow) {
+#pragma unroll
+          for (int q = 0; q < kBN / 16; ++q) {
+            const uint32_t w4[4] = {mbytes[q].x, mbytes[q].y, mbytes[q].z, mbytes[q].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t nz = __vcmpne4(w4[e], 0u) & 0x01010101u;   // 1 per nonzero byte
+              mbits[q >> 1] |= ((nz * 0x01020408u) >> 24) << (16 * (q & 1) + 4 * e);
+            }
+          }
+        }
+        // keys outside [ek_lo, ek_hi] or masked
+        const int lo = ek_lo - kbase, hi = ek_hi - kbase;
+        const bool any = lo > 0 || hi < kBN - 1 || (mrow && (mbits[0] | mbits[1] | mbits[2] | mbits[3]));
+        if (__any_sync(0xffffffffu, any)) {
+#pragma unroll
+          for (int i = 0; i < kBN; ++i)
+            if (i < lo || i > hi || ((mbits[i >> 5] >> (i & 31)) & 1u)) sv[i] = -INFINITY;
+        }
+      } else if (__any_sync(0xffffffffu, need_mask)) {
         // Warp-uniform decisions per 32-column chunk: chunks below every row's
         // limit stay, chunks above every limit are cleared, and only a chunk
         // that straddles the warp's limits (the diagonal block of a causal
@@ -744,7 +847,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
             p.part_lse[(size_t)my_piece * rows_all + rr] = (l > 0.f) ? __fmaf_rn(m, p.scale, __logf(l)) : -INFINITY;
         } else {
           if (write)
-            p.lse[rr] = (l > 0.f) ? __fmaf_rn(m, p.scale, __logf(l)) : INFINITY;
+            p.lse[rr] = (l > 0.f) ? __fmaf_rn(m, kExtras ? 0.6931471805599453f : p.scale, __logf(l))
+                                  : INFINITY;
           named_sync(kBarEpi + t, kBM);   // the slot's four warps staged their rows
           // copy-out: the slot's 128 threads walk the tile in 16-byte chunks,
           // consecutive threads on consecutive chunks of a row
@@ -844,7 +948,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           --ld;   // not issued: ld counts the loads in flight or landed
           break;
         }
-        const int kvt = sparse ? s_list[ev.t * kMaxSel + ev.j] : kv_lo + ev.j;
+        const int kvt = listed ? s_list[ev.t * kMaxSel + ev.j] : kv_lo + ev.j;
         FA_TR(5, ev.t, ev.j);
         mbar_arrive_expect_tx(BAR_FULL(s), SM::kStageBytes);
         const CUtensorMap* tm = ev.pv ? &p.tm_v : &p.tm_k;

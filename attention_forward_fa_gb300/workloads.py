@@ -140,6 +140,13 @@ def dense(name="dense", B=1, Hq=2, Hkv=None, Sq=128, Skv=None, D=64, Dv=None,
                    seed=seed)
 
 
+def upstream_grad(shape, dtype="bf16", seed=2001) -> np.ndarray:
+    """Seeded upstream gradient dO of a backward call: i.i.d. N(0,1) fp32
+    draws rounded to the input type (the bits)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return to_bits(_draw(rng, tuple(shape)), dtype)
+
+
 def block_sparse(name="block_sparse", B=1, H=16, S=16384, D=128, dtype="fp16",
                  n_random=15, pad_slots=1, mask=MASK_CAUSAL_DIAG_BLOCK, seed=1004,
                  per_head=True) -> Problem:

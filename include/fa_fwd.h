@@ -162,6 +162,59 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            const fa_block_sparse_t* kv_block_idx, const fa_topk_t* topk_idx,
            float rescale_threshold, void* stream);
 
+/* ---- optional terms of the operator ------------------------------------ */
+/*
+ * The "FlashAttentionScore" operator doc (gitcode ops-transformer), sections
+ * "Function description" (forward formula: s = scale * Q K^T + pse, masked,
+ * softmax, times V) and "Parameter description" (atten_mask, pse_type,
+ * sparse_mode, pre_tokens / next_tokens):
+ *
+ *   window       0: no window.
+ *                1: sparse_mode 0, key j visible from query i when
+ *                   i - pre_tokens <= j <= i + next_tokens (a band);
+ *                2: sparse_mode 3, bottom-right causal: j <= i + kv_len - q_len,
+ *                   so the last query of a sequence sees up to its last key
+ *                   (kv_len, q_len: the batch's actual lengths when seqlens
+ *                   is given, else Skv, Sq).
+ *                Top-left causal (sparse_mode 2) is FA_MASK_CAUSAL in
+ *                mask_mode; it may be combined with a window (both apply).
+ *   pre_tokens, next_tokens   window 1 only (any int; values beyond +-(Sq + Skv)
+ *                act as unbounded).
+ *   atten_mask   NULL, or DEVICE uint8 with element (b, h, i, j) at
+ *                atten_mask[b*mask_stride_b + h*mask_stride_h + i*mask_stride_q + j];
+ *                a nonzero byte masks key j for query i.  Strides in
+ *                elements, >= 0 (0 broadcasts over batch or head); the base,
+ *                mask_stride_q, mask_stride_h and mask_stride_b must be
+ *                multiples of 16 bytes and Skv a multiple of 16 (16-byte loads).
+ *   alibi        0: none; 1: pse_type 2, the position bias -slope_h * |i - j|
+ *                added after the scale, slope_h = 2^(-8 (h + 1) / Hq).
+ *
+ * A row whose keys are all masked gets O = 0 and LSE = +inf, as in fa_fwd.
+ */
+typedef struct {
+  int32_t window;
+  int32_t pre_tokens;
+  int32_t next_tokens;
+  int32_t alibi;
+  const uint8_t* atten_mask;
+  int64_t mask_stride_b;
+  int64_t mask_stride_h;
+  int64_t mask_stride_q;
+} fa_extras_t;
+
+/* fa_fwd with the optional terms above (`extras` is a host pointer, required).
+ * Dense / causal / ragged / GQA problems only (no block-sparse or top-k
+ * descriptors), D = Dv in {64, 128}, ceil(Skv / 128) <= 512; mask_mode
+ * FA_MASK_NONE or FA_MASK_CAUSAL plus the dtype flags.  Every other argument
+ * and output as fa_fwd.  Errors: FA_ERR_NULL (extras NULL), FA_ERR_SHAPE
+ * (window or alibi out of range, negative stride, Skv too long),
+ * FA_ERR_ALIGN (mask layout), FA_ERR_UNSUPPORTED (D, Dv), and those of
+ * fa_fwd.  Allocates nothing. */
+int fa_fwd_ext(const void* q, const void* k, const void* v, void* o, float* lse,
+               int B, int Hq, int Hkv, int Sq, int Skv, int D, int Dv, float scale,
+               int mask_mode, const int32_t* seqlens, const fa_extras_t* extras,
+               float rescale_threshold, void* stream);
+
 /* fa_fwd that also writes the output's rounding residual
  *   o_lo = fp32(O) - O rounded to o's type,
  * itself rounded to that type, same layout as o (rows past Sq / padded heads

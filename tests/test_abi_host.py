@@ -182,3 +182,33 @@ def test_noalloc_rejects_a_latent_beyond_its_scratch_before_any_cuda_call(lib):
                               stream=0)
     assert code16 != -9
 
+
+
+def call_ext(lib, ex, **kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=P, B=1, Hq=2, Hkv=2, Sq=128, Skv=128, D=128, Dv=128,
+             scale=0.1, mask_mode=0, seqlens=None, rescale_threshold=0.0, stream=0)
+    a.update(kw)
+    return B.fa_fwd_ext(extras=ex, **a)
+
+
+def _ex(**kw):
+    e = B.fa_extras_t()
+    for k, v in kw.items():
+        setattr(e, k, v)
+    return e
+
+
+@pytest.mark.parametrize("ex,kw,code", [
+    (None, {}, -1),
+    (_ex(window=3), {}, -2), (_ex(window=-1), {}, -2), (_ex(alibi=2), {}, -2),
+    (_ex(), dict(mask_mode=2), -2), (_ex(), dict(mask_mode=0x200, v=None), -3),
+    (_ex(), dict(Skv=128 * 513), -2),
+    (_ex(atten_mask=P, mask_stride_q=-16), {}, -2),
+    (_ex(atten_mask=P + 8, mask_stride_q=128), {}, -4),
+    (_ex(atten_mask=P, mask_stride_q=120), {}, -4),
+    (_ex(atten_mask=P, mask_stride_q=128, mask_stride_h=8), {}, -4),
+    (_ex(atten_mask=P, mask_stride_q=120), dict(Skv=120), -4),
+    (_ex(), dict(D=576, Dv=512), -3), (_ex(), dict(q=P + 8), -4), (_ex(), dict(B=0), -2),
+])
+def test_ext_argument_errors(lib, ex, kw, code):
+    assert call_ext(lib, ex, **kw) == code
