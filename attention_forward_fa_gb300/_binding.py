@@ -38,7 +38,10 @@ class fa_extras_t(ctypes.Structure):
     _fields_ = [("window", ctypes.c_int32), ("pre_tokens", ctypes.c_int32),
                 ("next_tokens", ctypes.c_int32), ("alibi", ctypes.c_int32),
                 ("atten_mask", ctypes.c_void_p), ("mask_stride_b", ctypes.c_int64),
-                ("mask_stride_h", ctypes.c_int64), ("mask_stride_q", ctypes.c_int64)]
+                ("mask_stride_h", ctypes.c_int64), ("mask_stride_q", ctypes.c_int64),
+                ("pse", ctypes.c_void_p), ("pse_stride_b", ctypes.c_int64),
+                ("pse_stride_h", ctypes.c_int64), ("pse_stride_q", ctypes.c_int64),
+                ("pse_type", ctypes.c_int32)]
 
 
 _lib = None
@@ -226,7 +229,8 @@ def flash_attention_forward(q, k, v=None, *, scale: Optional[float] = None, caus
                             mask_mode: Optional[int] = None, seqlens=None, block_idx=None,
                             topk_idx=None, rescale_threshold: float = 0.0, out=None, lse=None,
                             o_lo=None, window=None, bottom_right_causal: bool = False,
-                            atten_mask=None, alibi: bool = False, stream=None):
+                            atten_mask=None, alibi: bool = False, pse=None, pse_type: int = 0,
+                            stream=None):
     """Allocating convenience wrapper over fa_fwd.
 
     q [B,Hq,Sq,D], k [B,Hkv,Skv,D], v [B,Hkv,Skv,Dv] (or None with top-k and a
@@ -239,7 +243,9 @@ def flash_attention_forward(q, k, v=None, *, scale: Optional[float] = None, caus
     next_tokens) (sparse_mode 0), bottom_right_causal (sparse_mode 3),
     atten_mask (bool or uint8 CUDA tensor [..., Sq, Skv] broadcastable to
     [B, Hq, Sq, Skv], True / nonzero = masked; its last dimension contiguous),
-    alibi (pse_type 2)."""
+    alibi (pse_type 2), pse (a bias tensor of q's type [..., Sq, Skv]
+    broadcastable like atten_mask, last dim contiguous) with pse_type 0
+    (added after the scale) or 1 (before)."""
     import torch
     if q.dtype not in (torch.bfloat16, torch.float16):
         raise TypeError("q, k, v must be bf16 or fp16")
@@ -273,7 +279,7 @@ def flash_attention_forward(q, k, v=None, *, scale: Optional[float] = None, caus
         tk = (topk_idx, topk_idx.shape[-1], topk_idx.shape[-2] * topk_idx.shape[-1])
     if seqlens is not None:
         assert seqlens.dtype == torch.int32 and seqlens.is_cuda
-    if window is not None or bottom_right_causal or atten_mask is not None or alibi:
+    if window is not None or bottom_right_causal or atten_mask is not None or alibi or pse is not None:
         if o_lo not in (None, False) or bs is not None or tk is not None:
             raise ValueError("the optional terms apply to dense problems without o_lo")
         ex = fa_extras_t()
@@ -296,9 +302,22 @@ def flash_attention_forward(q, k, v=None, *, scale: Optional[float] = None, caus
             ex.atten_mask = m.data_ptr()
             ex.mask_stride_b, ex.mask_stride_h, ex.mask_stride_q = st(0), st(1), st(2)
             keep = m
+        keep_pse = None
+        if pse is not None:
+            b_ = pse
+            if b_.dtype != q.dtype or not b_.is_cuda or b_.stride(-1) != 1:
+                raise ValueError("pse must be a CUDA tensor of q's dtype with a contiguous last dim")
+            while b_.dim() < 4:
+                b_ = b_.unsqueeze(0)
+            def stp(d):
+                return 0 if b_.shape[d] == 1 else b_.stride(d)
+            ex.pse = b_.data_ptr()
+            ex.pse_stride_b, ex.pse_stride_h, ex.pse_stride_q = stp(0), stp(1), stp(2)
+            ex.pse_type = int(pse_type)
+            keep_pse = b_
         code = fa_fwd_ext(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
                           ex, rescale_threshold, stream)
-        del keep
+        del keep, keep_pse
         _raise(code)
         return out, lse
     if o_lo is None or o_lo is False:

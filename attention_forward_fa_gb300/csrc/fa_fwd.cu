@@ -471,6 +471,11 @@ int run_tiled(const void* q, const void* k, const void* v, void* o, void* o_lo, 
     prm.am_sh = ex->mask_stride_h;
     prm.am_sq = ex->mask_stride_q;
     prm.alibi = ex->alibi;
+    prm.pse = static_cast<const uint16_t*>(ex->pse);
+    prm.pse_sb = ex->pse_stride_b;
+    prm.pse_sh = ex->pse_stride_h;
+    prm.pse_sq = ex->pse_stride_q;
+    prm.pse_type = ex->pse_type;
   }
   const long long units = (long long)prm.units_per_q * prm.n_qpos;
   if (units > 0x7FFFFFFF) return FA_ERR_SHAPE;
@@ -727,6 +732,14 @@ int fa_fwd_ext(const void* q, const void* k, const void* v, void* o, float* lse,
   if (extras->window < 0 || extras->window > 2 || extras->alibi < 0 || extras->alibi > 1)
     return FA_ERR_SHAPE;
   if ((Skv + fa::kBN - 1) / fa::kBN > fa::kMaxSel) return FA_ERR_SHAPE;
+  if (extras->pse) {
+    if (extras->alibi || extras->pse_type < 0 || extras->pse_type > 1) return FA_ERR_SHAPE;
+    if (extras->pse_stride_b < 0 || extras->pse_stride_h < 0 || extras->pse_stride_q < 0)
+      return FA_ERR_SHAPE;
+    if (!aligned(extras->pse, 16) || extras->pse_stride_q % 8 || extras->pse_stride_h % 8 ||
+        extras->pse_stride_b % 8 || Skv % 8)
+      return FA_ERR_ALIGN;
+  }
   if (extras->atten_mask) {
     if (extras->mask_stride_b < 0 || extras->mask_stride_h < 0 || extras->mask_stride_q < 0)
       return FA_ERR_SHAPE;

@@ -93,6 +93,9 @@ struct TiledParams {
   const uint8_t* amask;        // explicit mask or null: nonzero byte = key masked
   long long am_sb, am_sh, am_sq;   // its strides (elements) over batch, head, query row
   int alibi;                   // 1: score bias -slope_h |i - j|, slope_h = 2^(-8 (h + 1) / Hq)
+  const uint16_t* pse;         // bias tensor or null: q's type, strides below (elements)
+  long long pse_sb, pse_sh, pse_sq;
+  int pse_type;                // 0: s * scale + pse; 1: (s + pse) * scale
 };
 
 // Trace points: compiled only with -DFA_TRACE (a profiling build); otherwise
@@ -475,10 +478,11 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       // of a tile about the same short length, and with the lazy threshold a
       // 300-key band reached 1.13x the elementwise bound on fp16 P alone.
       // Any row may be short under an explicit mask, and the ALiBi decay
-      // leaves few keys that matter (head 0 of 8 at 512 keys: 1.67x)
+      // leaves few keys that matter (head 0 of 8 at 512 keys: 1.67x); an
+      // arbitrary bias tensor may peak any row as well
       const int ka = ext_key_hi(p, qa, q_len, kv_len) - lo_a + 1;
       const int kb = hi_b - ext_key_lo(p, qb) + 1;
-      hilo = p.amask != nullptr || p.alibi || min(ka, kb) < 2 * kHiLoKeys;
+      hilo = p.amask != nullptr || p.alibi || p.pse != nullptr || min(ka, kb) < 2 * kHiLoKeys;
     } else if (live && sparse) {
       const int* lst = p.blk_idx + (long long)b * p.blk_stride_b +
                        (long long)(t ? h1 : h0) * p.blk_stride_h + (long long)qt * p.max_sel;
@@ -539,6 +543,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     // extras: the row's key range, its mask row and the ALiBi slope (log2 units)
     int ek_lo = 0, ek_hi = 0;
     const uint8_t* mrow = nullptr;
+    const uint16_t* prow = nullptr;
     float slope2 = 0.f;
     if constexpr (kExtras) {
       ek_lo = ext_key_lo(p, qi);
@@ -546,6 +551,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       const int h = t ? h1 : h0;
       if (p.amask)
         mrow = p.amask + b * p.am_sb + h * p.am_sh + (long long)min(qi, p.Sq - 1) * p.am_sq;
+      if (p.pse)
+        prow = p.pse + b * p.pse_sb + h * p.pse_sh + (long long)min(qi, p.Sq - 1) * p.pse_sq;
       if (p.alibi) slope2 = -exp2f(-8.f * (float)(h + 1) / (float)p.Hq) * 1.4426950408889634f;
     }
     float m = -INFINITY, l = 0.f;
@@ -561,6 +568,14 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           for (int q = 0; q < kBN / 16; ++q)
             mbytes[q] = kb0 + 16 * q < p.Skv ? __ldg(reinterpret_cast<const uint4*>(mrow + kb0 + 16 * q))
                                          : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (prow) {
+          // the bias row of this tile into L2 (read chunk by chunk below)
+          const int kb0 = s_list[t * kMaxSel + j] * kBN;
+#pragma unroll
+          for (int q = 0; q < kBN / 64; ++q)
+            if (kb0 + 64 * q < p.Skv)
+              asm volatile("prefetch.global.L2 [%0];" ::"l"(prow + kb0 + 64 * q));
         }
       }
       if (!dead && !__all_sync(0xffffffffu, wait_bar(BAR_SFULL(t), j & 1, wc))) dead = true;
@@ -608,6 +623,36 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         if (p.alibi) {
 #pragma unroll
           for (int i = 0; i < kBN; ++i) sv[i] = fmaf(sv[i], p.scale_log2, slope2 * fabsf(dq - (float)i));
+        } else if (prow) {
+          // the bias tensor, 32 keys (four 16-byte loads) at a time; keys
+          // past Skv read none (they are masked below)
+          constexpr float kL2e = 1.4426950408889634f;
+#pragma unroll
+          for (int cc = 0; cc < kBN / 32; ++cc) {
+            uint4 w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int col = kbase + 32 * cc + 8 * u;
+              w[u] = col < p.Skv ? __ldg(reinterpret_cast<const uint4*>(prow + col)) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t w4[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float b0 = kBF16 ? __uint_as_float(w4[e] << 16) : f16_lo_to_f32(w4[e]);
+                const float b1 = kBF16 ? __uint_as_float(w4[e] & 0xFFFF0000u) : f16_hi_to_f32(w4[e]);
+                const int i = 32 * cc + 8 * u + 2 * e;
+                if (p.pse_type == 1) {
+                  sv[i] = (sv[i] + b0) * p.scale_log2;
+                  sv[i + 1] = (sv[i + 1] + b1) * p.scale_log2;
+                } else {
+                  sv[i] = fmaf(sv[i], p.scale_log2, b0 * kL2e);
+                  sv[i + 1] = fmaf(sv[i + 1], p.scale_log2, b1 * kL2e);
+                }
+              }
+            }
+          }
         } else {
 #pragma unroll
           for (int i = 0; i < kBN; ++i) sv[i] *= p.scale_log2;

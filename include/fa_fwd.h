@@ -188,6 +188,14 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *                multiples of 16 bytes and Skv a multiple of 16 (16-byte loads).
  *   alibi        0: none; 1: pse_type 2, the position bias -slope_h * |i - j|
  *                added after the scale, slope_h = 2^(-8 (h + 1) / Hq).
+ *   pse          NULL, or DEVICE bias of q's type (bf16, or fp16 with
+ *                FA_DTYPE_FP16), element (b, h, i, j) at
+ *                pse[b*pse_stride_b + h*pse_stride_h + i*pse_stride_q + j];
+ *                strides in elements, >= 0 (0 broadcasts), multiples of 8,
+ *                the base 16-byte aligned and Skv a multiple of 8.
+ *   pse_type     with pse: 0 adds it after the scale (s = scale Q K^T + pse),
+ *                1 before (s = scale (Q K^T + pse)).  pse and alibi are
+ *                exclusive (the doc's pse_type picks one).
  *
  * A row whose keys are all masked gets O = 0 and LSE = +inf, as in fa_fwd.
  */
@@ -200,6 +208,11 @@ typedef struct {
   int64_t mask_stride_b;
   int64_t mask_stride_h;
   int64_t mask_stride_q;
+  const void* pse;
+  int64_t pse_stride_b;
+  int64_t pse_stride_h;
+  int64_t pse_stride_q;
+  int32_t pse_type;
 } fa_extras_t;
 
 /* fa_fwd with the optional terms above (`extras` is a host pointer, required).
@@ -207,8 +220,8 @@ typedef struct {
  * descriptors), D = Dv in {64, 128}, ceil(Skv / 128) <= 512; mask_mode
  * FA_MASK_NONE or FA_MASK_CAUSAL plus the dtype flags.  Every other argument
  * and output as fa_fwd.  Errors: FA_ERR_NULL (extras NULL), FA_ERR_SHAPE
- * (window or alibi out of range, negative stride, Skv too long),
- * FA_ERR_ALIGN (mask layout), FA_ERR_UNSUPPORTED (D, Dv), and those of
+ * (window, alibi or pse_type out of range, pse with alibi, negative stride,
+ * Skv too long), FA_ERR_ALIGN (mask or pse layout), FA_ERR_UNSUPPORTED (D, Dv), and those of
  * fa_fwd.  Allocates nothing. */
 int fa_fwd_ext(const void* q, const void* k, const void* v, void* o, float* lse,
                int B, int Hq, int Hkv, int Sq, int Skv, int D, int Dv, float scale,

@@ -209,6 +209,9 @@ def _ex(**kw):
     (_ex(atten_mask=P, mask_stride_q=128, mask_stride_h=8), {}, -4),
     (_ex(atten_mask=P, mask_stride_q=120), dict(Skv=120), -4),
     (_ex(), dict(D=576, Dv=512), -3), (_ex(), dict(q=P + 8), -4), (_ex(), dict(B=0), -2),
+    (_ex(pse=P, alibi=1), {}, -2), (_ex(pse=P, pse_type=2), {}, -2),
+    (_ex(pse=P, pse_stride_q=-8), {}, -2), (_ex(pse=P + 8, pse_stride_q=128), {}, -4),
+    (_ex(pse=P, pse_stride_q=124), {}, -4), (_ex(pse=P, pse_stride_q=128), dict(Skv=124), -4),
 ])
 def test_ext_argument_errors(lib, ex, kw, code):
     assert call_ext(lib, ex, **kw) == code

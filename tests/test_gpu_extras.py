@@ -1,7 +1,8 @@
 """GPU parity of the operator's optional terms (fa_fwd_ext) against the fp64
 oracle's Extras: the key window of sparse_mode 0 (pre_tokens / next_tokens),
-the bottom-right causal mask of sparse_mode 3, an explicit attention mask and
-the ALiBi position bias of pse_type 2 ("FlashAttentionScore" operator doc,
+the bottom-right causal mask of sparse_mode 3, an explicit attention mask, the
+ALiBi position bias of pse_type 2 and a pse bias tensor added after (pse_type
+0) or before (pse_type 1) the scale ("FlashAttentionScore" operator doc,
 gitcode ops-transformer, sections "Function description" and "Parameter
 description").  Tolerances as every forward parity test: elementwise
 |dO| <= 1e-4 + 7.8125e-3 |ref|, rel-L2 <= 3e-3, |dLSE| <= 2e-3, +inf rows
@@ -27,20 +28,35 @@ def _mask_bits(shape, frac, seed, full_rows=()):
     return m
 
 
-def _run(p, causal=False, window=None, bottom_right=False, mask=None, alibi=False, thr=0.0):
+def _bias(shape, dtype, seed, sigma=2.0):
+    """Seeded bias tensor: N(0, sigma^2) rounded to the input type; returns
+    (bits, float64 values)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    bits = W.to_bits((sigma * rng.standard_normal(shape)).astype(np.float32), dtype)
+    return bits, W.bits_to_f64(bits, dtype)
+
+
+def _run(p, causal=False, window=None, bottom_right=False, mask=None, alibi=False, thr=0.0,
+         pse=None, pse_type=0):
     import torch
     import attention_forward_fa_gb300 as fa
     d = to_device(p)
     am = torch.from_numpy(mask).cuda() if mask is not None else None
+    pse_t = None
+    if pse is not None:
+        tdt = torch.bfloat16 if p.dtype == "bf16" else torch.float16
+        pse_t = torch.from_numpy(pse[0].view(np.int16).copy()).cuda().view(tdt)
     o, lse = fa.flash_attention_forward(d["q"], d["k"], d["v"], scale=p.scale, causal=causal,
                                         seqlens=d["seqlens"], window=window,
                                         bottom_right_causal=bottom_right, atten_mask=am,
-                                        alibi=alibi, rescale_threshold=thr)
+                                        alibi=alibi, pse=pse_t, pse_type=pse_type,
+                                        rescale_threshold=thr)
     code = fa.fa_check_status()
     assert code == 0, fa.fa_strerror(code)
     torch.cuda.synchronize()
     ex = A.Extras(atten_mask=None if mask is None else mask.astype(np.float64),
-                  pse_type=2 if alibi else 1,
+                  pse=None if pse is None else pse[1],
+                  pse_type=2 if alibi else (pse_type if pse is not None else 1),
                   sparse_mode=0 if window is not None else (3 if bottom_right else None),
                   pre_tokens=window[0] if window is not None else 2 ** 31 - 1,
                   next_tokens=window[1] if window is not None else 2 ** 31 - 1)
@@ -127,3 +143,20 @@ def test_window_mask_and_alibi_together():
     m = _mask_bits((640, 640), 0.2, seed=591)
     O, L, Or, Lr = _run(p, causal=True, window=(257, 0), mask=m, alibi=True)
     compare(O, L, Or, Lr, "window + mask + alibi")
+
+
+@pytest.mark.parametrize("pse_type", [0, 1])
+def test_pse_bias_shared(pse_type):
+    """A [Sq, Skv] bf16 bias shared by every batch and head, causal."""
+    p = W.dense(name="pse", B=2, Hq=2, Sq=384, D=128, mask=W.MASK_CAUSAL, seed=60)
+    O, L, Or, Lr = _run(p, causal=True, pse=_bias((384, 384), "bf16", 601), pse_type=pse_type)
+    compare(O, L, Or, Lr, f"pse shared type {pse_type}")
+
+
+def test_pse_bias_per_head_fp16_with_window():
+    """A [1, Hq, Sq, Skv] fp16 bias (one per head), D 64, GQA 4:2, with a
+    two-sided window and a ragged key count (Skv 264)."""
+    p = W.dense(name="pse2", B=1, Hq=4, Hkv=2, Sq=256, Skv=264, D=64, dtype="fp16",
+                mask=W.MASK_NONE, seed=61)
+    O, L, Or, Lr = _run(p, window=(100, 30), pse=_bias((1, 4, 256, 264), "fp16", 611), pse_type=0)
+    compare(O, L, Or, Lr, "pse per head + window")
