@@ -41,7 +41,8 @@ class fa_extras_t(ctypes.Structure):
                 ("mask_stride_h", ctypes.c_int64), ("mask_stride_q", ctypes.c_int64),
                 ("pse", ctypes.c_void_p), ("pse_stride_b", ctypes.c_int64),
                 ("pse_stride_h", ctypes.c_int64), ("pse_stride_q", ctypes.c_int64),
-                ("pse_type", ctypes.c_int32)]
+                ("pse_type", ctypes.c_int32), ("keep_prob", ctypes.c_float),
+                ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64)]
 
 
 _lib = None
@@ -230,7 +231,7 @@ def flash_attention_forward(q, k, v=None, *, scale: Optional[float] = None, caus
                             topk_idx=None, rescale_threshold: float = 0.0, out=None, lse=None,
                             o_lo=None, window=None, bottom_right_causal: bool = False,
                             atten_mask=None, alibi: bool = False, pse=None, pse_type: int = 0,
-                            stream=None):
+                            dropout=None, stream=None):
     """Allocating convenience wrapper over fa_fwd.
 
     q [B,Hq,Sq,D], k [B,Hkv,Skv,D], v [B,Hkv,Skv,Dv] (or None with top-k and a
@@ -245,7 +246,8 @@ def flash_attention_forward(q, k, v=None, *, scale: Optional[float] = None, caus
     [B, Hq, Sq, Skv], True / nonzero = masked; its last dimension contiguous),
     alibi (pse_type 2), pse (a bias tensor of q's type [..., Sq, Skv]
     broadcastable like atten_mask, last dim contiguous) with pse_type 0
-    (added after the scale) or 1 (before)."""
+    (added after the scale) or 1 (before), dropout=(keep_prob, seed, offset)
+    (the Philox mask of include/fa_fwd.h)."""
     import torch
     if q.dtype not in (torch.bfloat16, torch.float16):
         raise TypeError("q, k, v must be bf16 or fp16")
@@ -279,7 +281,8 @@ def flash_attention_forward(q, k, v=None, *, scale: Optional[float] = None, caus
         tk = (topk_idx, topk_idx.shape[-1], topk_idx.shape[-2] * topk_idx.shape[-1])
     if seqlens is not None:
         assert seqlens.dtype == torch.int32 and seqlens.is_cuda
-    if window is not None or bottom_right_causal or atten_mask is not None or alibi or pse is not None:
+    if (window is not None or bottom_right_causal or atten_mask is not None or alibi
+            or pse is not None or dropout is not None):
         if o_lo not in (None, False) or bs is not None or tk is not None:
             raise ValueError("the optional terms apply to dense problems without o_lo")
         ex = fa_extras_t()
@@ -288,6 +291,8 @@ def flash_attention_forward(q, k, v=None, *, scale: Optional[float] = None, caus
             raise ValueError("window and bottom_right_causal are exclusive")
         ex.pre_tokens, ex.next_tokens = (int(window[0]), int(window[1])) if window is not None else (0, 0)
         ex.alibi = 1 if alibi else 0
+        if dropout is not None:
+            ex.keep_prob, ex.seed, ex.offset = float(dropout[0]), int(dropout[1]), int(dropout[2])
         keep = None
         if atten_mask is not None:
             m = atten_mask

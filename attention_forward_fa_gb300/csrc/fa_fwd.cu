@@ -476,6 +476,21 @@ int run_tiled(const void* q, const void* k, const void* v, void* o, void* o_lo, 
     prm.pse_sh = ex->pse_stride_h;
     prm.pse_sq = ex->pse_stride_q;
     prm.pse_type = ex->pse_type;
+    // dropout: keep a byte b when b < keep_prob * 255, as an integer bound
+    prm.keep_prob = 1.f;
+    prm.keep_thr = 256;
+    if (ex->keep_prob > 0.f && ex->keep_prob < 1.f) {
+      int thr = 0;
+      while (thr < 256 && (double)thr < (double)ex->keep_prob * 255.0) ++thr;
+      prm.keep_thr = thr;
+      prm.keep_prob = ex->keep_prob;
+      prm.drop_key0 = (uint32_t)(ex->seed & 0xFFFFFFFFull);
+      prm.drop_key1 = (uint32_t)(ex->seed >> 32);
+      prm.drop_ctr0 = ex->offset / 16;
+    }
+  } else {
+    prm.keep_prob = 1.f;
+    prm.keep_thr = 256;
   }
   const long long units = (long long)prm.units_per_q * prm.n_qpos;
   if (units > 0x7FFFFFFF) return FA_ERR_SHAPE;
@@ -732,6 +747,10 @@ int fa_fwd_ext(const void* q, const void* k, const void* v, void* o, float* lse,
   if (extras->window < 0 || extras->window > 2 || extras->alibi < 0 || extras->alibi > 1)
     return FA_ERR_SHAPE;
   if ((Skv + fa::kBN - 1) / fa::kBN > fa::kMaxSel) return FA_ERR_SHAPE;
+  // keep_prob 0 (a zero-initialised struct) or 1: no dropout
+  if (!(extras->keep_prob >= 0.f && extras->keep_prob <= 1.f)) return FA_ERR_SHAPE;
+  const bool dropout = extras->keep_prob > 0.f && extras->keep_prob < 1.f;
+  if (dropout && (extras->offset % 16 || Skv % 16)) return FA_ERR_SHAPE;
   if (extras->pse) {
     if (extras->alibi || extras->pse_type < 0 || extras->pse_type > 1) return FA_ERR_SHAPE;
     if (extras->pse_stride_b < 0 || extras->pse_stride_h < 0 || extras->pse_stride_q < 0)

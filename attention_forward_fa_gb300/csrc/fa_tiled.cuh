@@ -96,6 +96,13 @@ struct TiledParams {
   const uint16_t* pse;         // bias tensor or null: q's type, strides below (elements)
   long long pse_sb, pse_sh, pse_sq;
   int pse_type;                // 0: s * scale + pse; 1: (s + pse) * scale
+  // dropout, O = (P * M / keep_prob) V: element (b, h, i, j) of the
+  // row-major [B, Hq, Sq, Skv] grid is kept when byte (index % 16) of the
+  // Philox4x32-10 output for counter drop_ctr0 + index / 16 is below keep_thr
+  int keep_thr;                // 256: no dropout
+  float keep_prob;
+  uint32_t drop_key0, drop_key1;
+  unsigned long long drop_ctr0;
 };
 
 // Trace points: compiled only with -DFA_TRACE (a profiling build); otherwise
@@ -275,6 +282,23 @@ __device__ __forceinline__ int ext_key_hi(const TiledParams& p, int i, int q_len
   if (p.win_mode == 1) hi = min(hi, i + p.next_tokens);
   if (p.win_mode == 2) hi = min(hi, i + kv_len - q_len);  // bottom-right causal
   return hi;
+}
+
+// Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC 2011): per round (c0, c1, c2, c3) -> (hi(M1 c2) ^ c1 ^
+// k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0)), the key advanced by the Weyl
+// increments between rounds; the dropout generator of the FlashAttentionScore-
+// Grad write-up, section 5.3.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
 }
 
 // The order in which the MMA warp consumes K / V tiles, as a numbered event
@@ -482,7 +506,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       // arbitrary bias tensor may peak any row as well
       const int ka = ext_key_hi(p, qa, q_len, kv_len) - lo_a + 1;
       const int kb = hi_b - ext_key_lo(p, qb) + 1;
-      hilo = p.amask != nullptr || p.alibi || p.pse != nullptr || min(ka, kb) < 2 * kHiLoKeys;
+      hilo = p.amask != nullptr || p.alibi || p.pse != nullptr || p.keep_thr < 256 ||
+             min(ka, kb) < 2 * kHiLoKeys;
     } else if (live && sparse) {
       const int* lst = p.blk_idx + (long long)b * p.blk_stride_b +
                        (long long)(t ? h1 : h0) * p.blk_stride_h + (long long)qt * p.max_sel;
@@ -545,6 +570,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     const uint8_t* mrow = nullptr;
     const uint16_t* prow = nullptr;
     float slope2 = 0.f;
+    unsigned long long drop_row = 0;   // dropout: grid index of (b, h, row, key 0)
     if constexpr (kExtras) {
       ek_lo = ext_key_lo(p, qi);
       ek_hi = ext_key_hi(p, qi, q_len, kv_len);
@@ -554,13 +580,16 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       if (p.pse)
         prow = p.pse + b * p.pse_sb + h * p.pse_sh + (long long)min(qi, p.Sq - 1) * p.pse_sq;
       if (p.alibi) slope2 = -exp2f(-8.f * (float)(h + 1) / (float)p.Hq) * 1.4426950408889634f;
+      drop_row = ((unsigned long long)(b * p.Hq + h) * p.Sq + min(qi, p.Sq - 1)) * p.Skv;
     }
     float m = -INFINITY, l = 0.f;
     bool dead = false;   // a bounded wait expired: keep the hand-offs, skip the work
     for (int j = 0; j < nt; ++j) {
       // extras: this tile's bytes of the explicit mask, loaded before the S
-      // wait (128 keys per row, 16 bytes per load; keys past Skv read none)
+      // wait (128 keys per row, 16 bytes per load; keys past Skv read none),
+      // and its dropout keep bits
       uint4 mbytes[kBN / 16];
+      uint32_t dbits[kBN / 32] = {~0u, ~0u, ~0u, ~0u};
       if constexpr (kExtras) {
         if (mrow) {
           const int kb0 = s_list[t * kMaxSel + j] * kBN;
@@ -568,6 +597,25 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           for (int q = 0; q < kBN / 16; ++q)
             mbytes[q] = kb0 + 16 * q < p.Skv ? __ldg(reinterpret_cast<const uint4*>(mrow + kb0 + 16 * q))
                                          : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (p.keep_thr < 256) {
+          // the dropout keep bits of this tile's 128 keys: eight Philox
+          // outputs of 16 bytes, one byte per key (bytes of a word low first)
+          const int kb0 = s_list[t * kMaxSel + j] * kBN;
+          const unsigned long long c0 = p.drop_ctr0 + (drop_row + kb0) / 16;
+#pragma unroll
+          for (int q = 0; q < kBN / 16; ++q) {
+            const unsigned long long cq = c0 + q;
+            const uint4 r = philox4x32_10(make_uint4((uint32_t)cq, (uint32_t)(cq >> 32), 0u, 0u),
+                                          p.drop_key0, p.drop_key1);
+            const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+            uint32_t bits = 0;
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              bits |= (((w4[e >> 2] >> (8 * (e & 3))) & 0xFFu) < (uint32_t)p.keep_thr ? 1u : 0u) << e;
+            if (q & 1) dbits[q >> 1] |= bits << 16;
+            else dbits[q >> 1] = bits;
+          }
         }
         if (prow) {
           // the bias row of this tile into L2 (read chunk by chunk below)
@@ -752,6 +800,12 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
             a0 = ex2_approx(a0);
             a1 = ex2_approx(a1);
             sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(a0, a1));
+            if constexpr (kExtras) {
+              // dropout: the row sum keeps every p, the P.V operand only the kept
+              // ones (the 1 / keep_prob factor is applied with 1 / l)
+              a0 = ((dbits[cc] >> (2 * i)) & 1u) ? a0 : 0.f;
+              a1 = ((dbits[cc] >> (2 * i + 1)) & 1u) ? a1 : 0.f;
+            }
             ph[i] = pack_f16x2(a0, a1);
             pl[i] = pack_f16x2(a0 - f16_lo_to_f32(ph[i]), a1 - f16_hi_to_f32(ph[i]));
           }
@@ -816,7 +870,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
                      : "=r"(plane)
                      : "r"(((smem_u32(smem_raw) + 1023u) & ~1023u) + SM::kMiscOff + 8 + 4 * (5 + t)));
         const bool write = qi < p.Sq;
-        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        const float inv_l = (l > 0.f) ? 1.f / (kExtras ? l * p.keep_prob : l) : 0.f;
         const uint32_t tO = tmem + 256u + 128u * t + lane_off;
         const uint32_t stage = ((smem_u32(smem_raw) + 1023u) & ~1023u) + SM::kQOff + t * SM::kQBytes;
         const size_t rows_all = (size_t)p.B * p.Hq * p.Sq;

@@ -196,6 +196,19 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *   pse_type     with pse: 0 adds it after the scale (s = scale Q K^T + pse),
  *                1 before (s = scale (Q K^T + pse)).  pse and alibi are
  *                exclusive (the doc's pse_type picks one).
+ *   keep_prob    0 (a zero-initialised struct) or 1: no dropout.  In
+ *                (0, 1): dropout after the softmax,
+ *                O = (P * M / keep_prob) V with LSE still the softmax's
+ *                ("FlashAttentionScoreGrad" pytest framework write-up,
+ *                section 5.2).  M follows its section 5.3 generator:
+ *                element (b, h, i, j), at index e of the row-major
+ *                [B, Hq, Sq, Skv] grid, is kept when byte e % 16 of the
+ *                Philox4x32-10 output for counter offset / 16 + e / 16
+ *                (counter words: its low and high 32 bits, then 0, 0; key:
+ *                the seed's low and high 32 bits; bytes of the four output
+ *                words in order, low byte first) is below keep_prob * 255.
+ *                offset and Skv must be multiples of 16.
+ *   seed, offset the generator's seed and stream offset (in elements).
  *
  * A row whose keys are all masked gets O = 0 and LSE = +inf, as in fa_fwd.
  */
@@ -213,6 +226,9 @@ typedef struct {
   int64_t pse_stride_h;
   int64_t pse_stride_q;
   int32_t pse_type;
+  float keep_prob;
+  uint64_t seed;
+  uint64_t offset;
 } fa_extras_t;
 
 /* fa_fwd with the optional terms above (`extras` is a host pointer, required).
@@ -221,7 +237,8 @@ typedef struct {
  * FA_MASK_NONE or FA_MASK_CAUSAL plus the dtype flags.  Every other argument
  * and output as fa_fwd.  Errors: FA_ERR_NULL (extras NULL), FA_ERR_SHAPE
  * (window, alibi or pse_type out of range, pse with alibi, negative stride,
- * Skv too long), FA_ERR_ALIGN (mask or pse layout), FA_ERR_UNSUPPORTED (D, Dv), and those of
+ * Skv too long, keep_prob outside [0, 1], a dropout offset or Skv not a
+ * multiple of 16), FA_ERR_ALIGN (mask or pse layout), FA_ERR_UNSUPPORTED (D, Dv), and those of
  * fa_fwd.  Allocates nothing. */
 int fa_fwd_ext(const void* q, const void* k, const void* v, void* o, float* lse,
                int B, int Hq, int Hkv, int Sq, int Skv, int D, int Dv, float scale,

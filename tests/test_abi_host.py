@@ -212,6 +212,8 @@ def _ex(**kw):
     (_ex(pse=P, alibi=1), {}, -2), (_ex(pse=P, pse_type=2), {}, -2),
     (_ex(pse=P, pse_stride_q=-8), {}, -2), (_ex(pse=P + 8, pse_stride_q=128), {}, -4),
     (_ex(pse=P, pse_stride_q=124), {}, -4), (_ex(pse=P, pse_stride_q=128), dict(Skv=124), -4),
+    (_ex(keep_prob=-0.5), {}, -2), (_ex(keep_prob=1.5), {}, -2), (_ex(keep_prob=float("nan")), {}, -2),
+    (_ex(keep_prob=0.9, offset=8), {}, -2), (_ex(keep_prob=0.9), dict(Skv=136), -2),
 ])
 def test_ext_argument_errors(lib, ex, kw, code):
     assert call_ext(lib, ex, **kw) == code

@@ -1,8 +1,9 @@
 """GPU parity of the operator's optional terms (fa_fwd_ext) against the fp64
 oracle's Extras: the key window of sparse_mode 0 (pre_tokens / next_tokens),
 the bottom-right causal mask of sparse_mode 3, an explicit attention mask, the
-ALiBi position bias of pse_type 2 and a pse bias tensor added after (pse_type
-0) or before (pse_type 1) the scale ("FlashAttentionScore" operator doc,
+ALiBi position bias of pse_type 2, a pse bias tensor added after (pse_type
+0) or before (pse_type 1) the scale, and dropout with the Philox mask of the
+"FlashAttentionScoreGrad" write-up, section 5.3 ("FlashAttentionScore" operator doc,
 gitcode ops-transformer, sections "Function description" and "Parameter
 description").  Tolerances as every forward parity test: elementwise
 |dO| <= 1e-4 + 7.8125e-3 |ref|, rel-L2 <= 3e-3, |dLSE| <= 2e-3, +inf rows
@@ -12,6 +13,7 @@ import pytest
 
 from attention_forward_fa_gb300 import workloads as W
 from oracle import attention as A
+from oracle import backward as BW
 from tests.parity import compare, to_device
 
 pytestmark = pytest.mark.gpu
@@ -37,7 +39,7 @@ def _bias(shape, dtype, seed, sigma=2.0):
 
 
 def _run(p, causal=False, window=None, bottom_right=False, mask=None, alibi=False, thr=0.0,
-         pse=None, pse_type=0):
+         pse=None, pse_type=0, dropout=None):
     import torch
     import attention_forward_fa_gb300 as fa
     d = to_device(p)
@@ -50,11 +52,19 @@ def _run(p, causal=False, window=None, bottom_right=False, mask=None, alibi=Fals
                                         seqlens=d["seqlens"], window=window,
                                         bottom_right_causal=bottom_right, atten_mask=am,
                                         alibi=alibi, pse=pse_t, pse_type=pse_type,
-                                        rescale_threshold=thr)
+                                        dropout=dropout, rescale_threshold=thr)
     code = fa.fa_check_status()
     assert code == 0, fa.fa_strerror(code)
     torch.cuda.synchronize()
-    ex = A.Extras(atten_mask=None if mask is None else mask.astype(np.float64),
+    drop = {}
+    if dropout is not None:
+        keep, seed, offset = dropout
+        # keep_prob is a float32 argument of the C ABI (as of the operator):
+        # the byte bound keep_prob * 255 is taken from that value
+        keep = float(np.float32(keep))
+        mflat = BW.philox_dropout_mask(seed, offset, p.B * p.Hq * p.Sq * p.Skv, keep)
+        drop = dict(drop_mask=mflat.reshape(p.B, p.Hq, p.Sq, p.Skv).astype(np.float64), keep_prob=keep)
+    ex = A.Extras(**drop, atten_mask=None if mask is None else mask.astype(np.float64),
                   pse=None if pse is None else pse[1],
                   pse_type=2 if alibi else (pse_type if pse is not None else 1),
                   sparse_mode=0 if window is not None else (3 if bottom_right else None),
@@ -160,3 +170,39 @@ def test_pse_bias_per_head_fp16_with_window():
                 mask=W.MASK_NONE, seed=61)
     O, L, Or, Lr = _run(p, window=(100, 30), pse=_bias((1, 4, 256, 264), "fp16", 611), pse_type=0)
     compare(O, L, Or, Lr, "pse per head + window")
+
+
+def test_dropout_causal():
+    """keep_prob 0.9 on a causal problem: the Philox keep mask of every
+    (batch, head, row, key), the kept P scaled by 1 / keep_prob, LSE the
+    softmax's."""
+    p = W.dense(name="drop", B=1, Hq=2, Sq=256, D=128, mask=W.MASK_CAUSAL, seed=62)
+    O, L, Or, Lr = _run(p, causal=True, dropout=(0.9, 2024, 0))
+    compare(O, L, Or, Lr, "dropout 0.9")
+
+
+def test_dropout_offset_fp16_window_gqa():
+    """keep_prob 0.75 from stream offset 4096 * 16, with a seed above 2^32,
+    fp16 D 64, GQA 4:2, Sq 128 != Skv 384, and a key window."""
+    p = W.dense(name="drop2", B=2, Hq=4, Hkv=2, Sq=128, Skv=384, D=64, dtype="fp16",
+                mask=W.MASK_NONE, seed=63)
+    O, L, Or, Lr = _run(p, window=(200, 150), dropout=(0.75, (7 << 32) + 12345, 4096 * 16))
+    compare(O, L, Or, Lr, "dropout 0.75 + window")
+
+
+@pytest.mark.parametrize("keep", [0.9, 0.6])
+def test_dropout_mask_bit_exact(keep):
+    """Every keep bit visible in the output: q = 0 makes P uniform (1/128)
+    and v_j = e_j (one-hot), so O[i, j] = M_ij / (128 keep_prob): a single
+    flipped bit would miss the bound by two orders of magnitude.  keep 0.6
+    puts the byte bound next to an integer (float32 0.6 * 255 = 153.000006,
+    so byte 153 is kept)."""
+    import dataclasses
+    p = W.dense(name="dropbits", B=1, Hq=2, Sq=128, D=128, dtype="fp16", mask=W.MASK_NONE, seed=64)
+    q = np.zeros((1, 2, 128, 128), np.float32)
+    v = np.broadcast_to(np.eye(128, dtype=np.float32), (1, 2, 128, 128)).copy()
+    p = dataclasses.replace(p, q_bits=W.to_bits(q, "fp16"), v_bits=W.to_bits(v, "fp16"))
+    O, L, Or, Lr = _run(p, dropout=(keep, 99, 16 * 1000))
+    kept = Or * (128 * float(np.float32(keep)))
+    assert np.allclose(kept, np.round(kept)) and 0.5 < kept.mean() / keep < 1.5
+    compare(O, L, Or, Lr, f"dropout bits keep {keep}")
