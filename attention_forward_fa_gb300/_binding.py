@@ -15,6 +15,8 @@ FA_MASK_CAUSAL_DIAG_BLOCK = 2
 FA_DTYPE_FP16 = 0x100
 FA_V_FROM_K = 0x200
 FA_V_FP16 = 0x400
+FA_FP8_E4M3 = 0
+FA_FP8_E5M2 = 1
 
 FA_OK = 0
 
@@ -66,6 +68,11 @@ def library() -> ctypes.CDLL:
             ctypes.POINTER(fa_topk_t), ctypes.c_float, ctypes.c_void_p]
         lib.fa_fwd_noalloc.restype = ctypes.c_int
         lib.fa_fwd_noalloc.argtypes = lib.fa_fwd.argtypes
+        lib.fa_fwd_fp8.restype = ctypes.c_int
+        lib.fa_fwd_fp8.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_int, ctypes.c_void_p,
+                                                           ctypes.c_void_p] + [ctypes.c_int] * 7 + [
+            ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(fa_extras_t),
+            ctypes.c_float, ctypes.c_void_p]
         lib.fa_fwd_ext.restype = ctypes.c_int
         lib.fa_fwd_ext.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 7 + [
             ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(fa_extras_t),
@@ -173,6 +180,42 @@ def fa_fwd_ext(q, k, v, o, lse, B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D:
                                 D, Dv, float(scale), int(mask_mode), _ptr(seqlens),
                                 ctypes.byref(extras) if extras is not None else None,
                                 float(rescale_threshold), _stream(stream))
+
+
+def fa_fwd_fp8(q8, k8, v8, d_scale_q, d_scale_k, d_scale_v, fp8_format: int, o, lse, B: int,
+               Hq: int, Hkv: int, Sq: int, Skv: int, D: int, Dv: int, scale: float,
+               mask_mode: int, seqlens=None, extras=None, rescale_threshold: float = 0.0,
+               stream=None) -> int:
+    """Direct call of fa_fwd_fp8 (see include/fa_fwd.h).  Returns the FA_* code."""
+    return library().fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(d_scale_q), _ptr(d_scale_k),
+                                _ptr(d_scale_v), int(fp8_format), _ptr(o), _ptr(lse), B, Hq, Hkv,
+                                Sq, Skv, D, Dv, float(scale), int(mask_mode), _ptr(seqlens),
+                                ctypes.byref(extras) if extras is not None else None,
+                                float(rescale_threshold), _stream(stream))
+
+
+def flash_attention_forward_fp8(q8, k8, v8, d_scale_q, d_scale_k, d_scale_v, *, fp8_format="e4m3",
+                                scale: Optional[float] = None, causal: bool = False, seqlens=None,
+                                rescale_threshold: float = 0.0, stream=None):
+    """Allocating wrapper over fa_fwd_fp8: q8 / k8 / v8 CUDA tensors of fp8 bytes
+    (torch float8_e4m3fn / float8_e5m2 or uint8) [B, H, S, D], d_scale_* fp32
+    [B, H, ceil(S / 128)].  Returns (o fp16, lse)."""
+    import torch
+    B, Hq, Sq, D = q8.shape
+    _, Hkv, Skv, _ = k8.shape
+    Dv = v8.shape[-1]
+    for t in (q8, k8, v8, d_scale_q, d_scale_k, d_scale_v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("FP8 inputs and scales must be contiguous CUDA tensors")
+    fmt = {"e4m3": FA_FP8_E4M3, "e5m2": FA_FP8_E5M2}[fp8_format]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out = torch.empty((B, Hq, Sq, Dv), dtype=torch.float16, device=q8.device)
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q8.device)
+    _raise(fa_fwd_fp8(q8, k8, v8, d_scale_q, d_scale_k, d_scale_v, fmt, out, lse, B, Hq, Hkv, Sq,
+                      Skv, D, Dv, scale, FA_MASK_CAUSAL if causal else FA_MASK_NONE, seqlens, None,
+                      rescale_threshold, stream))
+    return out, lse
 
 
 def fa_fwd_noalloc(q, k, v, o, lse, B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int,

@@ -142,6 +142,61 @@ __global__ void __launch_bounds__(256) fa_convert_v_kernel(const uint4* __restri
   if ((vmax & 0xFFFFu) > 0x477Fu || (vmax >> 16) > 0x477Fu) atomicOr(status, fa::kStatusRange);
 }
 
+// FP8 inputs as fp16: the values of x_q (e4m3fn or e5m2 bytes), exact since
+// both formats lie inside fp16 (d_scale null; the attention kernel applies the
+// dequant scales), or x_q * d_scale of the row's block of 128 rows along S
+// rounded once to fp16.  x_q [planes, S, D], d_scale [planes, ceil(S / 128)].
+// Each thread converts 16 bytes.
+template <bool E5M2>
+__global__ void __launch_bounds__(256) fa_fp8_to_fp16_kernel(const uint4* __restrict__ in,
+                                                             const float* __restrict__ d_scale,
+                                                             uint4* __restrict__ out, size_t n16,
+                                                             int S, int D) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  const int nb = (S + 127) / 128;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16; i += stride) {
+    float d = 1.f;
+    if (d_scale) {
+      const size_t row = (i * 16) / (size_t)D;            // D is a multiple of 16
+      const size_t plane = row / (size_t)S;
+      d = d_scale[plane * nb + (int)(row - plane * S) / 128];
+    }
+    const uint4 w = in[i];
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const uint16_t two = (uint16_t)(ww[q] >> (16 * e));
+        uint32_t f2;
+        if (E5M2)
+          asm("{\n .reg .b16 t;\n mov.b16 t, %1;\n cvt.rn.f16x2.e5m2x2 %0, t;\n}" : "=r"(f2) : "h"(two));
+        else
+          asm("{\n .reg .b16 t;\n mov.b16 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}" : "=r"(f2) : "h"(two));
+        h[2 * q + e] = d_scale ? fa::pack_f16x2(fa::f16_lo_to_f32(f2) * d, fa::f16_hi_to_f32(f2) * d) : f2;
+      }
+    }
+    out[2 * i] = make_uint4(h[0], h[1], h[2], h[3]);
+    out[2 * i + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
+int fp8_to_fp16(const void* x8, const float* d_scale, void* x16, size_t planes, int S, int D,
+                bool e5m2, cudaStream_t st) {
+  const size_t n16 = planes * (size_t)S * D / 16;   // D is a multiple of 16
+  int blocks = (int)std::min<size_t>((n16 + 255) / 256, 152 * 8);
+  if (blocks < 1) blocks = 1;
+  if (e5m2)
+    fa_fp8_to_fp16_kernel<true><<<blocks, 256, 0, st>>>(static_cast<const uint4*>(x8), d_scale,
+                                                        static_cast<uint4*>(x16), n16, S, D);
+  else
+    fa_fp8_to_fp16_kernel<false><<<blocks, 256, 0, st>>>(static_cast<const uint4*>(x8), d_scale,
+                                                         static_cast<uint4*>(x16), n16, S, D);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
 int convert_v(const void* v, void* vh, size_t n_elems, int* status, cudaStream_t st) {
   const size_t n16 = n_elems / 8;
   int blocks = (int)std::min<size_t>((n16 + 255) / 256, 152 * 8);
@@ -352,6 +407,33 @@ int validate(const void* q, const void* k, const void* v, void* o, float* lse, i
   return FA_OK;
 }
 
+// Checks of the optional terms (fa_fwd_ext, fa_fwd_fp8); nothing is launched.
+int validate_extras(const fa_extras_t* extras, int Skv) {
+  if (extras->window < 0 || extras->window > 2 || extras->alibi < 0 || extras->alibi > 1)
+    return FA_ERR_SHAPE;
+  if ((Skv + fa::kBN - 1) / fa::kBN > fa::kMaxSel) return FA_ERR_SHAPE;
+  // keep_prob 0 (a zero-initialised struct) or 1: no dropout
+  if (!(extras->keep_prob >= 0.f && extras->keep_prob <= 1.f)) return FA_ERR_SHAPE;
+  const bool dropout = extras->keep_prob > 0.f && extras->keep_prob < 1.f;
+  if (dropout && (extras->offset % 16 || Skv % 16)) return FA_ERR_SHAPE;
+  if (extras->pse) {
+    if (extras->alibi || extras->pse_type < 0 || extras->pse_type > 1) return FA_ERR_SHAPE;
+    if (extras->pse_stride_b < 0 || extras->pse_stride_h < 0 || extras->pse_stride_q < 0)
+      return FA_ERR_SHAPE;
+    if (!aligned(extras->pse, 16) || extras->pse_stride_q % 8 || extras->pse_stride_h % 8 ||
+        extras->pse_stride_b % 8 || Skv % 8)
+      return FA_ERR_ALIGN;
+  }
+  if (extras->atten_mask) {
+    if (extras->mask_stride_b < 0 || extras->mask_stride_h < 0 || extras->mask_stride_q < 0)
+      return FA_ERR_SHAPE;
+    if (!aligned(extras->atten_mask, 16) || extras->mask_stride_q % 16 ||
+        extras->mask_stride_h % 16 || extras->mask_stride_b % 16 || Skv % 16)
+      return FA_ERR_ALIGN;
+  }
+  return FA_OK;
+}
+
 template <bool BF16>
 int launch_mla(const fa::MlaParams& prm, long long units, cudaStream_t st) {
   auto kern = fa::fa_mla_topk_kernel<BF16>;
@@ -410,7 +492,8 @@ int run_tiled(const void* q, const void* k, const void* v, void* o, void* o_lo, 
               int Hq, int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
               const int32_t* seqlens, const fa_block_sparse_t* kv_block_idx,
               float rescale_threshold, int* status, cudaStream_t st, bool may_alloc,
-              const fa_extras_t* ex = nullptr) {
+              const fa_extras_t* ex = nullptr, const float* ds_q = nullptr,
+              const float* ds_k = nullptr, const float* ds_v = nullptr) {
   const int mask = mask_mode & 0xF;
   const bool fp16 = (mask_mode & FA_DTYPE_FP16) != 0;
   const bool conv = !fp16 && !(mask_mode & FA_V_FP16);   // V arrives as bf16
@@ -492,6 +575,11 @@ int run_tiled(const void* q, const void* k, const void* v, void* o, void* o_lo, 
     prm.keep_prob = 1.f;
     prm.keep_thr = 256;
   }
+  prm.dsq = ds_q;
+  prm.dsk = ds_k;
+  prm.dsv = ds_v;
+  prm.ds_nbq = (Sq + 127) / 128;
+  prm.ds_nbk = (Skv + 127) / 128;
   const long long units = (long long)prm.units_per_q * prm.n_qpos;
   if (units > 0x7FFFFFFF) return FA_ERR_SHAPE;
 
@@ -744,33 +832,60 @@ int fa_fwd_ext(const void* q, const void* k, const void* v, void* o, float* lse,
                           nullptr, nullptr, rescale_threshold);
   if (rc != FA_OK) return rc;
   if ((mask_mode & FA_V_FROM_K) || (mask_mode & 0xF) > FA_MASK_CAUSAL) return FA_ERR_SHAPE;
-  if (extras->window < 0 || extras->window > 2 || extras->alibi < 0 || extras->alibi > 1)
-    return FA_ERR_SHAPE;
-  if ((Skv + fa::kBN - 1) / fa::kBN > fa::kMaxSel) return FA_ERR_SHAPE;
-  // keep_prob 0 (a zero-initialised struct) or 1: no dropout
-  if (!(extras->keep_prob >= 0.f && extras->keep_prob <= 1.f)) return FA_ERR_SHAPE;
-  const bool dropout = extras->keep_prob > 0.f && extras->keep_prob < 1.f;
-  if (dropout && (extras->offset % 16 || Skv % 16)) return FA_ERR_SHAPE;
-  if (extras->pse) {
-    if (extras->alibi || extras->pse_type < 0 || extras->pse_type > 1) return FA_ERR_SHAPE;
-    if (extras->pse_stride_b < 0 || extras->pse_stride_h < 0 || extras->pse_stride_q < 0)
-      return FA_ERR_SHAPE;
-    if (!aligned(extras->pse, 16) || extras->pse_stride_q % 8 || extras->pse_stride_h % 8 ||
-        extras->pse_stride_b % 8 || Skv % 8)
-      return FA_ERR_ALIGN;
-  }
-  if (extras->atten_mask) {
-    if (extras->mask_stride_b < 0 || extras->mask_stride_h < 0 || extras->mask_stride_q < 0)
-      return FA_ERR_SHAPE;
-    if (!aligned(extras->atten_mask, 16) || extras->mask_stride_q % 16 ||
-        extras->mask_stride_h % 16 || extras->mask_stride_b % 16 || Skv % 16)
-      return FA_ERR_ALIGN;
-  }
+  const int rce = validate_extras(extras, Skv);
+  if (rce != FA_OK) return rce;
   int* status = status_ptr();
   if (!status) return cuda_fail(cudaGetLastError());
   return run_tiled(q, k, v, o, nullptr, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mask_mode, seqlens,
                    nullptr, rescale_threshold, status, reinterpret_cast<cudaStream_t>(stream),
                    /*may_alloc=*/false, extras);
+}
+
+int fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* d_scale_q,
+               const float* d_scale_k, const float* d_scale_v, int fp8_format, void* o, float* lse,
+               int B, int Hq, int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
+               const int32_t* seqlens, const fa_extras_t* extras, float rescale_threshold,
+               void* stream) {
+  if (!d_scale_q || !d_scale_k || !d_scale_v) return FA_ERR_NULL;
+  if (fp8_format != FA_FP8_E4M3 && fp8_format != FA_FP8_E5M2) return FA_ERR_SHAPE;
+  if (mask_mode & ~0xF) return FA_ERR_SHAPE;     // o is fp16; no other flag applies
+  const int mm = mask_mode | FA_DTYPE_FP16;
+  // the arguments as the fp16 call will see them (q8, k8, v8 stand in for the copies)
+  int rc = validate(q8, k8, v8, o, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mm, seqlens, nullptr,
+                    nullptr, rescale_threshold);
+  if (rc != FA_OK) return rc;
+  if ((mask_mode & 0xF) > FA_MASK_CAUSAL) return FA_ERR_SHAPE;
+  if ((Skv + fa::kBN - 1) / fa::kBN > fa::kMaxSel) return FA_ERR_SHAPE;
+  if (!aligned(d_scale_q, 4) || !aligned(d_scale_k, 4) || !aligned(d_scale_v, 4))
+    return FA_ERR_ALIGN;
+  if (extras) {
+    const int rce = validate_extras(extras, Skv);
+    if (rce != FA_OK) return rce;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* status = status_ptr();
+  if (!status) return cuda_fail(cudaGetLastError());
+  // exact fp16 copies in stream-ordered scratch; the kernel applies the
+  // dequant scales (S by d_q d_k, P by d_v)
+  const size_t nq = (size_t)B * Hq * Sq * D, nk = (size_t)B * Hkv * Skv * D,
+               nv = (size_t)B * Hkv * Skv * Dv;
+  uint8_t* scratch = static_cast<uint8_t*>(scratch_alloc((nq + nk + nv) * 2, st));
+  if (!scratch) return cuda_fail(cudaGetLastError());
+  void* q16 = scratch;
+  void* k16 = scratch + nq * 2;
+  void* v16 = scratch + (nq + nk) * 2;
+  const bool e5m2 = fp8_format == FA_FP8_E5M2;
+  rc = fp8_to_fp16(q8, nullptr, q16, (size_t)B * Hq, Sq, D, e5m2, st);
+  if (rc == FA_OK) rc = fp8_to_fp16(k8, nullptr, k16, (size_t)B * Hkv, Skv, D, e5m2, st);
+  if (rc == FA_OK) rc = fp8_to_fp16(v8, nullptr, v16, (size_t)B * Hkv, Skv, Dv, e5m2, st);
+  fa_extras_t none;
+  std::memset(&none, 0, sizeof(none));
+  if (rc == FA_OK)
+    rc = run_tiled(q16, k16, v16, o, nullptr, lse, B, Hq, Hkv, Sq, Skv, D, Dv, scale, mm, seqlens,
+                   nullptr, rescale_threshold, status, st, /*may_alloc=*/true,
+                   extras ? extras : &none, d_scale_q, d_scale_k, d_scale_v);
+  cudaFreeAsync(scratch, st);
+  return rc;
 }
 
 int fa_fwd_o_lo(const void* q, const void* k, const void* v, void* o, void* o_lo, float* lse,

@@ -103,6 +103,16 @@ struct TiledParams {
   float keep_prob;
   uint32_t drop_key0, drop_key1;
   unsigned long long drop_ctr0;
+  // FP8 inputs (q, k and v hold the exact fp16 values of x_q): per-block
+  // dequant scales [planes][blocks of 128 rows] (null: none).  S of a (query
+  // tile, key tile) pair is scaled by d_q d_k; P of a key tile by d_v / dmax,
+  // dmax the largest d_v of the slot's tiles (so the fp16 P operand neither
+  // overflows nor falls into subnormals for the tiles that matter), and dmax
+  // joins 1 / l in the epilogue
+  const float* dsq;
+  const float* dsk;
+  const float* dsv;
+  int ds_nbq, ds_nbk;
 };
 
 // Trace points: compiled only with -DFA_TRACE (a profiling build); otherwise
@@ -507,7 +517,15 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       const int ka = ext_key_hi(p, qa, q_len, kv_len) - lo_a + 1;
       const int kb = hi_b - ext_key_lo(p, qb) + 1;
       hilo = p.amask != nullptr || p.alibi || p.pse != nullptr || p.keep_thr < 256 ||
-             min(ka, kb) < 2 * kHiLoKeys;
+             p.dsq != nullptr || min(ka, kb) < 2 * kHiLoKeys;
+      if (p.dsv) {
+        // the largest d_v over the slot's key tiles
+        float dm = 0.f;
+        for (int e = lane; e < n; e += 32)
+          dm = fmaxf(dm, p.dsv[(long long)(b * p.Hkv + kvh) * p.ds_nbk + t_lo + e]);
+        for (int o = 16; o > 0; o >>= 1) dm = fmaxf(dm, __shfl_xor_sync(0xffffffffu, dm, o));
+        if (lane == 0) s_slot[7 + t] = __float_as_int(dm > 0.f ? dm : 1.f);
+      }
     } else if (live && sparse) {
       const int* lst = p.blk_idx + (long long)b * p.blk_stride_b +
                        (long long)(t ? h1 : h0) * p.blk_stride_h + (long long)qt * p.max_sel;
@@ -571,6 +589,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
     const uint16_t* prow = nullptr;
     float slope2 = 0.f;
     unsigned long long drop_row = 0;   // dropout: grid index of (b, h, row, key 0)
+    float ds_q = 1.f;                  // FP8: the query block's dequant scale
+    float ds_vmax = 1.f;               // FP8: the largest d_v of the slot's tiles
     if constexpr (kExtras) {
       ek_lo = ext_key_lo(p, qi);
       ek_hi = ext_key_hi(p, qi, q_len, kv_len);
@@ -581,6 +601,8 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         prow = p.pse + b * p.pse_sb + h * p.pse_sh + (long long)min(qi, p.Sq - 1) * p.pse_sq;
       if (p.alibi) slope2 = -exp2f(-8.f * (float)(h + 1) / (float)p.Hq) * 1.4426950408889634f;
       drop_row = ((unsigned long long)(b * p.Hq + h) * p.Sq + min(qi, p.Sq - 1)) * p.Skv;
+      if (p.dsq) ds_q = p.dsq[(long long)(b * p.Hq + h) * p.ds_nbq + qt];
+      if (p.dsv && nt > 0) ds_vmax = __int_as_float(s_slot[7 + t]);
     }
     float m = -INFINITY, l = 0.f;
     bool dead = false;   // a bounded wait expired: keep the hand-offs, skip the work
@@ -590,7 +612,13 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
       // and its dropout keep bits
       uint4 mbytes[kBN / 16];
       uint32_t dbits[kBN / 32] = {~0u, ~0u, ~0u, ~0u};
+      float ds_qk = 1.f, ds_v = 1.f;   // FP8: this key tile's d_q d_k and d_v
       if constexpr (kExtras) {
+        if (p.dsq) {
+          const long long kb = (long long)(b * p.Hkv + kvh) * p.ds_nbk + s_list[t * kMaxSel + j];
+          ds_qk = ds_q * p.dsk[kb];
+          if (p.dsv) ds_v = p.dsv[kb] / ds_vmax;
+        }
         if (mrow) {
           const int kb0 = s_list[t * kMaxSel + j] * kBN;
 #pragma unroll
@@ -665,6 +693,11 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
 #pragma unroll
       for (int i = 0; i < kBN; ++i) sv[i] = __uint_as_float(su[i]);
       if constexpr (kExtras) {
+        if (p.dsq) {
+          // FP8: the products of the exact x_q values, dequantised
+#pragma unroll
+          for (int i = 0; i < kBN; ++i) sv[i] *= ds_qk;
+        }
         // scores in log2 units, s * scale * log2(e), plus the ALiBi bias
         // -slope_h |i - j| log2(e) (exact integer distances in fp32)
         const float dq = (float)(qi - kbase);
@@ -803,8 +836,9 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
             if constexpr (kExtras) {
               // dropout: the row sum keeps every p, the P.V operand only the kept
               // ones (the 1 / keep_prob factor is applied with 1 / l)
-              a0 = ((dbits[cc] >> (2 * i)) & 1u) ? a0 : 0.f;
-              a1 = ((dbits[cc] >> (2 * i + 1)) & 1u) ? a1 : 0.f;
+              // (FP8: d_v of the key tile joins the P.V operand)
+              a0 = ((dbits[cc] >> (2 * i)) & 1u) ? a0 * ds_v : 0.f;
+              a1 = ((dbits[cc] >> (2 * i + 1)) & 1u) ? a1 * ds_v : 0.f;
             }
             ph[i] = pack_f16x2(a0, a1);
             pl[i] = pack_f16x2(a0 - f16_lo_to_f32(ph[i]), a1 - f16_hi_to_f32(ph[i]));
@@ -870,7 +904,16 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
                      : "=r"(plane)
                      : "r"(((smem_u32(smem_raw) + 1023u) & ~1023u) + SM::kMiscOff + 8 + 4 * (5 + t)));
         const bool write = qi < p.Sq;
-        const float inv_l = (l > 0.f) ? 1.f / (kExtras ? l * p.keep_prob : l) : 0.f;
+        // (extras: the dropout factor and the FP8 V scale join 1 / l; the
+        // scale is re-read here rather than held across the loop)
+        float vmax = 1.f;
+        if constexpr (kExtras) {
+          if (p.dsv && nt > 0)
+            asm volatile("ld.shared.b32 %0, [%1];"
+                         : "=f"(vmax)
+                         : "r"(((smem_u32(smem_raw) + 1023u) & ~1023u) + SM::kMiscOff + 8 + 4 * (7 + t)));
+        }
+        const float inv_l = (l > 0.f) ? (kExtras ? vmax / (l * p.keep_prob) : 1.f / l) : 0.f;
         const uint32_t tO = tmem + 256u + 128u * t + lane_off;
         const uint32_t stage = ((smem_u32(smem_raw) + 1023u) & ~1023u) + SM::kQOff + t * SM::kQBytes;
         const size_t rows_all = (size_t)p.B * p.Hq * p.Sq;

@@ -245,6 +245,35 @@ int fa_fwd_ext(const void* q, const void* k, const void* v, void* o, float* lse,
                int mask_mode, const int32_t* seqlens, const fa_extras_t* extras,
                float rescale_threshold, void* stream);
 
+/* ---- FP8 inputs ---------------------------------------------------------- */
+#define FA_FP8_E4M3  0   /* e4m3fn: 1 sign, 4 exponent (bias 7), 3 mantissa bits, max 448 */
+#define FA_FP8_E5M2  1   /* e5m2:  1 sign, 5 exponent (bias 15), 2 mantissa bits, max 57344 */
+
+/* fa_fwd_fp8 -- the forward on FP8 query / key / value with full-quantisation
+ * dequant scales ("FlashAttentionScore" operator doc, gitcode ops-transformer,
+ * parameter table: d_scale_q / d_scale_k / d_scale_v), formed as the
+ * "FlashAttentionScoreGrad" pytest framework write-up, section 5.1, gives
+ * them: per (batch, head) along S in blocks of 128 rows, the attention then
+ * runs on x_q * d_scale.
+ *   q8 [B, Hq, Sq, D], k8 [B, Hkv, Skv, D], v8 [B, Hkv, Skv, Dv]: DEVICE
+ *      bytes in fp8_format (FA_FP8_E4M3 or FA_FP8_E5M2), 16-byte aligned;
+ *   d_scale_q [B, Hq, ceil(Sq / 128)], d_scale_k [B, Hkv, ceil(Skv / 128)],
+ *      d_scale_v [B, Hkv, ceil(Skv / 128)]: DEVICE fp32;
+ *   o [B, Hq, Sq, Dv]: fp16; lse, scale, seqlens, rescale_threshold as fa_fwd;
+ *   mask_mode: FA_MASK_NONE or FA_MASK_CAUSAL (no dtype flags);
+ *   extras: NULL, or the optional terms of fa_fwd_ext (a pse tensor is fp16).
+ * D = Dv in {64, 128}, ceil(Skv / 128) <= 512.  Q and K are copied to fp16
+ * exactly (both formats lie inside fp16) and the kernel scales S of each
+ * (query block, key block) pair by d_q d_k, so the scores see the exact x_q
+ * values; V is copied as x_q * d_v rounded once to fp16.  The copies live in
+ * stream-ordered scratch.  Errors as fa_fwd_ext, plus
+ * FA_ERR_NULL for a missing scale and FA_ERR_SHAPE for an unknown format. */
+int fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* d_scale_q,
+               const float* d_scale_k, const float* d_scale_v, int fp8_format, void* o, float* lse,
+               int B, int Hq, int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,
+               const int32_t* seqlens, const fa_extras_t* extras, float rescale_threshold,
+               void* stream);
+
 /* fa_fwd that also writes the output's rounding residual
  *   o_lo = fp32(O) - O rounded to o's type,
  * itself rounded to that type, same layout as o (rows past Sq / padded heads

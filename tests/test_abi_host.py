@@ -217,3 +217,21 @@ def _ex(**kw):
 ])
 def test_ext_argument_errors(lib, ex, kw, code):
     assert call_ext(lib, ex, **kw) == code
+
+
+def call_fp8(lib, **kw):
+    a = dict(q8=P, k8=P, v8=P, d_scale_q=P, d_scale_k=P, d_scale_v=P, fp8_format=0, o=P, lse=P,
+             B=1, Hq=2, Hkv=2, Sq=128, Skv=128, D=128, Dv=128, scale=0.1, mask_mode=0,
+             seqlens=None, extras=None, rescale_threshold=0.0, stream=0)
+    a.update(kw)
+    return B.fa_fwd_fp8(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d_scale_q=None), -1), (dict(d_scale_v=None), -1), (dict(q8=None), -1),
+    (dict(fp8_format=2), -2), (dict(mask_mode=0x100), -2), (dict(mask_mode=2), -2),
+    (dict(D=96, Dv=96), -3), (dict(q8=P + 8), -4), (dict(d_scale_k=P + 2), -4),
+    (dict(extras=_ex(window=5)), -2), (dict(B=0), -2), (dict(Skv=128 * 513), -2),
+])
+def test_fp8_argument_errors(lib, kw, code):
+    assert call_fp8(lib, **kw) == code
