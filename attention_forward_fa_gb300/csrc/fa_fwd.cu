@@ -534,6 +534,8 @@ int run_tiled(const void* q, const void* k, const void* v, void* o, void* o_lo, 
     prm.units_per_q = B * Hq;
     prm.n_qpos = (prm.n_qt + 1) / 2;
   }
+  // block lists: one head's units after another (unit_of in fa_tiled.cuh)
+  prm.head_major = kv_block_idx ? 1 : 0;
   prm.scale = scale;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.threshold = rescale_threshold;

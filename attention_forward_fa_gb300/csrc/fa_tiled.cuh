@@ -79,6 +79,7 @@ struct TiledParams {
   int n_qt;         // ceil(Sq / 128)
   int units_per_q;  // units that share one query position
   int n_qpos;       // query positions (tile pairs or tiles)
+  int head_major;   // 1: units ordered by (batch, head) first (block lists)
   int kv_split;     // pieces per unit along the KV tiles (1: no split); dense only
   float* part_o;    // kv_split > 1: O / l of every piece, fp32 [kv_split][B*Hq*Sq][Dv]
   float* part_lse;  // kv_split > 1: LSE of every piece (-inf: no key) [kv_split][B*Hq*Sq]
@@ -223,6 +224,17 @@ __device__ __forceinline__ Piece piece_range(int n0, int n1, int piece, int kv_s
 }
 __device__ __forceinline__ int piece_count(int n, Piece pc) { return max(0, min(n, pc.hi) - pc.lo); }
 
+// The unit a launch index stands for.  Units are numbered heaviest query
+// position first (u / units_per_q from the last position).  Block lists give
+// every query block its own list, typically of one length, so that order buys
+// no balance there; they run one head's positions after another instead, so
+// that the CTAs in flight share a few heads' K and V in L2.
+__device__ __forceinline__ int unit_of(const TiledParams& p, int idx) {
+  if (!p.head_major) return idx;
+  const int bh = idx / p.n_qpos, qpos = idx - bh * p.n_qpos;
+  return (p.n_qpos - 1 - qpos) * p.units_per_q + bh;
+}
+
 // Number of SMs of this GPU.
 __device__ __forceinline__ uint32_t sm_count() {
   uint32_t n;
@@ -236,8 +248,8 @@ template <int D, bool kSplit>
 __device__ __noinline__ void prefetch_unit_l2(const TiledParams& p) {
   constexpr int kBoxes = D / 64;
   const int kv_split = kSplit ? p.kv_split : 1;
-  const int u = kSplit ? (int)blockIdx.x / kv_split : (int)blockIdx.x;
-  const int piece = blockIdx.x - u * kv_split;
+  const int u = unit_of(p, kSplit ? (int)blockIdx.x / kv_split : (int)blockIdx.x);
+  const int piece = kSplit ? (int)(blockIdx.x % (unsigned)kv_split) : 0;
   const int qpos = p.n_qpos - 1 - u / p.units_per_q;
   const int bh = u % p.units_per_q;
   int b, h0, h1, qt0, qt1;
@@ -402,8 +414,9 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
 
   // ---------------------------------------------------------------- unit
   const int kv_split = kSplit ? p.kv_split : 1;
-  const int u = kSplit ? (int)blockIdx.x / kv_split : (int)blockIdx.x;   // pieces of one unit are neighbours
-  const int piece = blockIdx.x - u * kv_split;
+  // pieces of one unit are neighbours
+  const int u = unit_of(p, kSplit ? (int)blockIdx.x / kv_split : (int)blockIdx.x);
+  const int piece = kSplit ? (int)(blockIdx.x % (unsigned)kv_split) : 0;
   const int qpos = p.n_qpos - 1 - u / p.units_per_q;   // heaviest query positions first
   const int bh = u % p.units_per_q;
   int b, h0, h1, qt0, qt1;
