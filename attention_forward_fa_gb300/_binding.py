@@ -287,7 +287,8 @@ def flash_attention_forward(q, k, v=None, *, scale: Optional[float] = None, caus
     next_tokens) (sparse_mode 0), bottom_right_causal (sparse_mode 3),
     atten_mask (bool or uint8 CUDA tensor [..., Sq, Skv] broadcastable to
     [B, Hq, Sq, Skv], True / nonzero = masked; its last dimension contiguous),
-    alibi (pse_type 2), pse (a bias tensor of q's type [..., Sq, Skv]
+    alibi (True or 2: pse_type 2, -slope |i - j|; 3: pse_type 3, -slope
+    sqrt|i - j|), pse (a bias tensor of q's type [..., Sq, Skv]
     broadcastable like atten_mask, last dim contiguous) with pse_type 0
     (added after the scale) or 1 (before), dropout=(keep_prob, seed, offset)
     (the Philox mask of include/fa_fwd.h)."""
@@ -333,7 +334,7 @@ def flash_attention_forward(q, k, v=None, *, scale: Optional[float] = None, caus
         if window is not None and bottom_right_causal:
             raise ValueError("window and bottom_right_causal are exclusive")
         ex.pre_tokens, ex.next_tokens = (int(window[0]), int(window[1])) if window is not None else (0, 0)
-        ex.alibi = 1 if alibi else 0
+        ex.alibi = {False: 0, True: 1, 2: 1, 3: 2}[alibi]   # True = pse_type 2
         if dropout is not None:
             ex.keep_prob, ex.seed, ex.offset = float(dropout[0]), int(dropout[1]), int(dropout[2])
         keep = None

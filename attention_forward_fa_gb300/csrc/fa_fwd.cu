@@ -409,7 +409,7 @@ int validate(const void* q, const void* k, const void* v, void* o, float* lse, i
 
 // Checks of the optional terms (fa_fwd_ext, fa_fwd_fp8); nothing is launched.
 int validate_extras(const fa_extras_t* extras, int Skv) {
-  if (extras->window < 0 || extras->window > 2 || extras->alibi < 0 || extras->alibi > 1)
+  if (extras->window < 0 || extras->window > 2 || extras->alibi < 0 || extras->alibi > 2)
     return FA_ERR_SHAPE;
   if ((Skv + fa::kBN - 1) / fa::kBN > fa::kMaxSel) return FA_ERR_SHAPE;
   // keep_prob 0 (a zero-initialised struct) or 1: no dropout

@@ -93,7 +93,8 @@ struct TiledParams {
   int pre_tokens, next_tokens; // win_mode 1 (clamped by the host to +-(Sq + Skv))
   const uint8_t* amask;        // explicit mask or null: nonzero byte = key masked
   long long am_sb, am_sh, am_sq;   // its strides (elements) over batch, head, query row
-  int alibi;                   // 1: score bias -slope_h |i - j|, slope_h = 2^(-8 (h + 1) / Hq)
+  int alibi;                   // score bias -slope_h |i - j| (1) or -slope_h sqrt|i - j| (2),
+                               // slope_h = 2^(-8 (h + 1) / Hq)
   const uint16_t* pse;         // bias tensor or null: q's type, strides below (elements)
   long long pse_sb, pse_sh, pse_sq;
   int pse_type;                // 0: s * scale + pse; 1: (s + pse) * scale
@@ -714,9 +715,13 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
         // scores in log2 units, s * scale * log2(e), plus the ALiBi bias
         // -slope_h |i - j| log2(e) (exact integer distances in fp32)
         const float dq = (float)(qi - kbase);
-        if (p.alibi) {
+        if (p.alibi == 1) {
 #pragma unroll
           for (int i = 0; i < kBN; ++i) sv[i] = fmaf(sv[i], p.scale_log2, slope2 * fabsf(dq - (float)i));
+        } else if (p.alibi == 2) {
+          // pse_type 3: -slope_h sqrt(|i - j|)
+#pragma unroll
+          for (int i = 0; i < kBN; ++i) sv[i] = fmaf(sv[i], p.scale_log2, slope2 * sqrtf(fabsf(dq - (float)i)));
         } else if (prow) {
           // the bias tensor, 32 keys (four 16-byte loads) at a time; keys
           // past Skv read none (they are masked below)

@@ -187,7 +187,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *                mask_stride_q, mask_stride_h and mask_stride_b must be
  *                multiples of 16 bytes and Skv a multiple of 16 (16-byte loads).
  *   alibi        0: none; 1: pse_type 2, the position bias -slope_h * |i - j|
- *                added after the scale, slope_h = 2^(-8 (h + 1) / Hq).
+ *                added after the scale; 2: pse_type 3, -slope_h * sqrt(|i - j|);
+ *                slope_h = 2^(-8 (h + 1) / Hq).
  *   pse          NULL, or DEVICE bias of q's type (bf16, or fp16 with
  *                FA_DTYPE_FP16), element (b, h, i, j) at
  *                pse[b*pse_stride_b + h*pse_stride_h + i*pse_stride_q + j];

@@ -200,7 +200,7 @@ def _ex(**kw):
 
 @pytest.mark.parametrize("ex,kw,code", [
     (None, {}, -1),
-    (_ex(window=3), {}, -2), (_ex(window=-1), {}, -2), (_ex(alibi=2), {}, -2),
+    (_ex(window=3), {}, -2), (_ex(window=-1), {}, -2), (_ex(alibi=3), {}, -2),
     (_ex(), dict(mask_mode=2), -2), (_ex(), dict(mask_mode=0x200, v=None), -3),
     (_ex(), dict(Skv=128 * 513), -2),
     (_ex(atten_mask=P, mask_stride_q=-16), {}, -2),

@@ -66,7 +66,7 @@ def _run(p, causal=False, window=None, bottom_right=False, mask=None, alibi=Fals
         drop = dict(drop_mask=mflat.reshape(p.B, p.Hq, p.Sq, p.Skv).astype(np.float64), keep_prob=keep)
     ex = A.Extras(**drop, atten_mask=None if mask is None else mask.astype(np.float64),
                   pse=None if pse is None else pse[1],
-                  pse_type=2 if alibi else (pse_type if pse is not None else 1),
+                  pse_type=(3 if alibi == 3 else 2) if alibi else (pse_type if pse is not None else 1),
                   sparse_mode=0 if window is not None else (3 if bottom_right else None),
                   pre_tokens=window[0] if window is not None else 2 ** 31 - 1,
                   next_tokens=window[1] if window is not None else 2 ** 31 - 1)
@@ -206,3 +206,10 @@ def test_dropout_mask_bit_exact(keep):
     kept = Or * (128 * float(np.float32(keep)))
     assert np.allclose(kept, np.round(kept)) and 0.5 < kept.mean() / keep < 1.5
     compare(O, L, Or, Lr, f"dropout bits keep {keep}")
+
+
+def test_alibi_sqrt_causal_gqa():
+    """pse_type 3: -slope_h sqrt(|i - j|), 8 heads over 2 KV heads, causal."""
+    p = W.dense(name="alibi3", B=1, Hq=8, Hkv=2, Sq=384, D=128, mask=W.MASK_CAUSAL, seed=65)
+    O, L, Or, Lr = _run(p, causal=True, alibi=3)
+    compare(O, L, Or, Lr, "alibi sqrt")
