@@ -575,6 +575,7 @@ def run_ours(args, world, rank, local):
             "peak_source": f"{peak_src} bf16_tflops (burst); the fp16 products run at the same "
                            f"nominal rate",
             "traffic": dram_traffic(args.workload), "kernel": kernel,
+            "kernel_source_hash": kernel_source_hash("topk" if args.workload == "c5" else "dense"),
             "kernel_avg_ms": kern_avg_ms}
     if conv_pass:
         roof["other_kernel"] = {"name": "fa_convert_v_kernel (bf16 -> fp16 copy of the key latent)",
