@@ -354,12 +354,29 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
-// three-input maximum, as a chain of two-input maxima (the compiler may fuse
-// it): the inline three-input max.f32 returned maxima that were not among its
-// inputs in one build of the softmax (a too-large row max, hidden by the
-// rescale since l and O scale alike, but not in the LSE's last bits)
+// three-input maximum, as a chain of two-input maxima (the compiler may fuse it)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return fmaxf(fmaxf(a, b), c);
+}
+
+// Maximum of a row of N values held in registers (N a multiple of 8): eight
+// independent chains over 16 values per step, then 8 when fewer than 16 are
+// left, so that every read stays inside the row.
+template <int N>
+__device__ __forceinline__ float row_max(const float (&sv)[N]) {
+  static_assert(N >= 8 && N % 8 == 0, "row_max takes whole groups of 8");
+  float mx[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) mx[q] = sv[q];
+#pragma unroll
+  for (int i = 8; i < N; i += 16) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (i + 16 <= N) mx[q] = fmax3(mx[q], sv[i + q], sv[i + 8 + q]);
+      else mx[q] = fmaxf(mx[q], sv[i + q]);
+    }
+  }
+  return fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7])));
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {

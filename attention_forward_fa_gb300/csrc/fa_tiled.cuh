@@ -812,14 +812,7 @@ __global__ void __launch_bounds__(kTiledThreads, 1)
           }
         }
       }
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = sv[i];
-#pragma unroll
-      for (int i = 8; i < kBN; i += 16)
-#pragma unroll
-        for (int q = 0; q < 8; ++q) mx[q] = fmax3(mx[q], sv[i + q], sv[i + 8 + q]);
-      const float mb = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7])));
+      const float mb = row_max(sv);
       const float m_new = fmaxf(m, mb);
       float m_use = m_new, alpha = 1.f;
       if (m != -INFINITY) {
