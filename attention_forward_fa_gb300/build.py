@@ -37,9 +37,13 @@ def up_to_date() -> bool:
 def build(force: bool = False, verbose: bool = False) -> str:
     if not force and up_to_date():
         return LIB
+    # the backward's products are cuBLAS fp32 GEMMs; the toolkit's library
+    # directory goes into the run path so that the library loads without it
+    # on LD_LIBRARY_PATH
+    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc_path()))), "lib64")
     cmd = [nvcc_path(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
            "-shared", "-Xcompiler", "-fPIC", "-o", LIB + ".tmp",
-           *[os.path.join(CSRC, s) for s in SOURCES]]
+           *[os.path.join(CSRC, s) for s in SOURCES], "-lcublas", "-Xlinker", "-rpath=" + cuda_lib]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)

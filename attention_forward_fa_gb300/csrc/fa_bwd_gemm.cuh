@@ -1,0 +1,94 @@
+// Elementwise kernels of the backward that materialises S, P, dP and dS per
+// (KV head, head of its group) in fp32, with every product a plain fp32 GEMM:
+//   S = Q K^T,  P = exp(scale S - LSE),  dV += P^T dO,  dP = dO V^T,
+//   dS = P * (dP - d_row),  dQ = scale dS K,  dK += scale dS^T Q
+// (the steps of the BSA PyPTO implementation notes' backward: section 3.2
+// "Core design strategies", P recomputed from the forward's LSE; section 8.4,
+// d_row = rowsum(dO * O) computed once beforehand; section 1, dV unscaled,
+// dQ and dK scaled).  A batch of the GEMMs covers `planes` KV planes p (batch
+// b = p / Hkv) at one head g of each group, i.e. query planes p * G + g.
+#pragma once
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+// bf16 or fp16 -> fp32, n8 groups of 8 elements.
+template <bool kBF16>
+__global__ void __launch_bounds__(256) fa_bwd_to_f32_kernel(const uint4* __restrict__ in,
+                                                            float4* __restrict__ out, size_t n8) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const uint4 w = in[i];
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    float f[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      f[2 * e] = kBF16 ? __uint_as_float(ww[e] << 16) : f16_lo_to_f32(ww[e]);
+      f[2 * e + 1] = kBF16 ? __uint_as_float(ww[e] & 0xFFFF0000u) : f16_hi_to_f32(ww[e]);
+    }
+    out[2 * i] = make_float4(f[0], f[1], f[2], f[3]);
+    out[2 * i + 1] = make_float4(f[4], f[5], f[6], f[7]);
+  }
+}
+
+// fp32 -> bf16 or fp16 (round to nearest even), n8 groups of 8 elements.
+template <bool kBF16>
+__global__ void __launch_bounds__(256) fa_bwd_from_f32_kernel(const float4* __restrict__ in,
+                                                              uint4* __restrict__ out, size_t n8) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const float4 a = in[2 * i], c = in[2 * i + 1];
+    out[i] = kBF16 ? make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(c.x, c.y),
+                                pack_bf16x2(c.z, c.w))
+                   : make_uint4(pack_f16x2(a.x, a.y), pack_f16x2(a.z, a.w), pack_f16x2(c.x, c.y),
+                                pack_f16x2(c.z, c.w));
+  }
+}
+
+struct BwdGemmRows {
+  const float* lse;      // [B * Hq * Sq], natural-log units (+inf on rows without keys)
+  const float* d_row;    // [B * Hq * Sq]
+  const int* seqlens;    // per-batch lengths, or null
+  int Hkv, G, Sq, Skv;
+  int causal;            // top-left: key j is seen by row i iff j <= i
+  float scale;
+  int plane0;            // first KV plane of the batch of GEMMs
+  int g;                 // head of the group
+};
+
+// P = exp(scale * s - LSE) over S in place (0 for masked keys, rows past the
+// batch's length and rows without keys).  Grid: (Sq, planes); a block walks
+// one row.
+__global__ void __launch_bounds__(256) fa_bwd_p_kernel(float* __restrict__ s, BwdGemmRows r) {
+  const int i = blockIdx.x;
+  const int z = blockIdx.y;
+  const int p = r.plane0 + z;
+  const int b = p / r.Hkv;
+  const int q_len = r.seqlens ? min(r.seqlens[b], r.Sq) : r.Sq;
+  const int kv_len = r.seqlens ? min(r.seqlens[b], r.Skv) : r.Skv;
+  const float lse = r.lse[(size_t)(p * r.G + r.g) * r.Sq + i];
+  const bool row_ok = i < q_len && lse != INFINITY;
+  int lim = row_ok ? kv_len : 0;                 // keys j < lim are seen
+  if (r.causal) lim = min(lim, i + 1);
+  float* row = s + ((size_t)z * r.Sq + i) * r.Skv;
+  for (int j = threadIdx.x; j < r.Skv; j += blockDim.x)
+    row[j] = j < lim ? expf(fmaf(row[j], r.scale, -lse)) : 0.f;
+}
+
+// dS = P * (dP - d_row) over dP in place; exactly 0 where P is (masked keys,
+// padded rows: whatever dO holds there cannot reach dQ, dK or dV).
+// Grid: (Sq, planes).
+__global__ void __launch_bounds__(256) fa_bwd_ds_kernel(const float* __restrict__ pm,
+                                                        float* __restrict__ dp, BwdGemmRows r) {
+  const int i = blockIdx.x;
+  const int z = blockIdx.y;
+  const int p = r.plane0 + z;
+  const float d = r.d_row[(size_t)(p * r.G + r.g) * r.Sq + i];
+  const size_t base = ((size_t)z * r.Sq + i) * r.Skv;
+  for (int j = threadIdx.x; j < r.Skv; j += blockDim.x) {
+    const float pv = pm[base + j];
+    dp[base + j] = pv != 0.f ? pv * (dp[base + j] - d) : 0.f;
+  }
+}
+
+}  // namespace fa

@@ -16,6 +16,9 @@
 #include "fa_tiled.cuh"
 #include "fa_mla.cuh"
 #include "fa_bwd.cuh"
+#include "fa_bwd_gemm.cuh"
+
+#include <cublas_v2.h>
 
 namespace {
 
@@ -690,25 +693,41 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, void* o_lo, f
 }
 
 // ------------------------------------------------------------------ backward
-template <bool BF16>
-int launch_bwd(const fa::BwdParams& prm, int grid_kv, int grid_q, cudaStream_t st) {
-  auto k_kv = fa::fa_bwd_dkdv_kernel<BF16>;
-  auto k_q = fa::fa_bwd_dq_kernel<BF16>;
-  constexpr int smem = fa::BwdSmem::kAlloc;
-  static std::once_flag once[64];
-  static cudaError_t attr_err[64];
+// S and dP of one batch of the backward's GEMMs are held in fp32; a batch
+// covers as many KV planes as fit in this many bytes (at least one).
+constexpr size_t kBwdGemmBytes = size_t(1) << 30;
+
+// One cuBLAS handle per device, created on first use: fp32 products only
+// (pedantic math: no reduced-precision tensor-core paths) and no workspace,
+// so that calls on different streams share nothing on the device.  The mutex
+// covers a whole call's enqueue (the handle's stream is set per call).
+std::mutex g_blas_mu;
+cublasHandle_t blas_handle() {
+  static cublasHandle_t hs[64];
   int dev = 0;
-  cudaGetDevice(&dev);
-  std::call_once(once[dev & 63], [&] {
-    cudaError_t e = cudaFuncSetAttribute(k_kv, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_q, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    attr_err[dev & 63] = e;
-  });
-  if (attr_err[dev & 63] != cudaSuccess) return cuda_fail(attr_err[dev & 63]);
-  if (grid_kv > 0) k_kv<<<grid_kv, fa::kBwdThreads, smem, st>>>(prm);
-  if (grid_q > 0) k_q<<<grid_q, fa::kBwdThreads, smem, st>>>(prm);
-  const cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!hs[dev]) {
+    cublasHandle_t h = nullptr;
+    if (cublasCreate(&h) != CUBLAS_STATUS_SUCCESS) return nullptr;
+    if (cublasSetMathMode(h, CUBLAS_PEDANTIC_MATH) != CUBLAS_STATUS_SUCCESS ||
+        cublasSetWorkspace(h, nullptr, 0) != CUBLAS_STATUS_SUCCESS) {
+      cublasDestroy(h);
+      return nullptr;
+    }
+    hs[dev] = h;
+  }
+  return hs[dev];
+}
+
+// Row-major C[M, N] = alpha op(A) op(B) + beta C over `batch` strided
+// matrices (leading dimensions and strides in elements), as the column-major
+// product C^T = op(B)^T op(A)^T.
+bool gemm_rm(cublasHandle_t h, bool ta, bool tb, int M, int N, int K, float alpha, const float* A,
+             int lda, long long sA, const float* Bm, int ldb, long long sB, float beta, float* C,
+             int ldc, long long sC, int batch) {
+  return cublasSgemmStridedBatched(h, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N,
+                                   N, M, K, &alpha, Bm, ldb, sB, A, lda, sA, &beta, C, ldc, sC,
+                                   batch) == CUBLAS_STATUS_SUCCESS;
 }
 
 int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* o_lo,
@@ -735,72 +754,109 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* status = status_ptr();
   if (!status) return cuda_fail(cudaGetLastError());
+  std::lock_guard<std::mutex> lock(g_blas_mu);
+  cublasHandle_t h = blas_handle();
+  if (!h || cublasSetStream(h, st) != CUBLAS_STATUS_SUCCESS) return cuda_fail(cudaErrorUnknown);
 
-  // scratch: d_row, and fp16 copies of bf16 Q, K, V, dO (every product runs on fp16)
+  // Stream-ordered scratch: d_row; fp32 copies of Q, dO, K, V; fp32 dQ, dK, dV;
+  // S / P and dP / dS of one batch of KV planes.
+  const int G = Hq / Hkv;
+  const int planes = B * Hkv;
   const size_t nq = (size_t)B * Hq * Sq * 128, nk = (size_t)B * Hkv * Skv * 128;
   const size_t rows = (size_t)B * Hq * Sq;
-  const size_t drow_bytes = (rows * 4 + 255) & ~size_t(255);
-  const size_t bytes = drow_bytes + (fp16 ? 0 : 2 * (nq + nk) * 2);
-  uint8_t* scratch = static_cast<uint8_t*>(scratch_alloc(bytes, st));
+  const size_t plane_mat = (size_t)Sq * Skv;
+  const int chunk = (int)std::min<size_t>(
+      {(size_t)planes, (size_t)65535, std::max<size_t>(1, kBwdGemmBytes / (2 * plane_mat * 4))});
+  auto al = [](size_t b) { return (b + 255) & ~size_t(255); };
+  const size_t b_row = al(rows * 4), b_q = al(nq * 4), b_k = al(nk * 4);
+  const size_t b_m = al((size_t)chunk * plane_mat * 4);
+  uint8_t* scratch = static_cast<uint8_t*>(scratch_alloc(b_row + 3 * b_q + 4 * b_k + 2 * b_m, st));
   if (!scratch) return cuda_fail(cudaGetLastError());
-  float* d_row = reinterpret_cast<float*>(scratch);
-  const void *q16 = q, *k16 = k, *v16 = v, *do16 = dout;
+  uint8_t* c = scratch;
+  float* d_row = reinterpret_cast<float*>(c);
+  c += b_row;
+  float* q32 = reinterpret_cast<float*>(c);
+  float* do32 = reinterpret_cast<float*>(c + b_q);
+  float* dq32 = reinterpret_cast<float*>(c + 2 * b_q);
+  c += 3 * b_q;
+  float* k32 = reinterpret_cast<float*>(c);
+  float* v32 = reinterpret_cast<float*>(c + b_k);
+  float* dk32 = reinterpret_cast<float*>(c + 2 * b_k);
+  float* dv32 = reinterpret_cast<float*>(c + 3 * b_k);
+  c += 4 * b_k;
+  float* sm = reinterpret_cast<float*>(c);
+  float* dpm = reinterpret_cast<float*>(c + b_m);
+
   int rc = FA_OK;
-  if (!fp16) {
-    uint8_t* c = scratch + drow_bytes;
-    q16 = c;
-    do16 = c + nq * 2;
-    k16 = c + 2 * nq * 2;
-    v16 = c + 2 * nq * 2 + nk * 2;
-    rc = convert_v(q, const_cast<void*>(q16), nq, status, st);
-    if (rc == FA_OK) rc = convert_v(dout, const_cast<void*>(do16), nq, status, st);
-    if (rc == FA_OK) rc = convert_v(k, const_cast<void*>(k16), nk, status, st);
-    if (rc == FA_OK) rc = convert_v(v, const_cast<void*>(v16), nk, status, st);
+  auto launched = [&]() {
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess && rc == FA_OK) rc = cuda_fail(e);
+    return rc == FA_OK;
+  };
+  // fp32 copies (every row is a multiple of 8 elements: D = 128)
+  auto to32 = [&](const void* in, float* out, size_t n) {
+    const size_t n8 = n / 8;
+    const unsigned blocks = (unsigned)std::min<size_t>((n8 + 255) / 256, 4096);
+    if (fp16) fa::fa_bwd_to_f32_kernel<false><<<blocks, 256, 0, st>>>(static_cast<const uint4*>(in), reinterpret_cast<float4*>(out), n8);
+    else fa::fa_bwd_to_f32_kernel<true><<<blocks, 256, 0, st>>>(static_cast<const uint4*>(in), reinterpret_cast<float4*>(out), n8);
+    return launched();
+  };
+  auto from32 = [&](const float* in, void* out, size_t n) {
+    const size_t n8 = n / 8;
+    const unsigned blocks = (unsigned)std::min<size_t>((n8 + 255) / 256, 4096);
+    if (fp16) fa::fa_bwd_from_f32_kernel<false><<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(in), static_cast<uint4*>(out), n8);
+    else fa::fa_bwd_from_f32_kernel<true><<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(in), static_cast<uint4*>(out), n8);
+    return launched();
+  };
+  bool ok = to32(q, q32, nq) && to32(dout, do32, nq) && to32(k, k32, nk) && to32(v, v32, nk);
+  if (ok) {
+    const cudaError_t e1 = cudaMemsetAsync(dk32, 0, nk * 4, st);
+    const cudaError_t e2 = e1 == cudaSuccess ? cudaMemsetAsync(dv32, 0, nk * 4, st) : e1;
+    if (e2 != cudaSuccess) {
+      rc = cuda_fail(e2);
+      ok = false;
+    }
   }
-  if (rc == FA_OK) {
+  if (ok) {
+    // d_row = rowsum(dO * (O + o_lo)) from the forward's output as given
     const unsigned blocks = (unsigned)((rows + 7) / 8);
     const auto* o16 = static_cast<const uint16_t*>(o);
     const auto* lo16 = static_cast<const uint16_t*>(o_lo);
     const auto* d16 = static_cast<const uint16_t*>(dout);
     if (fp16) fa::fa_bwd_drow_kernel<false><<<blocks, 256, 0, st>>>(o16, lo16, d16, d_row, (long long)rows);
     else fa::fa_bwd_drow_kernel<true><<<blocks, 256, 0, st>>>(o16, lo16, d16, d_row, (long long)rows);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) rc = cuda_fail(e);
+    ok = launched();
   }
-  if (rc == FA_OK) {
-    fa::BwdParams prm;
-    std::memset(&prm, 0, sizeof(prm));
-    if (!encode_3d(&prm.tm_q, q16, true, 128, Sq, (uint64_t)B * Hq, 128) ||
-        !encode_3d(&prm.tm_do, do16, true, 128, Sq, (uint64_t)B * Hq, 128) ||
-        !encode_3d(&prm.tm_k, k16, true, 128, Skv, (uint64_t)B * Hkv, 128) ||
-        !encode_3d(&prm.tm_v, v16, true, 128, Skv, (uint64_t)B * Hkv, 128)) {
-      rc = cuda_fail(cudaErrorInvalidValue);
-    } else {
-      prm.lse = lse;
-      prm.d_row = d_row;
-      prm.dq = dq;
-      prm.dk = dk;
-      prm.dv = dv;
-      prm.seqlens = seqlens;
-      prm.B = B;
-      prm.Hq = Hq;
-      prm.Hkv = Hkv;
-      prm.Sq = Sq;
-      prm.Skv = Skv;
-      prm.G = Hq / Hkv;
-      prm.n_qt = (Sq + 127) / 128;
-      prm.n_kt = (Skv + 127) / 128;
-      prm.causal = mask == FA_MASK_CAUSAL;
-      prm.scale = scale;
-      prm.scale_log2 = scale * 1.4426950408889634f;
-      prm.timeout_ns = g_timeout_ns.load();
-      prm.status = status;
-      const long long grid_kv = (long long)prm.n_kt * B * Hkv, grid_q = (long long)prm.n_qt * B * Hq;
-      if (grid_kv > 0x7FFFFFFF || grid_q > 0x7FFFFFFF) rc = FA_ERR_SHAPE;
-      else rc = fp16 ? launch_bwd<false>(prm, (int)grid_kv, (int)grid_q, st)
-                     : launch_bwd<true>(prm, (int)grid_kv, (int)grid_q, st);
+  // per head g of every group and batch of KV planes [p0, p0 + np): the query
+  // planes are p * G + g, so Q, dO and dQ advance by G planes per KV plane
+  const long long sQ = (long long)G * Sq * 128, sK = (long long)Skv * 128, sM = (long long)plane_mat;
+  for (int g = 0; ok && g < G; ++g) {
+    for (int p0 = 0; ok && p0 < planes; p0 += chunk) {
+      const int np = std::min(chunk, planes - p0);
+      const long long qo = ((long long)p0 * G + g) * Sq * 128, ko = (long long)p0 * Skv * 128;
+      fa::BwdGemmRows r{lse, d_row, seqlens, Hkv, G, Sq, Skv, mask == FA_MASK_CAUSAL, scale, p0, g};
+      ok = gemm_rm(h, false, true, Sq, Skv, 128, 1.f, q32 + qo, 128, sQ, k32 + ko, 128, sK, 0.f, sm,
+                   Skv, sM, np);                                              // S = Q K^T
+      if (ok) {
+        fa::fa_bwd_p_kernel<<<dim3(Sq, np), 256, 0, st>>>(sm, r);           // P
+        ok = launched();
+      }
+      if (ok) ok = gemm_rm(h, true, false, Skv, 128, Sq, 1.f, sm, Skv, sM, do32 + qo, 128, sQ, 1.f,
+                           dv32 + ko, 128, sK, np);                           // dV += P^T dO
+      if (ok) ok = gemm_rm(h, false, true, Sq, Skv, 128, 1.f, do32 + qo, 128, sQ, v32 + ko, 128, sK,
+                           0.f, dpm, Skv, sM, np);                            // dP = dO V^T
+      if (ok) {
+        fa::fa_bwd_ds_kernel<<<dim3(Sq, np), 256, 0, st>>>(sm, dpm, r);     // dS
+        ok = launched();
+      }
+      if (ok) ok = gemm_rm(h, false, false, Sq, 128, Skv, scale, dpm, Skv, sM, k32 + ko, 128, sK,
+                           0.f, dq32 + qo, 128, sQ, np);                      // dQ = scale dS K
+      if (ok) ok = gemm_rm(h, true, false, Skv, 128, Sq, scale, dpm, Skv, sM, q32 + qo, 128, sQ,
+                           1.f, dk32 + ko, 128, sK, np);                      // dK += scale dS^T Q
+      if (!ok && rc == FA_OK) rc = cuda_fail(cudaErrorUnknown);
     }
   }
+  if (ok) ok = from32(dq32, dq, nq) && from32(dk32, dk, nk) && from32(dv32, dv, nk);
   cudaFreeAsync(scratch, st);
   return rc;
 }

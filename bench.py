@@ -450,6 +450,69 @@ def other_workloads(args, dev, dist, world, local, peak):
     return out
 
 
+def backward_workload(args, dev, dist, world, local, peak):
+    """fa_bwd on the benchmark's workload (B2 H16 S2048 D128 causal, bf16),
+    after one fa_fwd_o_lo call that provides o, its residual and the LSE, with
+    a seeded upstream gradient: K calls between a barrier + synchronize, CUDA
+    events around them, clocks sampled from an untimed soak on.  Reported
+    against the backward's algorithmic work, 2.5x the forward's (S, dP, dV,
+    dQ, dK: 2 D + 4 Dv ... = 1280 flops per unmasked pair at D = Dv = 128)."""
+    import numpy as np
+    import torch
+    import attention_forward_fa_gb300 as fa
+    from attention_forward_fa_gb300 import workloads as W
+    p = workload_problem("c2")
+    flops = 2.5 * W.algorithmic_flops(p)
+    tdt = torch.bfloat16 if p.dtype == "bf16" else torch.float16
+    to = lambda bits: torch.from_numpy(bits.view(np.int16).copy()).to(dev).view(tdt)  # noqa: E731
+    q, k, v = to(p.q_bits), to(p.k_bits), to(p.v_bits)
+    dout = to(W.upstream_grad((p.B, p.Hq, p.Sq, p.Dv), p.dtype, seed=2001))
+    causal = p.mask == W.MASK_CAUSAL
+    o, lse, o_lo = fa.flash_attention_forward(q, k, v, scale=p.scale, causal=causal, o_lo=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def call():
+        fa.flash_attention_backward(q, k, v, o, lse, dout, o_lo=o_lo, scale=p.scale, causal=causal,
+                                    dq=dq, dk=dk, dv=dv)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else local)
+    sampler.start()
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < args.workload_soak:
+        call()
+        torch.cuda.synchronize()
+    steps = max(3, min(args.workload_steps, 20))
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    status = fa.fa_check_status()
+    if status != 0:
+        raise RuntimeError("device status after the backward: " + fa.fa_strerror(status))
+    ms = max_over_ranks(dist, [e0.elapsed_time(e1) / steps], dev)[0]
+    achieved = flops / (ms * 1e-3) / 1e12
+    cfg = workload_desc(p, "c2")
+    cfg["pass"] = "backward: dQ, dK, dV from q, k, v, o + o_lo, LSE and a seeded N(0,1) upstream gradient"
+    return {"config": cfg,
+            "algorithmic_gflop": flops / 1e9, "ms_per_call": ms,
+            "tflops": whole_job_tflops(world, flops, ms), "frac": achieved / peak, "steps": steps,
+            "kernel": "fa_bwd: fp32 copies, d_row, per (KV head, group head) batch fp32 cuBLAS GEMMs "
+                      "for S, dV, dP, dQ, dK with P and dS kernels between them",
+            "timing": "eager, events around the K calls", "clocks": clocks}
+
+
 def run_ours(args, world, rank, local):
     import torch
     import attention_forward_fa_gb300 as fa
@@ -556,6 +619,7 @@ def run_ours(args, world, rank, local):
     others = None
     if args.workload == "c2" and not args.no_workloads:
         others = other_workloads(args, dev, dist, world, local, peak)
+        others["bwd_c2"] = backward_workload(args, dev, dist, world, local, peak)
     if rank != 0:
         if dist:
             dist.destroy_process_group()

@@ -303,9 +303,13 @@ int fa_fwd_o_lo(const void* q, const void* k, const void* v, void* o, void* o_lo
  * on causal problems dQ / dK then lose about an order of magnitude in
  * accuracy.  mask_mode: FA_MASK_NONE or FA_MASK_CAUSAL (top-left), plus
  * FA_DTYPE_FP16; seqlens as fa_fwd.  D = Dv = 128 only (FA_ERR_UNSUPPORTED
- * otherwise).  Rows past a batch's length get zero gradients.  Stream-ordered
- * scratch: d_row, and fp16 copies of bf16 inputs (FA_ERR_RANGE, reported by
- * fa_check_status, when a bf16 value exceeds the fp16 range).  Returns FA_OK
+ * otherwise).  Rows past a batch's length get zero gradients.  S, P, dP and
+ * dS are materialised in fp32 for a batch of (KV head, head of its group)
+ * planes at a time and every product is an fp32 cuBLAS GEMM.  Stream-ordered
+ * scratch (cudaMallocAsync, freed on `stream`): d_row; fp32 copies of q, k,
+ * v, dout; fp32 dq, dk, dv; and 2 * 4 * Sq * Skv bytes per plane of a batch,
+ * batches of up to 1 GiB (at least one plane).  Calls from several host
+ * threads serialise their enqueueing on one lock per process.  Returns FA_OK
  * or a negative FA_ERR_* code (nothing launched on an argument error). */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* o_lo,
            const float* lse, const void* dout, void* dq, void* dk, void* dv, int B, int Hq,
