@@ -1,5 +1,7 @@
 // Elementwise kernels of the backward that materialises S, P, dP and dS per
-// (KV head, head of its group) in fp32, with every product a plain fp32 GEMM:
+// (KV head, head of its group), with every product a plain library GEMM (bf16
+// tensor-core products with P and dS as bf16 hi + lo pairs for bf16 inputs,
+// fp32 products for fp16 inputs), accumulated in fp32:
 //   S = Q K^T,  P = exp(scale S - LSE),  dV += P^T dO,  dP = dO V^T,
 //   dS = P * (dP - d_row),  dQ = scale dS K,  dK += scale dS^T Q
 // (the steps of the BSA PyPTO implementation notes' backward: section 3.2
@@ -88,6 +90,55 @@ __global__ void __launch_bounds__(256) fa_bwd_ds_kernel(const float* __restrict_
   for (int j = threadIdx.x; j < r.Skv; j += blockDim.x) {
     const float pv = pm[base + j];
     dp[base + j] = pv != 0.f ? pv * (dp[base + j] - d) : 0.f;
+  }
+}
+
+// bf16 operands of the tensor-core products: P = exp(scale * s - LSE) (as
+// fa_bwd_p_kernel) split into hi = bf16(P) and lo = bf16(P - hi), written to
+// two bf16 matrices of the batch's layout.  Grid: (Sq, planes).
+__global__ void __launch_bounds__(256) fa_bwd_p_hilo_kernel(const float* __restrict__ s,
+                                                            uint16_t* __restrict__ ph,
+                                                            uint16_t* __restrict__ pl,
+                                                            BwdGemmRows r) {
+  const int i = blockIdx.x;
+  const int z = blockIdx.y;
+  const int p = r.plane0 + z;
+  const int b = p / r.Hkv;
+  const int q_len = r.seqlens ? min(r.seqlens[b], r.Sq) : r.Sq;
+  const int kv_len = r.seqlens ? min(r.seqlens[b], r.Skv) : r.Skv;
+  const float lse = r.lse[(size_t)(p * r.G + r.g) * r.Sq + i];
+  const bool row_ok = i < q_len && lse != INFINITY;
+  int lim = row_ok ? kv_len : 0;
+  if (r.causal) lim = min(lim, i + 1);
+  const size_t base = ((size_t)z * r.Sq + i) * r.Skv;
+  for (int j = threadIdx.x; j < r.Skv; j += blockDim.x) {
+    const float x = j < lim ? expf(fmaf(s[base + j], r.scale, -lse)) : 0.f;
+    const uint32_t h2 = pack_bf16x2(x, 0.f);
+    const float hf = __uint_as_float(h2 << 16);
+    ph[base + j] = (uint16_t)(h2 & 0xFFFFu);
+    pl[base + j] = (uint16_t)(pack_bf16x2(x - hf, 0.f) & 0xFFFFu);
+  }
+}
+
+// dS = P * (dP - d_row) with P = hi + lo read from the bf16 pair, written back
+// over the pair as bf16 hi and lo; exactly 0 where P is.  Grid: (Sq, planes).
+__global__ void __launch_bounds__(256) fa_bwd_ds_hilo_kernel(uint16_t* __restrict__ ph,
+                                                             uint16_t* __restrict__ pl,
+                                                             const float* __restrict__ dp,
+                                                             BwdGemmRows r) {
+  const int i = blockIdx.x;
+  const int z = blockIdx.y;
+  const int p = r.plane0 + z;
+  const float d = r.d_row[(size_t)(p * r.G + r.g) * r.Sq + i];
+  const size_t base = ((size_t)z * r.Sq + i) * r.Skv;
+  for (int j = threadIdx.x; j < r.Skv; j += blockDim.x) {
+    const float pv = __uint_as_float((uint32_t)ph[base + j] << 16) +
+                     __uint_as_float((uint32_t)pl[base + j] << 16);
+    const float x = pv != 0.f ? pv * (dp[base + j] - d) : 0.f;
+    const uint32_t h2 = pack_bf16x2(x, 0.f);
+    const float hf = __uint_as_float(h2 << 16);
+    ph[base + j] = (uint16_t)(h2 & 0xFFFFu);
+    pl[base + j] = (uint16_t)(pack_bf16x2(x - hf, 0.f) & 0xFFFFu);
   }
 }
 

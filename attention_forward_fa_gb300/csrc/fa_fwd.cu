@@ -729,6 +729,15 @@ bool gemm_rm(cublasHandle_t h, bool ta, bool tb, int M, int N, int K, float alph
                                    N, M, K, &alpha, Bm, ldb, sB, A, lda, sA, &beta, C, ldc, sC,
                                    batch) == CUBLAS_STATUS_SUCCESS;
 }
+// The same with bf16 A and B (tensor-core products, exact in fp32) and fp32 C.
+bool gemm_rm_bf16(cublasHandle_t h, bool ta, bool tb, int M, int N, int K, float alpha,
+                  const uint16_t* A, int lda, long long sA, const uint16_t* Bm, int ldb,
+                  long long sB, float beta, float* C, int ldc, long long sC, int batch) {
+  return cublasGemmStridedBatchedEx(h, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N,
+                                    N, M, K, &alpha, Bm, CUDA_R_16BF, ldb, sB, A, CUDA_R_16BF, lda,
+                                    sA, &beta, C, CUDA_R_32F, ldc, sC, batch, CUBLAS_COMPUTE_32F,
+                                    CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS;
+}
 
 int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* o_lo,
              const float* lse, const void* dout, void* dq, void* dk, void* dv, int B, int Hq,
@@ -758,8 +767,18 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   cublasHandle_t h = blas_handle();
   if (!h || cublasSetStream(h, st) != CUBLAS_STATUS_SUCCESS) return cuda_fail(cudaErrorUnknown);
 
-  // Stream-ordered scratch: d_row; fp32 copies of Q, dO, K, V; fp32 dQ, dK, dV;
-  // S / P and dP / dS of one batch of KV planes.
+  // bf16 inputs: S and dP straight from them on the tensor cores, P and dS as
+  // bf16 hi + lo pairs (about 16 significant bits) for dV, dQ and dK.  fp16
+  // inputs: fp32 copies and fp32 products throughout (an fp16 hi part could
+  // overflow on a large dS).  Both accumulate dQ, dK, dV in fp32.
+  const bool tc = !fp16;
+  const cublasMath_t math = tc ? cublasMath_t(CUBLAS_DEFAULT_MATH | CUBLAS_MATH_DISALLOW_REDUCED_PRECISION_REDUCTION)
+                               : CUBLAS_PEDANTIC_MATH;
+  if (cublasSetMathMode(h, math) != CUBLAS_STATUS_SUCCESS) return cuda_fail(cudaErrorUnknown);
+
+  // Stream-ordered scratch: d_row; fp32 dQ, dK, dV; S (then dP) of one batch
+  // of KV planes; with bf16 inputs the bf16 hi / lo of P (then dS), else fp32
+  // copies of Q, dO, K, V and a second fp32 matrix for P / dS.
   const int G = Hq / Hkv;
   const int planes = B * Hkv;
   const size_t nq = (size_t)B * Hq * Sq * 128, nk = (size_t)B * Hkv * Skv * 128;
@@ -769,23 +788,35 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
       {(size_t)planes, (size_t)65535, std::max<size_t>(1, kBwdGemmBytes / (2 * plane_mat * 4))});
   auto al = [](size_t b) { return (b + 255) & ~size_t(255); };
   const size_t b_row = al(rows * 4), b_q = al(nq * 4), b_k = al(nk * 4);
-  const size_t b_m = al((size_t)chunk * plane_mat * 4);
-  uint8_t* scratch = static_cast<uint8_t*>(scratch_alloc(b_row + 3 * b_q + 4 * b_k + 2 * b_m, st));
+  const size_t b_m = al((size_t)chunk * plane_mat * 4), b_h = al((size_t)chunk * plane_mat * 2);
+  const size_t bytes = b_row + b_q + 2 * b_k + b_m + (tc ? 2 * b_h : 2 * b_q + 2 * b_k + b_m);
+  uint8_t* scratch = static_cast<uint8_t*>(scratch_alloc(bytes, st));
   if (!scratch) return cuda_fail(cudaGetLastError());
   uint8_t* c = scratch;
   float* d_row = reinterpret_cast<float*>(c);
   c += b_row;
-  float* q32 = reinterpret_cast<float*>(c);
-  float* do32 = reinterpret_cast<float*>(c + b_q);
-  float* dq32 = reinterpret_cast<float*>(c + 2 * b_q);
-  c += 3 * b_q;
-  float* k32 = reinterpret_cast<float*>(c);
-  float* v32 = reinterpret_cast<float*>(c + b_k);
-  float* dk32 = reinterpret_cast<float*>(c + 2 * b_k);
-  float* dv32 = reinterpret_cast<float*>(c + 3 * b_k);
-  c += 4 * b_k;
+  float* dq32 = reinterpret_cast<float*>(c);
+  c += b_q;
+  float* dk32 = reinterpret_cast<float*>(c);
+  float* dv32 = reinterpret_cast<float*>(c + b_k);
+  c += 2 * b_k;
   float* sm = reinterpret_cast<float*>(c);
-  float* dpm = reinterpret_cast<float*>(c + b_m);
+  c += b_m;
+  uint16_t* ph = nullptr;
+  uint16_t* pl = nullptr;
+  float *q32 = nullptr, *do32 = nullptr, *k32 = nullptr, *v32 = nullptr, *dpm = nullptr;
+  if (tc) {
+    ph = reinterpret_cast<uint16_t*>(c);
+    pl = reinterpret_cast<uint16_t*>(c + b_h);
+  } else {
+    q32 = reinterpret_cast<float*>(c);
+    do32 = reinterpret_cast<float*>(c + b_q);
+    c += 2 * b_q;
+    k32 = reinterpret_cast<float*>(c);
+    v32 = reinterpret_cast<float*>(c + b_k);
+    c += 2 * b_k;
+    dpm = reinterpret_cast<float*>(c);
+  }
 
   int rc = FA_OK;
   auto launched = [&]() {
@@ -797,8 +828,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   auto to32 = [&](const void* in, float* out, size_t n) {
     const size_t n8 = n / 8;
     const unsigned blocks = (unsigned)std::min<size_t>((n8 + 255) / 256, 4096);
-    if (fp16) fa::fa_bwd_to_f32_kernel<false><<<blocks, 256, 0, st>>>(static_cast<const uint4*>(in), reinterpret_cast<float4*>(out), n8);
-    else fa::fa_bwd_to_f32_kernel<true><<<blocks, 256, 0, st>>>(static_cast<const uint4*>(in), reinterpret_cast<float4*>(out), n8);
+    fa::fa_bwd_to_f32_kernel<false><<<blocks, 256, 0, st>>>(static_cast<const uint4*>(in), reinterpret_cast<float4*>(out), n8);
     return launched();
   };
   auto from32 = [&](const float* in, void* out, size_t n) {
@@ -808,7 +838,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
     else fa::fa_bwd_from_f32_kernel<true><<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(in), static_cast<uint4*>(out), n8);
     return launched();
   };
-  bool ok = to32(q, q32, nq) && to32(dout, do32, nq) && to32(k, k32, nk) && to32(v, v32, nk);
+  bool ok = tc || (to32(q, q32, nq) && to32(dout, do32, nq) && to32(k, k32, nk) && to32(v, v32, nk));
   if (ok) {
     const cudaError_t e1 = cudaMemsetAsync(dk32, 0, nk * 4, st);
     const cudaError_t e2 = e1 == cudaSuccess ? cudaMemsetAsync(dv32, 0, nk * 4, st) : e1;
@@ -830,29 +860,58 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   // per head g of every group and batch of KV planes [p0, p0 + np): the query
   // planes are p * G + g, so Q, dO and dQ advance by G planes per KV plane
   const long long sQ = (long long)G * Sq * 128, sK = (long long)Skv * 128, sM = (long long)plane_mat;
+  const auto* q16 = static_cast<const uint16_t*>(q);
+  const auto* k16 = static_cast<const uint16_t*>(k);
+  const auto* v16 = static_cast<const uint16_t*>(v);
+  const auto* do16 = static_cast<const uint16_t*>(dout);
   for (int g = 0; ok && g < G; ++g) {
     for (int p0 = 0; ok && p0 < planes; p0 += chunk) {
       const int np = std::min(chunk, planes - p0);
       const long long qo = ((long long)p0 * G + g) * Sq * 128, ko = (long long)p0 * Skv * 128;
       fa::BwdGemmRows r{lse, d_row, seqlens, Hkv, G, Sq, Skv, mask == FA_MASK_CAUSAL, scale, p0, g};
-      ok = gemm_rm(h, false, true, Sq, Skv, 128, 1.f, q32 + qo, 128, sQ, k32 + ko, 128, sK, 0.f, sm,
-                   Skv, sM, np);                                              // S = Q K^T
-      if (ok) {
-        fa::fa_bwd_p_kernel<<<dim3(Sq, np), 256, 0, st>>>(sm, r);           // P
-        ok = launched();
+      const dim3 eg(Sq, np);
+      if (tc) {
+        ok = gemm_rm_bf16(h, false, true, Sq, Skv, 128, 1.f, q16 + qo, 128, sQ, k16 + ko, 128, sK,
+                          0.f, sm, Skv, sM, np);                              // S = Q K^T
+        if (ok) {
+          fa::fa_bwd_p_hilo_kernel<<<eg, 256, 0, st>>>(sm, ph, pl, r);        // P = hi + lo
+          ok = launched();
+        }
+        for (int part = 0; ok && part < 2; ++part)                           // dV += P^T dO
+          ok = gemm_rm_bf16(h, true, false, Skv, 128, Sq, 1.f, part ? pl : ph, Skv, sM, do16 + qo,
+                            128, sQ, 1.f, dv32 + ko, 128, sK, np);
+        if (ok) ok = gemm_rm_bf16(h, false, true, Sq, Skv, 128, 1.f, do16 + qo, 128, sQ, v16 + ko,
+                                  128, sK, 0.f, sm, Skv, sM, np);             // dP = dO V^T
+        if (ok) {
+          fa::fa_bwd_ds_hilo_kernel<<<eg, 256, 0, st>>>(ph, pl, sm, r);       // dS = hi + lo
+          ok = launched();
+        }
+        for (int part = 0; ok && part < 2; ++part)                           // dQ = scale dS K
+          ok = gemm_rm_bf16(h, false, false, Sq, 128, Skv, scale, part ? pl : ph, Skv, sM,
+                            k16 + ko, 128, sK, part ? 1.f : 0.f, dq32 + qo, 128, sQ, np);
+        for (int part = 0; ok && part < 2; ++part)                           // dK += scale dS^T Q
+          ok = gemm_rm_bf16(h, true, false, Skv, 128, Sq, scale, part ? pl : ph, Skv, sM,
+                            q16 + qo, 128, sQ, 1.f, dk32 + ko, 128, sK, np);
+      } else {
+        ok = gemm_rm(h, false, true, Sq, Skv, 128, 1.f, q32 + qo, 128, sQ, k32 + ko, 128, sK, 0.f,
+                     sm, Skv, sM, np);                                        // S = Q K^T
+        if (ok) {
+          fa::fa_bwd_p_kernel<<<eg, 256, 0, st>>>(sm, r);                     // P
+          ok = launched();
+        }
+        if (ok) ok = gemm_rm(h, true, false, Skv, 128, Sq, 1.f, sm, Skv, sM, do32 + qo, 128, sQ,
+                             1.f, dv32 + ko, 128, sK, np);                    // dV += P^T dO
+        if (ok) ok = gemm_rm(h, false, true, Sq, Skv, 128, 1.f, do32 + qo, 128, sQ, v32 + ko, 128,
+                             sK, 0.f, dpm, Skv, sM, np);                      // dP = dO V^T
+        if (ok) {
+          fa::fa_bwd_ds_kernel<<<eg, 256, 0, st>>>(sm, dpm, r);               // dS
+          ok = launched();
+        }
+        if (ok) ok = gemm_rm(h, false, false, Sq, 128, Skv, scale, dpm, Skv, sM, k32 + ko, 128, sK,
+                             0.f, dq32 + qo, 128, sQ, np);                    // dQ = scale dS K
+        if (ok) ok = gemm_rm(h, true, false, Skv, 128, Sq, scale, dpm, Skv, sM, q32 + qo, 128, sQ,
+                             1.f, dk32 + ko, 128, sK, np);                    // dK += scale dS^T Q
       }
-      if (ok) ok = gemm_rm(h, true, false, Skv, 128, Sq, 1.f, sm, Skv, sM, do32 + qo, 128, sQ, 1.f,
-                           dv32 + ko, 128, sK, np);                           // dV += P^T dO
-      if (ok) ok = gemm_rm(h, false, true, Sq, Skv, 128, 1.f, do32 + qo, 128, sQ, v32 + ko, 128, sK,
-                           0.f, dpm, Skv, sM, np);                            // dP = dO V^T
-      if (ok) {
-        fa::fa_bwd_ds_kernel<<<dim3(Sq, np), 256, 0, st>>>(sm, dpm, r);     // dS
-        ok = launched();
-      }
-      if (ok) ok = gemm_rm(h, false, false, Sq, 128, Skv, scale, dpm, Skv, sM, k32 + ko, 128, sK,
-                           0.f, dq32 + qo, 128, sQ, np);                      // dQ = scale dS K
-      if (ok) ok = gemm_rm(h, true, false, Skv, 128, Sq, scale, dpm, Skv, sM, q32 + qo, 128, sQ,
-                           1.f, dk32 + ko, 128, sK, np);                      // dK += scale dS^T Q
       if (!ok && rc == FA_OK) rc = cuda_fail(cudaErrorUnknown);
     }
   }

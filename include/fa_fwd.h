@@ -304,11 +304,13 @@ int fa_fwd_o_lo(const void* q, const void* k, const void* v, void* o, void* o_lo
  * accuracy.  mask_mode: FA_MASK_NONE or FA_MASK_CAUSAL (top-left), plus
  * FA_DTYPE_FP16; seqlens as fa_fwd.  D = Dv = 128 only (FA_ERR_UNSUPPORTED
  * otherwise).  Rows past a batch's length get zero gradients.  S, P, dP and
- * dS are materialised in fp32 for a batch of (KV head, head of its group)
- * planes at a time and every product is an fp32 cuBLAS GEMM.  Stream-ordered
- * scratch (cudaMallocAsync, freed on `stream`): d_row; fp32 copies of q, k,
- * v, dout; fp32 dq, dk, dv; and 2 * 4 * Sq * Skv bytes per plane of a batch,
- * batches of up to 1 GiB (at least one plane).  Calls from several host
+ * dS are materialised for a batch of (KV head, head of its group) planes at a
+ * time and every product is a cuBLAS GEMM accumulating in fp32: bf16 inputs
+ * on the tensor cores (S and dP exact, P and dS as bf16 hi + lo pairs), fp16
+ * inputs in fp32.  Stream-ordered scratch (cudaMallocAsync, freed on
+ * `stream`): d_row; fp32 dq, dk, dv; 8 * Sq * Skv bytes per plane of a batch,
+ * batches of up to 1 GiB (at least one plane); with fp16 inputs also fp32
+ * copies of q, k, v, dout and 4 * Sq * Skv more bytes per plane.  Calls from several host
  * threads serialise their enqueueing on one lock per process.  Returns FA_OK
  * or a negative FA_ERR_* code (nothing launched on an argument error). */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* o_lo,
