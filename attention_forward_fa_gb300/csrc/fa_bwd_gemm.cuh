@@ -95,7 +95,14 @@ __global__ void __launch_bounds__(256) fa_bwd_ds_kernel(const float* __restrict_
 
 // bf16 operands of the tensor-core products: P = exp(scale * s - LSE) (as
 // fa_bwd_p_kernel) split into hi = bf16(P) and lo = bf16(P - hi), written to
-// two bf16 matrices of the batch's layout.  Grid: (Sq, planes).
+// two bf16 matrices of the batch's layout.  kV elements per thread and step:
+// 8 (32-byte loads, 16-byte stores) when Skv is a multiple of 8, else 1.
+// Grid: (Sq, planes).
+__device__ __forceinline__ void bf16_hilo(float x, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(x, 0.f) & 0xFFFFu;
+  lo = pack_bf16x2(x - __uint_as_float(hi << 16), 0.f) & 0xFFFFu;
+}
+template <int kV>
 __global__ void __launch_bounds__(256) fa_bwd_p_hilo_kernel(const float* __restrict__ s,
                                                             uint16_t* __restrict__ ph,
                                                             uint16_t* __restrict__ pl,
@@ -111,17 +118,35 @@ __global__ void __launch_bounds__(256) fa_bwd_p_hilo_kernel(const float* __restr
   int lim = row_ok ? kv_len : 0;
   if (r.causal) lim = min(lim, i + 1);
   const size_t base = ((size_t)z * r.Sq + i) * r.Skv;
-  for (int j = threadIdx.x; j < r.Skv; j += blockDim.x) {
-    const float x = j < lim ? expf(fmaf(s[base + j], r.scale, -lse)) : 0.f;
-    const uint32_t h2 = pack_bf16x2(x, 0.f);
-    const float hf = __uint_as_float(h2 << 16);
-    ph[base + j] = (uint16_t)(h2 & 0xFFFFu);
-    pl[base + j] = (uint16_t)(pack_bf16x2(x - hf, 0.f) & 0xFFFFu);
+  for (int j0 = threadIdx.x * kV; j0 < r.Skv; j0 += blockDim.x * kV) {
+    float x[kV];
+    if constexpr (kV == 8) {
+      const float4 a = *reinterpret_cast<const float4*>(s + base + j0);
+      const float4 c = *reinterpret_cast<const float4*>(s + base + j0 + 4);
+      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+      x[4] = c.x; x[5] = c.y; x[6] = c.z; x[7] = c.w;
+    } else {
+      x[0] = s[base + j0];
+    }
+    uint32_t h[kV], l[kV];
+#pragma unroll
+    for (int e = 0; e < kV; ++e) bf16_hilo(j0 + e < lim ? expf(fmaf(x[e], r.scale, -lse)) : 0.f, h[e], l[e]);
+    if constexpr (kV == 8) {
+      *reinterpret_cast<uint4*>(ph + base + j0) =
+          make_uint4(h[0] | h[1] << 16, h[2] | h[3] << 16, h[4] | h[5] << 16, h[6] | h[7] << 16);
+      *reinterpret_cast<uint4*>(pl + base + j0) =
+          make_uint4(l[0] | l[1] << 16, l[2] | l[3] << 16, l[4] | l[5] << 16, l[6] | l[7] << 16);
+    } else {
+      ph[base + j0] = (uint16_t)h[0];
+      pl[base + j0] = (uint16_t)l[0];
+    }
   }
 }
 
 // dS = P * (dP - d_row) with P = hi + lo read from the bf16 pair, written back
-// over the pair as bf16 hi and lo; exactly 0 where P is.  Grid: (Sq, planes).
+// over the pair as bf16 hi and lo; exactly 0 where P is.  kV as above.
+// Grid: (Sq, planes).
+template <int kV>
 __global__ void __launch_bounds__(256) fa_bwd_ds_hilo_kernel(uint16_t* __restrict__ ph,
                                                              uint16_t* __restrict__ pl,
                                                              const float* __restrict__ dp,
@@ -131,14 +156,37 @@ __global__ void __launch_bounds__(256) fa_bwd_ds_hilo_kernel(uint16_t* __restric
   const int p = r.plane0 + z;
   const float d = r.d_row[(size_t)(p * r.G + r.g) * r.Sq + i];
   const size_t base = ((size_t)z * r.Sq + i) * r.Skv;
-  for (int j = threadIdx.x; j < r.Skv; j += blockDim.x) {
-    const float pv = __uint_as_float((uint32_t)ph[base + j] << 16) +
-                     __uint_as_float((uint32_t)pl[base + j] << 16);
-    const float x = pv != 0.f ? pv * (dp[base + j] - d) : 0.f;
-    const uint32_t h2 = pack_bf16x2(x, 0.f);
-    const float hf = __uint_as_float(h2 << 16);
-    ph[base + j] = (uint16_t)(h2 & 0xFFFFu);
-    pl[base + j] = (uint16_t)(pack_bf16x2(x - hf, 0.f) & 0xFFFFu);
+  for (int j0 = threadIdx.x * kV; j0 < r.Skv; j0 += blockDim.x * kV) {
+    float pv[kV], dv[kV];
+    if constexpr (kV == 8) {
+      const uint4 hh = *reinterpret_cast<const uint4*>(ph + base + j0);
+      const uint4 ll = *reinterpret_cast<const uint4*>(pl + base + j0);
+      const uint32_t hw[4] = {hh.x, hh.y, hh.z, hh.w}, lw[4] = {ll.x, ll.y, ll.z, ll.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        pv[2 * e] = __uint_as_float(hw[e] << 16) + __uint_as_float(lw[e] << 16);
+        pv[2 * e + 1] = __uint_as_float(hw[e] & 0xFFFF0000u) + __uint_as_float(lw[e] & 0xFFFF0000u);
+      }
+      const float4 a = *reinterpret_cast<const float4*>(dp + base + j0);
+      const float4 c = *reinterpret_cast<const float4*>(dp + base + j0 + 4);
+      dv[0] = a.x; dv[1] = a.y; dv[2] = a.z; dv[3] = a.w;
+      dv[4] = c.x; dv[5] = c.y; dv[6] = c.z; dv[7] = c.w;
+    } else {
+      pv[0] = __uint_as_float((uint32_t)ph[base + j0] << 16) + __uint_as_float((uint32_t)pl[base + j0] << 16);
+      dv[0] = dp[base + j0];
+    }
+    uint32_t h[kV], l[kV];
+#pragma unroll
+    for (int e = 0; e < kV; ++e) bf16_hilo(pv[e] != 0.f ? pv[e] * (dv[e] - d) : 0.f, h[e], l[e]);
+    if constexpr (kV == 8) {
+      *reinterpret_cast<uint4*>(ph + base + j0) =
+          make_uint4(h[0] | h[1] << 16, h[2] | h[3] << 16, h[4] | h[5] << 16, h[6] | h[7] << 16);
+      *reinterpret_cast<uint4*>(pl + base + j0) =
+          make_uint4(l[0] | l[1] << 16, l[2] | l[3] << 16, l[4] | l[5] << 16, l[6] | l[7] << 16);
+    } else {
+      ph[base + j0] = (uint16_t)h[0];
+      pl[base + j0] = (uint16_t)l[0];
+    }
   }
 }
 

@@ -874,7 +874,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
         ok = gemm_rm_bf16(h, false, true, Sq, Skv, 128, 1.f, q16 + qo, 128, sQ, k16 + ko, 128, sK,
                           0.f, sm, Skv, sM, np);                              // S = Q K^T
         if (ok) {
-          fa::fa_bwd_p_hilo_kernel<<<eg, 256, 0, st>>>(sm, ph, pl, r);        // P = hi + lo
+          if (Skv % 8 == 0) fa::fa_bwd_p_hilo_kernel<8><<<eg, 256, 0, st>>>(sm, ph, pl, r);
+          else fa::fa_bwd_p_hilo_kernel<1><<<eg, 256, 0, st>>>(sm, ph, pl, r);   // P = hi + lo
           ok = launched();
         }
         for (int part = 0; ok && part < 2; ++part)                           // dV += P^T dO
@@ -883,7 +884,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
         if (ok) ok = gemm_rm_bf16(h, false, true, Sq, Skv, 128, 1.f, do16 + qo, 128, sQ, v16 + ko,
                                   128, sK, 0.f, sm, Skv, sM, np);             // dP = dO V^T
         if (ok) {
-          fa::fa_bwd_ds_hilo_kernel<<<eg, 256, 0, st>>>(ph, pl, sm, r);       // dS = hi + lo
+          if (Skv % 8 == 0) fa::fa_bwd_ds_hilo_kernel<8><<<eg, 256, 0, st>>>(ph, pl, sm, r);
+          else fa::fa_bwd_ds_hilo_kernel<1><<<eg, 256, 0, st>>>(ph, pl, sm, r);  // dS = hi + lo
           ok = launched();
         }
         for (int part = 0; ok && part < 2; ++part)                           // dQ = scale dS K

@@ -508,8 +508,9 @@ def backward_workload(args, dev, dist, world, local, peak):
     return {"config": cfg,
             "algorithmic_gflop": flops / 1e9, "ms_per_call": ms,
             "tflops": whole_job_tflops(world, flops, ms), "frac": achieved / peak, "steps": steps,
-            "kernel": "fa_bwd: fp32 copies, d_row, per (KV head, group head) batch fp32 cuBLAS GEMMs "
-                      "for S, dV, dP, dQ, dK with P and dS kernels between them",
+            "kernel": "fa_bwd: d_row, then per batch of (KV head, group head) planes cuBLAS bf16 "
+                      "tensor-core GEMMs (fp32 accumulation) for S, dP and, with P and dS as bf16 "
+                      "hi + lo pairs, dV, dQ, dK; this library's P, dS and conversion kernels",
             "timing": "eager, events around the K calls", "clocks": clocks}
 
 
@@ -530,6 +531,22 @@ def run_ours(args, world, rank, local):
         dist.barrier()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.backward:
+        # the backward entry of the c2 line on its own (a short run to profile)
+        peaks, _ = measured_peaks()
+        args.workload_steps, args.workload_soak = args.steps, args.soak
+        e = backward_workload(args, dev, dist, world, local, float(peaks["bf16_tflops"]))
+        if rank == 0:
+            print(json.dumps({"metric": "attention bwd TFLOP/s on 1 GB300 (algorithmic) and % of dense "
+                                        "BF16 tensor peak; ms/call",
+                              "value": e["tflops"], "unit": "TFLOP/s", "n_gpus": world,
+                              "steps": e["steps"], "warmup": 3, "ms_per_step": e["ms_per_call"],
+                              "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                              "dtype": "bf16", "data": "synthetic", **{k: e[k] for k in e
+                                                                      if k not in ("tflops", "steps")}}))
+        if dist:
+            dist.destroy_process_group()
+        return 0
     p = workload_problem(args.workload, args.mla_tokens)
     flops = W.algorithmic_flops(p)
     prep = Prepared(p, dev)
@@ -690,6 +707,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c2",
                     help="c2 (default) is the benchmark line; the others time the same path "
                          "on the other workloads")
+    ap.add_argument("--backward", action="store_true",
+                    help="time only the backward (fa_bwd) on the c2 workload, its own JSON line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
