@@ -56,13 +56,15 @@ struct BwdGemmRows {
   float scale;
   int plane0;            // first KV plane of the batch of GEMMs
   int g;                 // head of the group
+  int row0;              // first row of the row block (grid.x counts rows from here)
+  int ncols;             // keys [0, ncols) of the block's rows are written (the rest unused)
 };
 
 // P = exp(scale * s - LSE) over S in place (0 for masked keys, rows past the
 // batch's length and rows without keys).  Grid: (Sq, planes); a block walks
 // one row.
 __global__ void __launch_bounds__(256) fa_bwd_p_kernel(float* __restrict__ s, BwdGemmRows r) {
-  const int i = blockIdx.x;
+  const int i = r.row0 + blockIdx.x;
   const int z = blockIdx.y;
   const int p = r.plane0 + z;
   const int b = p / r.Hkv;
@@ -73,7 +75,7 @@ __global__ void __launch_bounds__(256) fa_bwd_p_kernel(float* __restrict__ s, Bw
   int lim = row_ok ? kv_len : 0;                 // keys j < lim are seen
   if (r.causal) lim = min(lim, i + 1);
   float* row = s + ((size_t)z * r.Sq + i) * r.Skv;
-  for (int j = threadIdx.x; j < r.Skv; j += blockDim.x)
+  for (int j = threadIdx.x; j < r.ncols; j += blockDim.x)
     row[j] = j < lim ? expf(fmaf(row[j], r.scale, -lse)) : 0.f;
 }
 
@@ -82,12 +84,12 @@ __global__ void __launch_bounds__(256) fa_bwd_p_kernel(float* __restrict__ s, Bw
 // Grid: (Sq, planes).
 __global__ void __launch_bounds__(256) fa_bwd_ds_kernel(const float* __restrict__ pm,
                                                         float* __restrict__ dp, BwdGemmRows r) {
-  const int i = blockIdx.x;
+  const int i = r.row0 + blockIdx.x;
   const int z = blockIdx.y;
   const int p = r.plane0 + z;
   const float d = r.d_row[(size_t)(p * r.G + r.g) * r.Sq + i];
   const size_t base = ((size_t)z * r.Sq + i) * r.Skv;
-  for (int j = threadIdx.x; j < r.Skv; j += blockDim.x) {
+  for (int j = threadIdx.x; j < r.ncols; j += blockDim.x) {
     const float pv = pm[base + j];
     dp[base + j] = pv != 0.f ? pv * (dp[base + j] - d) : 0.f;
   }
@@ -96,7 +98,8 @@ __global__ void __launch_bounds__(256) fa_bwd_ds_kernel(const float* __restrict_
 // bf16 operands of the tensor-core products: P = exp(scale * s - LSE) (as
 // fa_bwd_p_kernel) split into hi = bf16(P) and lo = bf16(P - hi), written to
 // two bf16 matrices of the batch's layout.  kV elements per thread and step:
-// 8 (32-byte loads, 16-byte stores) when Skv is a multiple of 8, else 1.
+// 8 (32-byte loads, 16-byte stores) when Skv and ncols are multiples of 8,
+// else 1.
 // Grid: (Sq, planes).
 __device__ __forceinline__ void bf16_hilo(float x, uint32_t& hi, uint32_t& lo) {
   hi = pack_bf16x2(x, 0.f) & 0xFFFFu;
@@ -107,7 +110,7 @@ __global__ void __launch_bounds__(256) fa_bwd_p_hilo_kernel(const float* __restr
                                                             uint16_t* __restrict__ ph,
                                                             uint16_t* __restrict__ pl,
                                                             BwdGemmRows r) {
-  const int i = blockIdx.x;
+  const int i = r.row0 + blockIdx.x;
   const int z = blockIdx.y;
   const int p = r.plane0 + z;
   const int b = p / r.Hkv;
@@ -118,7 +121,7 @@ __global__ void __launch_bounds__(256) fa_bwd_p_hilo_kernel(const float* __restr
   int lim = row_ok ? kv_len : 0;
   if (r.causal) lim = min(lim, i + 1);
   const size_t base = ((size_t)z * r.Sq + i) * r.Skv;
-  for (int j0 = threadIdx.x * kV; j0 < r.Skv; j0 += blockDim.x * kV) {
+  for (int j0 = threadIdx.x * kV; j0 < r.ncols; j0 += blockDim.x * kV) {
     float x[kV];
     if constexpr (kV == 8) {
       const float4 a = *reinterpret_cast<const float4*>(s + base + j0);
@@ -151,12 +154,12 @@ __global__ void __launch_bounds__(256) fa_bwd_ds_hilo_kernel(uint16_t* __restric
                                                              uint16_t* __restrict__ pl,
                                                              const float* __restrict__ dp,
                                                              BwdGemmRows r) {
-  const int i = blockIdx.x;
+  const int i = r.row0 + blockIdx.x;
   const int z = blockIdx.y;
   const int p = r.plane0 + z;
   const float d = r.d_row[(size_t)(p * r.G + r.g) * r.Sq + i];
   const size_t base = ((size_t)z * r.Sq + i) * r.Skv;
-  for (int j0 = threadIdx.x * kV; j0 < r.Skv; j0 += blockDim.x * kV) {
+  for (int j0 = threadIdx.x * kV; j0 < r.ncols; j0 += blockDim.x * kV) {
     float pv[kV], dv[kV];
     if constexpr (kV == 8) {
       const uint4 hh = *reinterpret_cast<const uint4*>(ph + base + j0);

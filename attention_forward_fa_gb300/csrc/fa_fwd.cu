@@ -696,6 +696,9 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, void* o_lo, f
 // S and dP of one batch of the backward's GEMMs are held in fp32; a batch
 // covers as many KV planes as fit in this many bytes (at least one).
 constexpr size_t kBwdGemmBytes = size_t(1) << 30;
+// Query rows per block of the causal backward's GEMMs (each block against the
+// keys up to its last row).
+constexpr int kBwdRowBlock = 512;
 
 // One cuBLAS handle per device, created on first use: fp32 products only
 // (pedantic math: no reduced-precision tensor-core paths) and no workspace,
@@ -868,51 +871,63 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
     for (int p0 = 0; ok && p0 < planes; p0 += chunk) {
       const int np = std::min(chunk, planes - p0);
       const long long qo = ((long long)p0 * G + g) * Sq * 128, ko = (long long)p0 * Skv * 128;
-      fa::BwdGemmRows r{lse, d_row, seqlens, Hkv, G, Sq, Skv, mask == FA_MASK_CAUSAL, scale, p0, g};
-      const dim3 eg(Sq, np);
-      if (tc) {
-        ok = gemm_rm_bf16(h, false, true, Sq, Skv, 128, 1.f, q16 + qo, 128, sQ, k16 + ko, 128, sK,
-                          0.f, sm, Skv, sM, np);                              // S = Q K^T
-        if (ok) {
-          if (Skv % 8 == 0) fa::fa_bwd_p_hilo_kernel<8><<<eg, 256, 0, st>>>(sm, ph, pl, r);
-          else fa::fa_bwd_p_hilo_kernel<1><<<eg, 256, 0, st>>>(sm, ph, pl, r);   // P = hi + lo
-          ok = launched();
+      // Causal problems go in blocks of kBwdRowBlock query rows, each against
+      // the keys up to its last row only (top-left: row i sees keys j <= i), so
+      // that the masked half of S is neither computed nor stored.
+      const bool causal = mask == FA_MASK_CAUSAL;
+      const int rb = causal ? kBwdRowBlock : Sq;
+      for (int r0 = 0; ok && r0 < Sq; r0 += rb) {
+        const int r1 = std::min(Sq, r0 + rb), nr = r1 - r0;
+        const int nc = causal ? std::min(Skv, r1) : Skv;   // keys [0, nc) of these rows
+        fa::BwdGemmRows r{lse, d_row, seqlens, Hkv, G, Sq, Skv, causal, scale, p0, g, r0, nc};
+        const dim3 eg(nr, np);
+        const long long qr = qo + (long long)r0 * 128;       // the block's rows of Q, dO, dQ
+        const long long mr = (long long)r0 * Skv;           // ... of S, P, dP, dS
+        const bool vec = Skv % 8 == 0 && nc % 8 == 0;
+        if (tc) {
+          ok = gemm_rm_bf16(h, false, true, nr, nc, 128, 1.f, q16 + qr, 128, sQ, k16 + ko, 128, sK,
+                            0.f, sm + mr, Skv, sM, np);                       // S = Q K^T
+          if (ok) {
+            if (vec) fa::fa_bwd_p_hilo_kernel<8><<<eg, 256, 0, st>>>(sm, ph, pl, r);
+            else fa::fa_bwd_p_hilo_kernel<1><<<eg, 256, 0, st>>>(sm, ph, pl, r);   // P = hi + lo
+            ok = launched();
+          }
+          for (int part = 0; ok && part < 2; ++part)                         // dV += P^T dO
+            ok = gemm_rm_bf16(h, true, false, nc, 128, nr, 1.f, (part ? pl : ph) + mr, Skv, sM,
+                              do16 + qr, 128, sQ, 1.f, dv32 + ko, 128, sK, np);
+          if (ok) ok = gemm_rm_bf16(h, false, true, nr, nc, 128, 1.f, do16 + qr, 128, sQ, v16 + ko,
+                                    128, sK, 0.f, sm + mr, Skv, sM, np);      // dP = dO V^T
+          if (ok) {
+            if (vec) fa::fa_bwd_ds_hilo_kernel<8><<<eg, 256, 0, st>>>(ph, pl, sm, r);
+            else fa::fa_bwd_ds_hilo_kernel<1><<<eg, 256, 0, st>>>(ph, pl, sm, r);  // dS = hi + lo
+            ok = launched();
+          }
+          for (int part = 0; ok && part < 2; ++part)                         // dQ = scale dS K
+            ok = gemm_rm_bf16(h, false, false, nr, 128, nc, scale, (part ? pl : ph) + mr, Skv, sM,
+                              k16 + ko, 128, sK, part ? 1.f : 0.f, dq32 + qr, 128, sQ, np);
+          for (int part = 0; ok && part < 2; ++part)                         // dK += scale dS^T Q
+            ok = gemm_rm_bf16(h, true, false, nc, 128, nr, scale, (part ? pl : ph) + mr, Skv, sM,
+                              q16 + qr, 128, sQ, 1.f, dk32 + ko, 128, sK, np);
+        } else {
+          ok = gemm_rm(h, false, true, nr, nc, 128, 1.f, q32 + qr, 128, sQ, k32 + ko, 128, sK, 0.f,
+                       sm + mr, Skv, sM, np);                                 // S = Q K^T
+          if (ok) {
+            fa::fa_bwd_p_kernel<<<eg, 256, 0, st>>>(sm, r);                   // P
+            ok = launched();
+          }
+          if (ok) ok = gemm_rm(h, true, false, nc, 128, nr, 1.f, sm + mr, Skv, sM, do32 + qr, 128,
+                               sQ, 1.f, dv32 + ko, 128, sK, np);              // dV += P^T dO
+          if (ok) ok = gemm_rm(h, false, true, nr, nc, 128, 1.f, do32 + qr, 128, sQ, v32 + ko, 128,
+                               sK, 0.f, dpm + mr, Skv, sM, np);               // dP = dO V^T
+          if (ok) {
+            fa::fa_bwd_ds_kernel<<<eg, 256, 0, st>>>(sm, dpm, r);             // dS
+            ok = launched();
+          }
+          if (ok) ok = gemm_rm(h, false, false, nr, 128, nc, scale, dpm + mr, Skv, sM, k32 + ko,
+                               128, sK, 0.f, dq32 + qr, 128, sQ, np);         // dQ = scale dS K
+          if (ok) ok = gemm_rm(h, true, false, nc, 128, nr, scale, dpm + mr, Skv, sM, q32 + qr,
+                               128, sQ, 1.f, dk32 + ko, 128, sK, np);         // dK += scale dS^T Q
         }
-        for (int part = 0; ok && part < 2; ++part)                           // dV += P^T dO
-          ok = gemm_rm_bf16(h, true, false, Skv, 128, Sq, 1.f, part ? pl : ph, Skv, sM, do16 + qo,
-                            128, sQ, 1.f, dv32 + ko, 128, sK, np);
-        if (ok) ok = gemm_rm_bf16(h, false, true, Sq, Skv, 128, 1.f, do16 + qo, 128, sQ, v16 + ko,
-                                  128, sK, 0.f, sm, Skv, sM, np);             // dP = dO V^T
-        if (ok) {
-          if (Skv % 8 == 0) fa::fa_bwd_ds_hilo_kernel<8><<<eg, 256, 0, st>>>(ph, pl, sm, r);
-          else fa::fa_bwd_ds_hilo_kernel<1><<<eg, 256, 0, st>>>(ph, pl, sm, r);  // dS = hi + lo
-          ok = launched();
-        }
-        for (int part = 0; ok && part < 2; ++part)                           // dQ = scale dS K
-          ok = gemm_rm_bf16(h, false, false, Sq, 128, Skv, scale, part ? pl : ph, Skv, sM,
-                            k16 + ko, 128, sK, part ? 1.f : 0.f, dq32 + qo, 128, sQ, np);
-        for (int part = 0; ok && part < 2; ++part)                           // dK += scale dS^T Q
-          ok = gemm_rm_bf16(h, true, false, Skv, 128, Sq, scale, part ? pl : ph, Skv, sM,
-                            q16 + qo, 128, sQ, 1.f, dk32 + ko, 128, sK, np);
-      } else {
-        ok = gemm_rm(h, false, true, Sq, Skv, 128, 1.f, q32 + qo, 128, sQ, k32 + ko, 128, sK, 0.f,
-                     sm, Skv, sM, np);                                        // S = Q K^T
-        if (ok) {
-          fa::fa_bwd_p_kernel<<<eg, 256, 0, st>>>(sm, r);                     // P
-          ok = launched();
-        }
-        if (ok) ok = gemm_rm(h, true, false, Skv, 128, Sq, 1.f, sm, Skv, sM, do32 + qo, 128, sQ,
-                             1.f, dv32 + ko, 128, sK, np);                    // dV += P^T dO
-        if (ok) ok = gemm_rm(h, false, true, Sq, Skv, 128, 1.f, do32 + qo, 128, sQ, v32 + ko, 128,
-                             sK, 0.f, dpm, Skv, sM, np);                      // dP = dO V^T
-        if (ok) {
-          fa::fa_bwd_ds_kernel<<<eg, 256, 0, st>>>(sm, dpm, r);               // dS
-          ok = launched();
-        }
-        if (ok) ok = gemm_rm(h, false, false, Sq, 128, Skv, scale, dpm, Skv, sM, k32 + ko, 128, sK,
-                             0.f, dq32 + qo, 128, sQ, np);                    // dQ = scale dS K
-        if (ok) ok = gemm_rm(h, true, false, Skv, 128, Sq, scale, dpm, Skv, sM, q32 + qo, 128, sQ,
-                             1.f, dk32 + ko, 128, sK, np);                    // dK += scale dS^T Q
       }
       if (!ok && rc == FA_OK) rc = cuda_fail(cudaErrorUnknown);
     }
