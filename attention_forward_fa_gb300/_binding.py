@@ -385,8 +385,8 @@ def flash_attention_forward(q, k, v=None, *, scale: Optional[float] = None, caus
 def flash_attention_backward(q, k, v, o, lse, dout, *, o_lo=None, scale: Optional[float] = None,
                              causal: bool = False, seqlens=None, dq=None, dk=None, dv=None,
                              stream=None):
-    """Allocating wrapper over fa_bwd: q, o, dout [B,Hq,Sq,128], k, v
-    [B,Hkv,Skv,128] (bf16 or fp16 CUDA tensors, contiguous), lse [B,Hq,Sq]
+    """Allocating wrapper over fa_bwd: q, o, dout [B,Hq,Sq,D], k, v
+    [B,Hkv,Skv,D] (D = 64 or 128; bf16 or fp16 CUDA tensors, contiguous), lse [B,Hq,Sq]
     fp32 from the forward, o_lo its residual (recommended).  Returns
     (dq, dk, dv) in the inputs' type."""
     import torch

@@ -582,25 +582,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   bwd_teardown(tmem);
 }
 
-// d_row = rowsum(dO * (O + O_lo)) in fp32, one warp per row of 128 values.
+// d_row = rowsum(dO * (O + O_lo)) in fp32, one warp per row of D values
+// (D a multiple of 4: each lane takes 4 consecutive values per step).
 template <bool kBF16>
 __global__ void __launch_bounds__(256) fa_bwd_drow_kernel(const uint16_t* __restrict__ o,
                                                           const uint16_t* __restrict__ o_lo,
                                                           const uint16_t* __restrict__ dout,
-                                                          float* __restrict__ d_row, long long rows) {
+                                                          float* __restrict__ d_row, long long rows,
+                                                          int D) {
   const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
-  const uint2 vo = reinterpret_cast<const uint2*>(o + r * 128)[lane];
-  const uint2 vd = reinterpret_cast<const uint2*>(dout + r * 128)[lane];
-  const uint2 vl = o_lo ? reinterpret_cast<const uint2*>(o_lo + r * 128)[lane] : make_uint2(0u, 0u);
   auto lo = [](uint32_t w) { return kBF16 ? __uint_as_float(w << 16) : f16_lo_to_f32(w); };
   auto hi = [](uint32_t w) { return kBF16 ? __uint_as_float(w & 0xFFFF0000u) : f16_hi_to_f32(w); };
   float acc = 0.f;
-  acc = fmaf(lo(vd.x), lo(vo.x) + lo(vl.x), acc);
-  acc = fmaf(hi(vd.x), hi(vo.x) + hi(vl.x), acc);
-  acc = fmaf(lo(vd.y), lo(vo.y) + lo(vl.y), acc);
-  acc = fmaf(hi(vd.y), hi(vo.y) + hi(vl.y), acc);
+  for (int c = 4 * lane; c < D; c += 128) {
+    const uint2 vo = *reinterpret_cast<const uint2*>(o + r * D + c);
+    const uint2 vd = *reinterpret_cast<const uint2*>(dout + r * D + c);
+    const uint2 vl = o_lo ? *reinterpret_cast<const uint2*>(o_lo + r * D + c) : make_uint2(0u, 0u);
+    acc = fmaf(lo(vd.x), lo(vo.x) + lo(vl.x), acc);
+    acc = fmaf(hi(vd.x), hi(vo.x) + hi(vl.x), acc);
+    acc = fmaf(lo(vd.y), lo(vo.y) + lo(vl.y), acc);
+    acc = fmaf(hi(vd.y), hi(vo.y) + hi(vl.y), acc);
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (lane == 0) d_row[r] = acc;

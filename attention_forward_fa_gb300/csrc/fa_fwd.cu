@@ -756,7 +756,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
       (long long)Skv * 128 > (1LL << 31))
     return FA_ERR_SHAPE;
   if (((long long)B * Hq * Sq + 7) / 8 > 0x7FFFFFFF) return FA_ERR_SHAPE;   // the d_row launch's grid
-  if (D != 128 || Dv != 128) return FA_ERR_UNSUPPORTED;
+  if (D != Dv || (D != 64 && D != 128)) return FA_ERR_UNSUPPORTED;
   for (const void* t : {q, k, v, o, dout, static_cast<const void*>(dq), static_cast<const void*>(dk),
                         static_cast<const void*>(dv)})
     if (!aligned(t, 16)) return FA_ERR_ALIGN;
@@ -784,7 +784,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   // copies of Q, dO, K, V and a second fp32 matrix for P / dS.
   const int G = Hq / Hkv;
   const int planes = B * Hkv;
-  const size_t nq = (size_t)B * Hq * Sq * 128, nk = (size_t)B * Hkv * Skv * 128;
+  const size_t nq = (size_t)B * Hq * Sq * D, nk = (size_t)B * Hkv * Skv * D;
   const size_t rows = (size_t)B * Hq * Sq;
   const size_t plane_mat = (size_t)Sq * Skv;
   const int chunk = (int)std::min<size_t>(
@@ -827,7 +827,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
     if (e != cudaSuccess && rc == FA_OK) rc = cuda_fail(e);
     return rc == FA_OK;
   };
-  // fp32 copies (every row is a multiple of 8 elements: D = 128)
+  // fp32 copies (every row is a multiple of 8 elements: D = 64 or 128)
   auto to32 = [&](const void* in, float* out, size_t n) {
     const size_t n8 = n / 8;
     const unsigned blocks = (unsigned)std::min<size_t>((n8 + 255) / 256, 4096);
@@ -856,13 +856,13 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
     const auto* o16 = static_cast<const uint16_t*>(o);
     const auto* lo16 = static_cast<const uint16_t*>(o_lo);
     const auto* d16 = static_cast<const uint16_t*>(dout);
-    if (fp16) fa::fa_bwd_drow_kernel<false><<<blocks, 256, 0, st>>>(o16, lo16, d16, d_row, (long long)rows);
-    else fa::fa_bwd_drow_kernel<true><<<blocks, 256, 0, st>>>(o16, lo16, d16, d_row, (long long)rows);
+    if (fp16) fa::fa_bwd_drow_kernel<false><<<blocks, 256, 0, st>>>(o16, lo16, d16, d_row, (long long)rows, D);
+    else fa::fa_bwd_drow_kernel<true><<<blocks, 256, 0, st>>>(o16, lo16, d16, d_row, (long long)rows, D);
     ok = launched();
   }
   // per head g of every group and batch of KV planes [p0, p0 + np): the query
   // planes are p * G + g, so Q, dO and dQ advance by G planes per KV plane
-  const long long sQ = (long long)G * Sq * 128, sK = (long long)Skv * 128, sM = (long long)plane_mat;
+  const long long sQ = (long long)G * Sq * D, sK = (long long)Skv * D, sM = (long long)plane_mat;
   const auto* q16 = static_cast<const uint16_t*>(q);
   const auto* k16 = static_cast<const uint16_t*>(k);
   const auto* v16 = static_cast<const uint16_t*>(v);
@@ -870,7 +870,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   for (int g = 0; ok && g < G; ++g) {
     for (int p0 = 0; ok && p0 < planes; p0 += chunk) {
       const int np = std::min(chunk, planes - p0);
-      const long long qo = ((long long)p0 * G + g) * Sq * 128, ko = (long long)p0 * Skv * 128;
+      const long long qo = ((long long)p0 * G + g) * Sq * D, ko = (long long)p0 * Skv * D;
       // Causal problems go in blocks of kBwdRowBlock query rows, each against
       // the keys up to its last row only (top-left: row i sees keys j <= i), so
       // that the masked half of S is neither computed nor stored.
@@ -881,11 +881,11 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
         const int nc = causal ? std::min(Skv, r1) : Skv;   // keys [0, nc) of these rows
         fa::BwdGemmRows r{lse, d_row, seqlens, Hkv, G, Sq, Skv, causal, scale, p0, g, r0, nc};
         const dim3 eg(nr, np);
-        const long long qr = qo + (long long)r0 * 128;       // the block's rows of Q, dO, dQ
+        const long long qr = qo + (long long)r0 * D;       // the block's rows of Q, dO, dQ
         const long long mr = (long long)r0 * Skv;           // ... of S, P, dP, dS
         const bool vec = Skv % 8 == 0 && nc % 8 == 0;
         if (tc) {
-          ok = gemm_rm_bf16(h, false, true, nr, nc, 128, 1.f, q16 + qr, 128, sQ, k16 + ko, 128, sK,
+          ok = gemm_rm_bf16(h, false, true, nr, nc, D, 1.f, q16 + qr, D, sQ, k16 + ko, D, sK,
                             0.f, sm + mr, Skv, sM, np);                       // S = Q K^T
           if (ok) {
             if (vec) fa::fa_bwd_p_hilo_kernel<8><<<eg, 256, 0, st>>>(sm, ph, pl, r);
@@ -893,40 +893,40 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
             ok = launched();
           }
           for (int part = 0; ok && part < 2; ++part)                         // dV += P^T dO
-            ok = gemm_rm_bf16(h, true, false, nc, 128, nr, 1.f, (part ? pl : ph) + mr, Skv, sM,
-                              do16 + qr, 128, sQ, 1.f, dv32 + ko, 128, sK, np);
-          if (ok) ok = gemm_rm_bf16(h, false, true, nr, nc, 128, 1.f, do16 + qr, 128, sQ, v16 + ko,
-                                    128, sK, 0.f, sm + mr, Skv, sM, np);      // dP = dO V^T
+            ok = gemm_rm_bf16(h, true, false, nc, D, nr, 1.f, (part ? pl : ph) + mr, Skv, sM,
+                              do16 + qr, D, sQ, 1.f, dv32 + ko, D, sK, np);
+          if (ok) ok = gemm_rm_bf16(h, false, true, nr, nc, D, 1.f, do16 + qr, D, sQ, v16 + ko,
+                                    D, sK, 0.f, sm + mr, Skv, sM, np);      // dP = dO V^T
           if (ok) {
             if (vec) fa::fa_bwd_ds_hilo_kernel<8><<<eg, 256, 0, st>>>(ph, pl, sm, r);
             else fa::fa_bwd_ds_hilo_kernel<1><<<eg, 256, 0, st>>>(ph, pl, sm, r);  // dS = hi + lo
             ok = launched();
           }
           for (int part = 0; ok && part < 2; ++part)                         // dQ = scale dS K
-            ok = gemm_rm_bf16(h, false, false, nr, 128, nc, scale, (part ? pl : ph) + mr, Skv, sM,
-                              k16 + ko, 128, sK, part ? 1.f : 0.f, dq32 + qr, 128, sQ, np);
+            ok = gemm_rm_bf16(h, false, false, nr, D, nc, scale, (part ? pl : ph) + mr, Skv, sM,
+                              k16 + ko, D, sK, part ? 1.f : 0.f, dq32 + qr, D, sQ, np);
           for (int part = 0; ok && part < 2; ++part)                         // dK += scale dS^T Q
-            ok = gemm_rm_bf16(h, true, false, nc, 128, nr, scale, (part ? pl : ph) + mr, Skv, sM,
-                              q16 + qr, 128, sQ, 1.f, dk32 + ko, 128, sK, np);
+            ok = gemm_rm_bf16(h, true, false, nc, D, nr, scale, (part ? pl : ph) + mr, Skv, sM,
+                              q16 + qr, D, sQ, 1.f, dk32 + ko, D, sK, np);
         } else {
-          ok = gemm_rm(h, false, true, nr, nc, 128, 1.f, q32 + qr, 128, sQ, k32 + ko, 128, sK, 0.f,
+          ok = gemm_rm(h, false, true, nr, nc, D, 1.f, q32 + qr, D, sQ, k32 + ko, D, sK, 0.f,
                        sm + mr, Skv, sM, np);                                 // S = Q K^T
           if (ok) {
             fa::fa_bwd_p_kernel<<<eg, 256, 0, st>>>(sm, r);                   // P
             ok = launched();
           }
-          if (ok) ok = gemm_rm(h, true, false, nc, 128, nr, 1.f, sm + mr, Skv, sM, do32 + qr, 128,
-                               sQ, 1.f, dv32 + ko, 128, sK, np);              // dV += P^T dO
-          if (ok) ok = gemm_rm(h, false, true, nr, nc, 128, 1.f, do32 + qr, 128, sQ, v32 + ko, 128,
+          if (ok) ok = gemm_rm(h, true, false, nc, D, nr, 1.f, sm + mr, Skv, sM, do32 + qr, D,
+                               sQ, 1.f, dv32 + ko, D, sK, np);              // dV += P^T dO
+          if (ok) ok = gemm_rm(h, false, true, nr, nc, D, 1.f, do32 + qr, D, sQ, v32 + ko, D,
                                sK, 0.f, dpm + mr, Skv, sM, np);               // dP = dO V^T
           if (ok) {
             fa::fa_bwd_ds_kernel<<<eg, 256, 0, st>>>(sm, dpm, r);             // dS
             ok = launched();
           }
-          if (ok) ok = gemm_rm(h, false, false, nr, 128, nc, scale, dpm + mr, Skv, sM, k32 + ko,
-                               128, sK, 0.f, dq32 + qr, 128, sQ, np);         // dQ = scale dS K
-          if (ok) ok = gemm_rm(h, true, false, nc, 128, nr, scale, dpm + mr, Skv, sM, q32 + qr,
-                               128, sQ, 1.f, dk32 + ko, 128, sK, np);         // dK += scale dS^T Q
+          if (ok) ok = gemm_rm(h, false, false, nr, D, nc, scale, dpm + mr, Skv, sM, k32 + ko,
+                               D, sK, 0.f, dq32 + qr, D, sQ, np);         // dQ = scale dS K
+          if (ok) ok = gemm_rm(h, true, false, nc, D, nr, scale, dpm + mr, Skv, sM, q32 + qr,
+                               D, sQ, 1.f, dk32 + ko, D, sK, np);         // dK += scale dS^T Q
         }
       }
       if (!ok && rc == FA_OK) rc = cuda_fail(cudaErrorUnknown);

@@ -296,13 +296,13 @@ int fa_fwd_o_lo(const void* q, const void* k, const void* v, void* o, void* o_lo
  * ("BSA PyPTO implementation notes" (gitcode pypto-gym), sections 3.2
  * "Core design strategies" (recomputation), 8.4 (d_row precomputed) and 1
  * (dV unscaled, dQ / dK scaled)).  GQA: dK / dV sum over the heads of a group.
- * q, o, dout, dq: [B, Hq, Sq, 128]; k, v, dk, dv: [B, Hkv, Skv, 128]; lse:
+ * q, o, dout, dq: [B, Hq, Sq, D]; k, v, dk, dv: [B, Hkv, Skv, D]; lse:
  * [B, Hq, Sq] fp32 as fa_fwd wrote it; all DEVICE memory, bf16 (or fp16 with
  * FA_DTYPE_FP16 in mask_mode), 16-byte aligned (lse 4).  o_lo: the residual
  * from fa_fwd_o_lo, or NULL; without it the dpsum uses the rounded output, and
  * on causal problems dQ / dK then lose about an order of magnitude in
  * accuracy.  mask_mode: FA_MASK_NONE or FA_MASK_CAUSAL (top-left), plus
- * FA_DTYPE_FP16; seqlens as fa_fwd.  D = Dv = 128 only (FA_ERR_UNSUPPORTED
+ * FA_DTYPE_FP16; seqlens as fa_fwd.  D = Dv, 64 or 128 (FA_ERR_UNSUPPORTED
  * otherwise).  Rows past a batch's length get zero gradients.  S, P, dP and
  * dS are materialised for a batch of (KV head, head of its group) planes at a
  * time and every product is a cuBLAS GEMM accumulating in fp32: bf16 inputs

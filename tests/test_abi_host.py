@@ -128,7 +128,7 @@ def test_o_lo_pointer_checks(lib):
 
 @pytest.mark.parametrize("change, code", [
     (dict(q=None), -1), (dict(dout=None), -1), (dict(lse=None), -1),
-    (dict(D=64, Dv=64), -3), (dict(Dv=64), -3),
+    (dict(D=96, Dv=96), -3), (dict(Dv=64), -3),
     (dict(Hq=3, Hkv=2), -2), (dict(Sq=0), -2), (dict(mask_mode=2), -2), (dict(mask_mode=0x200), -2),
     (dict(dk=P + 8), -4), (dict(o_lo=P + 2), -4),
 ])

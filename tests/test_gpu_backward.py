@@ -71,6 +71,9 @@ CASES = [
     ("gqa8_full", dict(B=1, Hq=8, Hkv=1, Sq=256, D=128, mask=W.MASK_NONE, seed=35)),
     ("causal_1024", dict(B=1, Hq=1, Sq=1024, D=128, mask=W.MASK_CAUSAL, seed=36)),
     ("sq_ne_skv", dict(B=1, Hq=2, Sq=256, Skv=512, D=128, mask=W.MASK_NONE, seed=37)),
+    ("d64_causal_ragged", dict(B=1, Hq=2, Sq=700, D=64, mask=W.MASK_CAUSAL, seed=39)),
+    ("d64_gqa_fp16_lengths", dict(B=2, Hq=4, Hkv=2, Sq=600, D=64, mask=W.MASK_CAUSAL, dtype="fp16",
+                                  seqlens=[600, 250], seed=40)),
 ]
 
 
