@@ -93,6 +93,15 @@ def test_backward_benchmark_workload_sampled_heads():
     _check(g, ref, "c2 heads 0, 7, 15")
 
 
+def test_backward_across_several_plane_batches():
+    """16 heads at S 4096 hold 2 GiB of S and dP, so fa_bwd runs two batches
+    of 8 planes (1 GiB each) and 8 causal row blocks per batch: every element
+    of heads 0 and 7 (first batch) and 8 and 15 (second)."""
+    p = W.dense(name="batches", B=1, Hq=16, Sq=4096, D=64, mask=W.MASK_CAUSAL, seed=41)
+    g, ref = _run(p, heads=[0, 7, 8, 15])
+    _check(g, ref, "S 4096, heads 0, 7, 8, 15")
+
+
 def test_backward_empty_rows_have_zero_gradients():
     """A batch of length 0 and rows past a batch's length: zero dQ, dK, dV."""
     p = W.dense(name="empty", B=2, Hq=2, Sq=256, D=128, mask=W.MASK_CAUSAL, seqlens=[0, 77], seed=38)
