@@ -19,6 +19,15 @@ FA_FP8_E4M3 = 0
 FA_FP8_E5M2 = 1
 
 FA_OK = 0
+FA_ERR_NULL = -1
+FA_ERR_SHAPE = -2
+FA_ERR_UNSUPPORTED = -3
+FA_ERR_ALIGN = -4
+FA_ERR_THRESHOLD = -5
+FA_ERR_CUDA = -6
+FA_ERR_DEVICE_TIMEOUT = -7
+FA_ERR_RANGE = -8
+FA_ERR_SCRATCH = -9
 
 
 class FaError(RuntimeError):

@@ -1,7 +1,7 @@
 // Elementwise kernels of the backward that materialises S, P, dP and dS per
-// (KV head, head of its group), with every product a plain library GEMM (bf16
-// tensor-core products with P and dS as bf16 hi + lo pairs for bf16 inputs,
-// fp32 products for fp16 inputs), accumulated in fp32:
+// (KV head, head of its group), with every product a tensor-core GEMM of the
+// inputs' 16-bit type accumulated in fp32; P and dS enter the products as
+// hi + lo pairs of that type:
 //   S = Q K^T,  P = exp(scale S - LSE),  dV += P^T dO,  dP = dO V^T,
 //   dS = P * (dP - d_row),  dQ = scale dS K,  dK += scale dS^T Q
 // (the steps of the BSA PyPTO implementation notes' backward: section 3.2
@@ -13,25 +13,6 @@
 #include "fa_ptx.cuh"
 
 namespace fa {
-
-// bf16 or fp16 -> fp32, n8 groups of 8 elements.
-template <bool kBF16>
-__global__ void __launch_bounds__(256) fa_bwd_to_f32_kernel(const uint4* __restrict__ in,
-                                                            float4* __restrict__ out, size_t n8) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const uint4 w = in[i];
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-    float f[8];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      f[2 * e] = kBF16 ? __uint_as_float(ww[e] << 16) : f16_lo_to_f32(ww[e]);
-      f[2 * e + 1] = kBF16 ? __uint_as_float(ww[e] & 0xFFFF0000u) : f16_hi_to_f32(ww[e]);
-    }
-    out[2 * i] = make_float4(f[0], f[1], f[2], f[3]);
-    out[2 * i + 1] = make_float4(f[4], f[5], f[6], f[7]);
-  }
-}
 
 // fp32 -> bf16 or fp16 (round to nearest even), n8 groups of 8 elements.
 template <bool kBF16>
@@ -58,54 +39,26 @@ struct BwdGemmRows {
   int g;                 // head of the group
   int row0;              // first row of the row block (grid.x counts rows from here)
   int ncols;             // keys [0, ncols) of the block's rows are written (the rest unused)
+  int* status;           // fp16 pairs: kStatusRange when a dS value is beyond the fp16 range
 };
 
-// P = exp(scale * s - LSE) over S in place (0 for masked keys, rows past the
-// batch's length and rows without keys).  Grid: (Sq, planes); a block walks
-// one row.
-__global__ void __launch_bounds__(256) fa_bwd_p_kernel(float* __restrict__ s, BwdGemmRows r) {
-  const int i = r.row0 + blockIdx.x;
-  const int z = blockIdx.y;
-  const int p = r.plane0 + z;
-  const int b = p / r.Hkv;
-  const int q_len = r.seqlens ? min(r.seqlens[b], r.Sq) : r.Sq;
-  const int kv_len = r.seqlens ? min(r.seqlens[b], r.Skv) : r.Skv;
-  const float lse = r.lse[(size_t)(p * r.G + r.g) * r.Sq + i];
-  const bool row_ok = i < q_len && lse != INFINITY;
-  int lim = row_ok ? kv_len : 0;                 // keys j < lim are seen
-  if (r.causal) lim = min(lim, i + 1);
-  float* row = s + ((size_t)z * r.Sq + i) * r.Skv;
-  for (int j = threadIdx.x; j < r.ncols; j += blockDim.x)
-    row[j] = j < lim ? expf(fmaf(row[j], r.scale, -lse)) : 0.f;
+// 16-bit operands of the tensor-core products: P = exp(scale * s - LSE), 0 on
+// masked keys, rows past the batch's length and rows without keys, split into
+// hi = P rounded to the inputs' type and lo = (P - hi) rounded, written to two
+// matrices of the batch's layout.  kV elements per thread and step: 8 (32-byte
+// loads, 16-byte stores) when Skv and ncols are multiples of 8, else 1.
+// Grid: (rows of the block, planes).
+template <bool kBF16>
+__device__ __forceinline__ float h16_to_f32(uint32_t h) {
+  return kBF16 ? __uint_as_float(h << 16) : f16_lo_to_f32(h);
 }
-
-// dS = P * (dP - d_row) over dP in place; exactly 0 where P is (masked keys,
-// padded rows: whatever dO holds there cannot reach dQ, dK or dV).
-// Grid: (Sq, planes).
-__global__ void __launch_bounds__(256) fa_bwd_ds_kernel(const float* __restrict__ pm,
-                                                        float* __restrict__ dp, BwdGemmRows r) {
-  const int i = r.row0 + blockIdx.x;
-  const int z = blockIdx.y;
-  const int p = r.plane0 + z;
-  const float d = r.d_row[(size_t)(p * r.G + r.g) * r.Sq + i];
-  const size_t base = ((size_t)z * r.Sq + i) * r.Skv;
-  for (int j = threadIdx.x; j < r.ncols; j += blockDim.x) {
-    const float pv = pm[base + j];
-    dp[base + j] = pv != 0.f ? pv * (dp[base + j] - d) : 0.f;
-  }
+template <bool kBF16>
+__device__ __forceinline__ void split_hilo(float x, uint32_t& hi, uint32_t& lo) {
+  hi = (kBF16 ? pack_bf16x2(x, 0.f) : pack_f16x2(x, 0.f)) & 0xFFFFu;
+  const float r = x - h16_to_f32<kBF16>(hi);
+  lo = (kBF16 ? pack_bf16x2(r, 0.f) : pack_f16x2(r, 0.f)) & 0xFFFFu;
 }
-
-// bf16 operands of the tensor-core products: P = exp(scale * s - LSE) (as
-// fa_bwd_p_kernel) split into hi = bf16(P) and lo = bf16(P - hi), written to
-// two bf16 matrices of the batch's layout.  kV elements per thread and step:
-// 8 (32-byte loads, 16-byte stores) when Skv and ncols are multiples of 8,
-// else 1.
-// Grid: (Sq, planes).
-__device__ __forceinline__ void bf16_hilo(float x, uint32_t& hi, uint32_t& lo) {
-  hi = pack_bf16x2(x, 0.f) & 0xFFFFu;
-  lo = pack_bf16x2(x - __uint_as_float(hi << 16), 0.f) & 0xFFFFu;
-}
-template <int kV>
+template <bool kBF16, int kV>
 __global__ void __launch_bounds__(256) fa_bwd_p_hilo_kernel(const float* __restrict__ s,
                                                             uint16_t* __restrict__ ph,
                                                             uint16_t* __restrict__ pl,
@@ -133,7 +86,8 @@ __global__ void __launch_bounds__(256) fa_bwd_p_hilo_kernel(const float* __restr
     }
     uint32_t h[kV], l[kV];
 #pragma unroll
-    for (int e = 0; e < kV; ++e) bf16_hilo(j0 + e < lim ? expf(fmaf(x[e], r.scale, -lse)) : 0.f, h[e], l[e]);
+    for (int e = 0; e < kV; ++e)
+      split_hilo<kBF16>(j0 + e < lim ? expf(fmaf(x[e], r.scale, -lse)) : 0.f, h[e], l[e]);
     if constexpr (kV == 8) {
       *reinterpret_cast<uint4*>(ph + base + j0) =
           make_uint4(h[0] | h[1] << 16, h[2] | h[3] << 16, h[4] | h[5] << 16, h[6] | h[7] << 16);
@@ -146,10 +100,12 @@ __global__ void __launch_bounds__(256) fa_bwd_p_hilo_kernel(const float* __restr
   }
 }
 
-// dS = P * (dP - d_row) with P = hi + lo read from the bf16 pair, written back
-// over the pair as bf16 hi and lo; exactly 0 where P is.  kV as above.
-// Grid: (Sq, planes).
-template <int kV>
+// dS = P * (dP - d_row) with P = hi + lo read from the pair, written back over
+// the pair as hi and lo of the inputs' type; exactly 0 where P is (masked
+// keys, padded rows: whatever dO holds there cannot reach dQ, dK or dV).  An
+// fp16 dS beyond the fp16 range sets kStatusRange.  kV as above.
+// Grid: (rows of the block, planes).
+template <bool kBF16, int kV>
 __global__ void __launch_bounds__(256) fa_bwd_ds_hilo_kernel(uint16_t* __restrict__ ph,
                                                              uint16_t* __restrict__ pl,
                                                              const float* __restrict__ dp,
@@ -167,20 +123,26 @@ __global__ void __launch_bounds__(256) fa_bwd_ds_hilo_kernel(uint16_t* __restric
       const uint32_t hw[4] = {hh.x, hh.y, hh.z, hh.w}, lw[4] = {ll.x, ll.y, ll.z, ll.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        pv[2 * e] = __uint_as_float(hw[e] << 16) + __uint_as_float(lw[e] << 16);
-        pv[2 * e + 1] = __uint_as_float(hw[e] & 0xFFFF0000u) + __uint_as_float(lw[e] & 0xFFFF0000u);
+        pv[2 * e] = h16_to_f32<kBF16>(hw[e] & 0xFFFFu) + h16_to_f32<kBF16>(lw[e] & 0xFFFFu);
+        pv[2 * e + 1] = h16_to_f32<kBF16>(hw[e] >> 16) + h16_to_f32<kBF16>(lw[e] >> 16);
       }
       const float4 a = *reinterpret_cast<const float4*>(dp + base + j0);
       const float4 c = *reinterpret_cast<const float4*>(dp + base + j0 + 4);
       dv[0] = a.x; dv[1] = a.y; dv[2] = a.z; dv[3] = a.w;
       dv[4] = c.x; dv[5] = c.y; dv[6] = c.z; dv[7] = c.w;
     } else {
-      pv[0] = __uint_as_float((uint32_t)ph[base + j0] << 16) + __uint_as_float((uint32_t)pl[base + j0] << 16);
+      pv[0] = h16_to_f32<kBF16>(ph[base + j0]) + h16_to_f32<kBF16>(pl[base + j0]);
       dv[0] = dp[base + j0];
     }
     uint32_t h[kV], l[kV];
+    bool big = false;
 #pragma unroll
-    for (int e = 0; e < kV; ++e) bf16_hilo(pv[e] != 0.f ? pv[e] * (dv[e] - d) : 0.f, h[e], l[e]);
+    for (int e = 0; e < kV; ++e) {
+      const float x = pv[e] != 0.f ? pv[e] * (dv[e] - d) : 0.f;
+      if (!kBF16) big |= !(fabsf(x) <= 65504.f);
+      split_hilo<kBF16>(x, h[e], l[e]);
+    }
+    if (!kBF16 && big) atomicOr(r.status, kStatusRange);
     if constexpr (kV == 8) {
       *reinterpret_cast<uint4*>(ph + base + j0) =
           make_uint4(h[0] | h[1] << 16, h[2] | h[3] << 16, h[4] | h[5] << 16, h[6] | h[7] << 16);

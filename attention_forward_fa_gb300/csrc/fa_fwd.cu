@@ -700,10 +700,10 @@ constexpr size_t kBwdGemmBytes = size_t(1) << 30;
 // keys up to its last row).
 constexpr int kBwdRowBlock = 512;
 
-// One cuBLAS handle per device, created on first use: fp32 products only
-// (pedantic math: no reduced-precision tensor-core paths) and no workspace,
-// so that calls on different streams share nothing on the device.  The mutex
-// covers a whole call's enqueue (the handle's stream is set per call).
+// One cuBLAS handle per device, created on first use: no reduced-precision
+// reductions inside the products and no workspace, so that calls on
+// different streams share nothing on the device.  The mutex covers a whole
+// call's enqueue (the handle's stream is set per call).
 std::mutex g_blas_mu;
 cublasHandle_t blas_handle() {
   static cublasHandle_t hs[64];
@@ -712,7 +712,9 @@ cublasHandle_t blas_handle() {
   if (!hs[dev]) {
     cublasHandle_t h = nullptr;
     if (cublasCreate(&h) != CUBLAS_STATUS_SUCCESS) return nullptr;
-    if (cublasSetMathMode(h, CUBLAS_PEDANTIC_MATH) != CUBLAS_STATUS_SUCCESS ||
+    if (cublasSetMathMode(h, cublasMath_t(CUBLAS_DEFAULT_MATH |
+                                          CUBLAS_MATH_DISALLOW_REDUCED_PRECISION_REDUCTION)) !=
+            CUBLAS_STATUS_SUCCESS ||
         cublasSetWorkspace(h, nullptr, 0) != CUBLAS_STATUS_SUCCESS) {
       cublasDestroy(h);
       return nullptr;
@@ -724,21 +726,14 @@ cublasHandle_t blas_handle() {
 
 // Row-major C[M, N] = alpha op(A) op(B) + beta C over `batch` strided
 // matrices (leading dimensions and strides in elements), as the column-major
-// product C^T = op(B)^T op(A)^T.
-bool gemm_rm(cublasHandle_t h, bool ta, bool tb, int M, int N, int K, float alpha, const float* A,
-             int lda, long long sA, const float* Bm, int ldb, long long sB, float beta, float* C,
-             int ldc, long long sC, int batch) {
-  return cublasSgemmStridedBatched(h, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N,
-                                   N, M, K, &alpha, Bm, ldb, sB, A, lda, sA, &beta, C, ldc, sC,
-                                   batch) == CUBLAS_STATUS_SUCCESS;
-}
-// The same with bf16 A and B (tensor-core products, exact in fp32) and fp32 C.
-bool gemm_rm_bf16(cublasHandle_t h, bool ta, bool tb, int M, int N, int K, float alpha,
-                  const uint16_t* A, int lda, long long sA, const uint16_t* Bm, int ldb,
-                  long long sB, float beta, float* C, int ldc, long long sC, int batch) {
+// product C^T = op(B)^T op(A)^T: A and B bf16 (or fp16) on the tensor cores,
+// products exact in fp32, C fp32.
+bool gemm_rm16(cublasHandle_t h, cudaDataType_t t, bool ta, bool tb, int M, int N, int K,
+               float alpha, const uint16_t* A, int lda, long long sA, const uint16_t* Bm, int ldb,
+               long long sB, float beta, float* C, int ldc, long long sC, int batch) {
   return cublasGemmStridedBatchedEx(h, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N,
-                                    N, M, K, &alpha, Bm, CUDA_R_16BF, ldb, sB, A, CUDA_R_16BF, lda,
-                                    sA, &beta, C, CUDA_R_32F, ldc, sC, batch, CUBLAS_COMPUTE_32F,
+                                    N, M, K, &alpha, Bm, t, ldb, sB, A, t, lda, sA, &beta, C,
+                                    CUDA_R_32F, ldc, sC, batch, CUBLAS_COMPUTE_32F,
                                     CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS;
 }
 
@@ -770,29 +765,26 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   cublasHandle_t h = blas_handle();
   if (!h || cublasSetStream(h, st) != CUBLAS_STATUS_SUCCESS) return cuda_fail(cudaErrorUnknown);
 
-  // bf16 inputs: S and dP straight from them on the tensor cores, P and dS as
-  // bf16 hi + lo pairs (about 16 significant bits) for dV, dQ and dK.  fp16
-  // inputs: fp32 copies and fp32 products throughout (an fp16 hi part could
-  // overflow on a large dS).  Both accumulate dQ, dK, dV in fp32.
-  const bool tc = !fp16;
-  const cublasMath_t math = tc ? cublasMath_t(CUBLAS_DEFAULT_MATH | CUBLAS_MATH_DISALLOW_REDUCED_PRECISION_REDUCTION)
-                               : CUBLAS_PEDANTIC_MATH;
-  if (cublasSetMathMode(h, math) != CUBLAS_STATUS_SUCCESS) return cuda_fail(cudaErrorUnknown);
+  // S and dP straight from the inputs on the tensor cores; P and dS as hi +
+  // lo pairs of the inputs' type (about 16 significant bits for bf16, 22 for
+  // fp16, whose lo parts reach the subnormals below 2^-14) for dV, dQ and dK;
+  // dQ, dK, dV accumulate in fp32.  An fp16 dS beyond 65504 sets the range
+  // bit of the status word.
+  const cudaDataType_t t16 = fp16 ? CUDA_R_16F : CUDA_R_16BF;
 
   // Stream-ordered scratch: d_row; fp32 dQ, dK, dV; S (then dP) of one batch
-  // of KV planes; with bf16 inputs the bf16 hi / lo of P (then dS), else fp32
-  // copies of Q, dO, K, V and a second fp32 matrix for P / dS.
+  // of KV planes in fp32 and the hi / lo pair of P (then dS).
   const int G = Hq / Hkv;
   const int planes = B * Hkv;
   const size_t nq = (size_t)B * Hq * Sq * D, nk = (size_t)B * Hkv * Skv * D;
   const size_t rows = (size_t)B * Hq * Sq;
   const size_t plane_mat = (size_t)Sq * Skv;
   const int chunk = (int)std::min<size_t>(
-      {(size_t)planes, (size_t)65535, std::max<size_t>(1, kBwdGemmBytes / (2 * plane_mat * 4))});
+      {(size_t)planes, (size_t)65535, std::max<size_t>(1, kBwdGemmBytes / (plane_mat * 8))});
   auto al = [](size_t b) { return (b + 255) & ~size_t(255); };
   const size_t b_row = al(rows * 4), b_q = al(nq * 4), b_k = al(nk * 4);
   const size_t b_m = al((size_t)chunk * plane_mat * 4), b_h = al((size_t)chunk * plane_mat * 2);
-  const size_t bytes = b_row + b_q + 2 * b_k + b_m + (tc ? 2 * b_h : 2 * b_q + 2 * b_k + b_m);
+  const size_t bytes = b_row + b_q + 2 * b_k + b_m + 2 * b_h;
   uint8_t* scratch = static_cast<uint8_t*>(scratch_alloc(bytes, st));
   if (!scratch) return cuda_fail(cudaGetLastError());
   uint8_t* c = scratch;
@@ -805,21 +797,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   c += 2 * b_k;
   float* sm = reinterpret_cast<float*>(c);
   c += b_m;
-  uint16_t* ph = nullptr;
-  uint16_t* pl = nullptr;
-  float *q32 = nullptr, *do32 = nullptr, *k32 = nullptr, *v32 = nullptr, *dpm = nullptr;
-  if (tc) {
-    ph = reinterpret_cast<uint16_t*>(c);
-    pl = reinterpret_cast<uint16_t*>(c + b_h);
-  } else {
-    q32 = reinterpret_cast<float*>(c);
-    do32 = reinterpret_cast<float*>(c + b_q);
-    c += 2 * b_q;
-    k32 = reinterpret_cast<float*>(c);
-    v32 = reinterpret_cast<float*>(c + b_k);
-    c += 2 * b_k;
-    dpm = reinterpret_cast<float*>(c);
-  }
+  uint16_t* ph = reinterpret_cast<uint16_t*>(c);
+  uint16_t* pl = reinterpret_cast<uint16_t*>(c + b_h);
 
   int rc = FA_OK;
   auto launched = [&]() {
@@ -827,13 +806,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
     if (e != cudaSuccess && rc == FA_OK) rc = cuda_fail(e);
     return rc == FA_OK;
   };
-  // fp32 copies (every row is a multiple of 8 elements: D = 64 or 128)
-  auto to32 = [&](const void* in, float* out, size_t n) {
-    const size_t n8 = n / 8;
-    const unsigned blocks = (unsigned)std::min<size_t>((n8 + 255) / 256, 4096);
-    fa::fa_bwd_to_f32_kernel<false><<<blocks, 256, 0, st>>>(static_cast<const uint4*>(in), reinterpret_cast<float4*>(out), n8);
-    return launched();
-  };
+  // every row is a multiple of 8 elements (D = 64 or 128)
   auto from32 = [&](const float* in, void* out, size_t n) {
     const size_t n8 = n / 8;
     const unsigned blocks = (unsigned)std::min<size_t>((n8 + 255) / 256, 4096);
@@ -841,8 +814,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
     else fa::fa_bwd_from_f32_kernel<true><<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(in), static_cast<uint4*>(out), n8);
     return launched();
   };
-  bool ok = tc || (to32(q, q32, nq) && to32(dout, do32, nq) && to32(k, k32, nk) && to32(v, v32, nk));
-  if (ok) {
+  bool ok = true;
+  {
     const cudaError_t e1 = cudaMemsetAsync(dk32, 0, nk * 4, st);
     const cudaError_t e2 = e1 == cudaSuccess ? cudaMemsetAsync(dv32, 0, nk * 4, st) : e1;
     if (e2 != cudaSuccess) {
@@ -879,55 +852,45 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
       for (int r0 = 0; ok && r0 < Sq; r0 += rb) {
         const int r1 = std::min(Sq, r0 + rb), nr = r1 - r0;
         const int nc = causal ? std::min(Skv, r1) : Skv;   // keys [0, nc) of these rows
-        fa::BwdGemmRows r{lse, d_row, seqlens, Hkv, G, Sq, Skv, causal, scale, p0, g, r0, nc};
+        fa::BwdGemmRows r{lse, d_row, seqlens, Hkv, G, Sq, Skv, causal, scale, p0, g, r0, nc,
+                          status};
         const dim3 eg(nr, np);
         const long long qr = qo + (long long)r0 * D;       // the block's rows of Q, dO, dQ
         const long long mr = (long long)r0 * Skv;           // ... of S, P, dP, dS
         const bool vec = Skv % 8 == 0 && nc % 8 == 0;
-        if (tc) {
-          ok = gemm_rm_bf16(h, false, true, nr, nc, D, 1.f, q16 + qr, D, sQ, k16 + ko, D, sK,
-                            0.f, sm + mr, Skv, sM, np);                       // S = Q K^T
-          if (ok) {
-            if (vec) fa::fa_bwd_p_hilo_kernel<8><<<eg, 256, 0, st>>>(sm, ph, pl, r);
-            else fa::fa_bwd_p_hilo_kernel<1><<<eg, 256, 0, st>>>(sm, ph, pl, r);   // P = hi + lo
-            ok = launched();
-          }
-          for (int part = 0; ok && part < 2; ++part)                         // dV += P^T dO
-            ok = gemm_rm_bf16(h, true, false, nc, D, nr, 1.f, (part ? pl : ph) + mr, Skv, sM,
-                              do16 + qr, D, sQ, 1.f, dv32 + ko, D, sK, np);
-          if (ok) ok = gemm_rm_bf16(h, false, true, nr, nc, D, 1.f, do16 + qr, D, sQ, v16 + ko,
-                                    D, sK, 0.f, sm + mr, Skv, sM, np);      // dP = dO V^T
-          if (ok) {
-            if (vec) fa::fa_bwd_ds_hilo_kernel<8><<<eg, 256, 0, st>>>(ph, pl, sm, r);
-            else fa::fa_bwd_ds_hilo_kernel<1><<<eg, 256, 0, st>>>(ph, pl, sm, r);  // dS = hi + lo
-            ok = launched();
-          }
-          for (int part = 0; ok && part < 2; ++part)                         // dQ = scale dS K
-            ok = gemm_rm_bf16(h, false, false, nr, D, nc, scale, (part ? pl : ph) + mr, Skv, sM,
-                              k16 + ko, D, sK, part ? 1.f : 0.f, dq32 + qr, D, sQ, np);
-          for (int part = 0; ok && part < 2; ++part)                         // dK += scale dS^T Q
-            ok = gemm_rm_bf16(h, true, false, nc, D, nr, scale, (part ? pl : ph) + mr, Skv, sM,
-                              q16 + qr, D, sQ, 1.f, dk32 + ko, D, sK, np);
-        } else {
-          ok = gemm_rm(h, false, true, nr, nc, D, 1.f, q32 + qr, D, sQ, k32 + ko, D, sK, 0.f,
+        ok = gemm_rm16(h, t16, false, true, nr, nc, D, 1.f, q16 + qr, D, sQ, k16 + ko, D, sK, 0.f,
                        sm + mr, Skv, sM, np);                                 // S = Q K^T
-          if (ok) {
-            fa::fa_bwd_p_kernel<<<eg, 256, 0, st>>>(sm, r);                   // P
-            ok = launched();
+        if (ok) {                                                             // P = hi + lo
+          if (fp16) {
+            if (vec) fa::fa_bwd_p_hilo_kernel<false, 8><<<eg, 256, 0, st>>>(sm, ph, pl, r);
+            else fa::fa_bwd_p_hilo_kernel<false, 1><<<eg, 256, 0, st>>>(sm, ph, pl, r);
+          } else {
+            if (vec) fa::fa_bwd_p_hilo_kernel<true, 8><<<eg, 256, 0, st>>>(sm, ph, pl, r);
+            else fa::fa_bwd_p_hilo_kernel<true, 1><<<eg, 256, 0, st>>>(sm, ph, pl, r);
           }
-          if (ok) ok = gemm_rm(h, true, false, nc, D, nr, 1.f, sm + mr, Skv, sM, do32 + qr, D,
-                               sQ, 1.f, dv32 + ko, D, sK, np);              // dV += P^T dO
-          if (ok) ok = gemm_rm(h, false, true, nr, nc, D, 1.f, do32 + qr, D, sQ, v32 + ko, D,
-                               sK, 0.f, dpm + mr, Skv, sM, np);               // dP = dO V^T
-          if (ok) {
-            fa::fa_bwd_ds_kernel<<<eg, 256, 0, st>>>(sm, dpm, r);             // dS
-            ok = launched();
-          }
-          if (ok) ok = gemm_rm(h, false, false, nr, D, nc, scale, dpm + mr, Skv, sM, k32 + ko,
-                               D, sK, 0.f, dq32 + qr, D, sQ, np);         // dQ = scale dS K
-          if (ok) ok = gemm_rm(h, true, false, nc, D, nr, scale, dpm + mr, Skv, sM, q32 + qr,
-                               D, sQ, 1.f, dk32 + ko, D, sK, np);         // dK += scale dS^T Q
+          ok = launched();
         }
+        for (int part = 0; ok && part < 2; ++part)                           // dV += P^T dO
+          ok = gemm_rm16(h, t16, true, false, nc, D, nr, 1.f, (part ? pl : ph) + mr, Skv, sM,
+                         do16 + qr, D, sQ, 1.f, dv32 + ko, D, sK, np);
+        if (ok) ok = gemm_rm16(h, t16, false, true, nr, nc, D, 1.f, do16 + qr, D, sQ, v16 + ko, D,
+                               sK, 0.f, sm + mr, Skv, sM, np);               // dP = dO V^T
+        if (ok) {                                                             // dS = hi + lo
+          if (fp16) {
+            if (vec) fa::fa_bwd_ds_hilo_kernel<false, 8><<<eg, 256, 0, st>>>(ph, pl, sm, r);
+            else fa::fa_bwd_ds_hilo_kernel<false, 1><<<eg, 256, 0, st>>>(ph, pl, sm, r);
+          } else {
+            if (vec) fa::fa_bwd_ds_hilo_kernel<true, 8><<<eg, 256, 0, st>>>(ph, pl, sm, r);
+            else fa::fa_bwd_ds_hilo_kernel<true, 1><<<eg, 256, 0, st>>>(ph, pl, sm, r);
+          }
+          ok = launched();
+        }
+        for (int part = 0; ok && part < 2; ++part)                           // dQ = scale dS K
+          ok = gemm_rm16(h, t16, false, false, nr, D, nc, scale, (part ? pl : ph) + mr, Skv, sM,
+                         k16 + ko, D, sK, part ? 1.f : 0.f, dq32 + qr, D, sQ, np);
+        for (int part = 0; ok && part < 2; ++part)                           // dK += scale dS^T Q
+          ok = gemm_rm16(h, t16, true, false, nc, D, nr, scale, (part ? pl : ph) + mr, Skv, sM,
+                         q16 + qr, D, sQ, 1.f, dk32 + ko, D, sK, np);
       }
       if (!ok && rc == FA_OK) rc = cuda_fail(cudaErrorUnknown);
     }

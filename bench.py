@@ -474,8 +474,9 @@ def other_workloads(args, dev, dist, world, local, peak):
     return out
 
 
-def backward_workload(args, dev, dist, world, local, peak):
-    """fa_bwd on the benchmark's workload (B2 H16 S2048 D128 causal, bf16),
+def backward_workload(args, dev, dist, world, local, peak, dtype="bf16"):
+    """fa_bwd on the benchmark's workload (B2 H16 S2048 D128 causal, bf16, or
+    the same draws rounded to fp16 with dtype="fp16"),
     after one fa_fwd_o_lo call that provides o, its residual and the LSE, with
     a seeded upstream gradient: K calls between a barrier + synchronize, CUDA
     events around them, clocks sampled from an untimed soak on.  Reported
@@ -485,7 +486,7 @@ def backward_workload(args, dev, dist, world, local, peak):
     import torch
     import attention_forward_fa_gb300 as fa
     from attention_forward_fa_gb300 import workloads as W
-    p = workload_problem("c2")
+    p = workload_problem("c2") if dtype == "bf16" else W.config(2, dtype=dtype)
     flops = 2.5 * W.algorithmic_flops(p)
     tdt = torch.bfloat16 if p.dtype == "bf16" else torch.float16
     to = lambda bits: torch.from_numpy(bits.view(np.int16).copy()).to(dev).view(tdt)  # noqa: E731
@@ -528,12 +529,15 @@ def backward_workload(args, dev, dist, world, local, peak):
     ms = max_over_ranks(dist, [e0.elapsed_time(e1) / steps], dev)[0]
     achieved = flops / (ms * 1e-3) / 1e12
     cfg = workload_desc(p, "c2")
+    cfg["dtype"] = p.dtype
+    if p.dtype != "bf16":
+        cfg["workload"] = cfg["workload"].replace("bf16", p.dtype)
     cfg["pass"] = "backward: dQ, dK, dV from q, k, v, o + o_lo, LSE and a seeded N(0,1) upstream gradient"
     return {"config": cfg,
             "algorithmic_gflop": flops / 1e9, "ms_per_call": ms,
             "tflops": whole_job_tflops(world, flops, ms), "frac": achieved / peak, "steps": steps,
-            "kernel": "fa_bwd: d_row, then per batch of (KV head, group head) planes cuBLAS bf16 "
-                      "tensor-core GEMMs (fp32 accumulation) for S, dP and, with P and dS as bf16 "
+            "kernel": f"fa_bwd: d_row, then per batch of (KV head, group head) planes cuBLAS {p.dtype} "
+                      f"tensor-core GEMMs (fp32 accumulation) for S, dP and, with P and dS as {p.dtype} "
                       "hi + lo pairs, dV, dQ, dK; this library's P, dS and conversion kernels",
             "timing": "eager, events around the K calls", "clocks": clocks}
 
@@ -559,14 +563,17 @@ def run_ours(args, world, rank, local):
         # the backward entry of the c2 line on its own (a short run to profile)
         peaks, _ = measured_peaks()
         args.workload_steps, args.workload_soak = args.steps, args.soak
-        e = backward_workload(args, dev, dist, world, local, float(peaks["bf16_tflops"]))
+        # fp16 tensor-core products run at the bf16 rate: the same peak
+        e = backward_workload(args, dev, dist, world, local, float(peaks["bf16_tflops"]),
+                              dtype="fp16" if args.fp16 else "bf16")
         if rank == 0:
             print(json.dumps({"metric": "attention bwd TFLOP/s on 1 GB300 (algorithmic) and % of dense "
                                         "BF16 tensor peak; ms/call",
                               "value": e["tflops"], "unit": "TFLOP/s", "n_gpus": world,
                               "steps": e["steps"], "warmup": 3, "ms_per_step": e["ms_per_call"],
                               "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                              "dtype": "bf16", "data": "synthetic", **{k: e[k] for k in e
+                              "dtype": "fp16" if args.fp16 else "bf16", "data": "synthetic",
+                              **{k: e[k] for k in e
                                                                       if k not in ("tflops", "steps")}}))
         if dist:
             dist.destroy_process_group()
@@ -735,6 +742,8 @@ def main():
                          "on the other workloads")
     ap.add_argument("--backward", action="store_true",
                     help="time only the backward (fa_bwd) on the c2 workload, its own JSON line")
+    ap.add_argument("--fp16", action="store_true",
+                    help="with --backward: the same workload's draws rounded to fp16")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -74,7 +74,8 @@ extern "C" {
 #define FA_ERR_DEVICE_TIMEOUT  -7  /* a bounded on-chip wait expired (kernel bailed)  */
 #define FA_ERR_RANGE           -8  /* a bf16 value outside the fp16 range (|x| >      */
                                    /* 65504) met an fp16 product (V; with top-k also  */
-                                   /* Q and the key latent)                           */
+                                   /* Q and the key latent), or fa_bwd with fp16      */
+                                   /* inputs met a dS beyond that range               */
 #define FA_ERR_SCRATCH         -9  /* fa_fwd_noalloc, top-k: the bf16 key latent     */
                                    /* needs more than its fixed scratch               */
                                    /* (B*Skv*D*2 > 32 MiB)                            */
@@ -305,14 +306,15 @@ int fa_fwd_o_lo(const void* q, const void* k, const void* v, void* o, void* o_lo
  * FA_DTYPE_FP16; seqlens as fa_fwd.  D = Dv, 64 or 128 (FA_ERR_UNSUPPORTED
  * otherwise).  Rows past a batch's length get zero gradients.  S, P, dP and
  * dS are materialised for a batch of (KV head, head of its group) planes at a
- * time and every product is a cuBLAS GEMM accumulating in fp32: bf16 inputs
- * on the tensor cores (S and dP exact, P and dS as bf16 hi + lo pairs), fp16
- * inputs in fp32.  Stream-ordered scratch (cudaMallocAsync, freed on
- * `stream`): d_row; fp32 dq, dk, dv; 8 * Sq * Skv bytes per plane of a batch,
- * batches of up to 1 GiB (at least one plane); with fp16 inputs also fp32
- * copies of q, k, v, dout and 4 * Sq * Skv more bytes per plane.  Calls from several host
- * threads serialise their enqueueing on one lock per process.  Returns FA_OK
- * or a negative FA_ERR_* code (nothing launched on an argument error). */
+ * time and every product is a cuBLAS tensor-core GEMM of the inputs' type
+ * accumulating in fp32 (S and dP exact, P and dS as hi + lo pairs of that
+ * type).  With fp16 inputs a |dS| beyond 65504 cannot be held by the pair:
+ * the gradients are then not finite and fa_check_status() reports
+ * FA_ERR_RANGE.  Stream-ordered scratch (cudaMallocAsync, freed on `stream`):
+ * d_row; fp32 dq, dk, dv; 8 * Sq * Skv bytes per plane of a batch, batches of
+ * up to 1 GiB (at least one plane).  Calls from several host threads
+ * serialise their enqueueing on one lock per process.  Returns FA_OK or a
+ * negative FA_ERR_* code (nothing launched on an argument error). */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* o_lo,
            const float* lse, const void* dout, void* dq, void* dk, void* dv, int B, int Hq,
            int Hkv, int Sq, int Skv, int D, int Dv, float scale, int mask_mode,

@@ -235,3 +235,20 @@ def call_fp8(lib, **kw):
 ])
 def test_fp8_argument_errors(lib, kw, code):
     assert call_fp8(lib, **kw) == code
+
+
+def test_binding_constants_match_the_header():
+    """Every FA_* integer #define of include/fa_fwd.h has the same value in the
+    Python binding."""
+    import re
+    from pathlib import Path
+    import attention_forward_fa_gb300._binding as B
+
+    text = (Path(__file__).resolve().parents[1] / "include" / "fa_fwd.h").read_text()
+    found = re.findall(r"^#define\s+(FA_[A-Z0-9_]+)\s+(-?(?:0x[0-9A-Fa-f]+|\d+))\b", text, re.M)
+    assert len(found) >= 10
+    for name, val in found:
+        if hasattr(B, name):
+            assert getattr(B, name) == int(val, 0), name
+    for name in ("FA_OK", "FA_ERR_RANGE", "FA_ERR_DEVICE_TIMEOUT", "FA_MASK_CAUSAL", "FA_DTYPE_FP16"):
+        assert name in dict(found), name

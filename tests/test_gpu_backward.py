@@ -7,8 +7,9 @@ oracle.backward.attention_bwd evaluated on the exact forward (oracle O and
 LSE) under the BSA PyPTO implementation notes' tolerances (section 6.1: atol
 1e-4, rtol 7.8125e-3, the same bound as the forward's).  The recomputation
 P = exp(scale S - LSE) and the precomputed d_row = rowsum(dO * (o + o_lo))
-follow the notes' sections 3.2 and 8.4; fa_bwd materialises S, P, dP and dS
-per batch of heads in fp32, with fp32 GEMMs for the products.
+follow the notes' sections 3.2 and 8.4; fa_bwd materialises S and dP per
+batch of heads in fp32 from 16-bit tensor-core GEMMs, and P and dS as hi + lo
+pairs of the inputs' type for the products that take them.
 """
 import numpy as np
 import pytest
@@ -91,6 +92,86 @@ def test_backward_benchmark_workload_sampled_heads():
     p = W.config(2)
     g, ref = _run(p, heads=[0, 7, 15])
     _check(g, ref, "c2 heads 0, 7, 15")
+
+
+def test_backward_benchmark_workload_fp16_sampled_heads():
+    """The benchmark workload's shape in fp16 (fp16 GEMMs, fp16 hi + lo pairs
+    whose lo parts reach the subnormals): every element of heads 0 and 15."""
+    p = W.dense(name="c2_fp16", B=2, Hq=16, Sq=2048, D=128, mask=W.MASK_CAUSAL, dtype="fp16",
+                seed=42)
+    g, ref = _run(p, heads=[0, 15])
+    _check(g, ref, "c2 shape fp16, heads 0, 15")
+
+
+def _large_ds_inputs(dtype):
+    """Q, K = 0.25 * N(0, 1) (S within +-0.1: P nearly uniform over each
+    causal row's keys), V = 256 * random signs, dO = 256: dP - d_row reaches
+    ~1e6, so dS = P (dP - d_row) passes 65504 on the first rows of every head
+    (P ~ 1/2, 1/3, ...).  Values are rounded to `dtype` first, so both sides
+    see the same inputs."""
+    rng = np.random.default_rng(43)
+    B, H, S, D = 1, 2, 128, 64
+    rnd = lambda x: W.bits_to_f64(W.to_bits(x, dtype), dtype)  # noqa: E731
+    q = rnd(0.25 * rng.standard_normal((B, H, S, D)))
+    k = rnd(0.25 * rng.standard_normal((B, H, S, D)))
+    v = 256.0 * rng.choice([-1.0, 1.0], size=(B, H, S, D))
+    do = np.full((B, H, S, D), 256.0)
+    return q, k, v, do
+
+
+def _max_abs_ds(q, k, v, do):
+    """max |dS| of the inputs above in fp64 (the precondition of the range
+    test: P recomputed densely, causal, d_row from the exact O)."""
+    scale = 1.0 / np.sqrt(q.shape[-1])
+    s = np.einsum("bhid,bhjd->bhij", q, k) * scale
+    s = np.where(np.tril(np.ones(s.shape[-2:], dtype=bool)), s, -np.inf)
+    p = np.exp(s - s.max(-1, keepdims=True))
+    p /= p.sum(-1, keepdims=True)
+    dp = np.einsum("bhid,bhjd->bhij", do, v)
+    o = np.einsum("bhij,bhjd->bhid", p, v)
+    return float(np.abs(p * (dp - (do * o).sum(-1, keepdims=True))).max())
+
+
+def _large_ds_run(dtype):
+    import torch
+    import attention_forward_fa_gb300 as fa
+
+    q, k, v, do = _large_ds_inputs(dtype)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    t = [torch.from_numpy(x).to(tdt).cuda().contiguous() for x in (q, k, v, do)]
+    o, lse, o_lo = fa.flash_attention_forward(t[0], t[1], t[2], causal=True, o_lo=True)
+    code = fa.fa_check_status()
+    assert code == 0, fa.fa_strerror(code)
+    dq, dk, dv = fa.flash_attention_backward(t[0], t[1], t[2], o, lse, t[3], o_lo=o_lo, causal=True)
+    code = fa.fa_check_status()
+    return code, (q, k, v, do), [x.float().cpu().double().numpy() for x in (dq, dk, dv)]
+
+
+def test_backward_fp16_ds_beyond_range_is_reported():
+    """fp16 inputs whose dS passes the fp16 range: fa_check_status reports
+    FA_ERR_RANGE after the backward (the inputs themselves are in range)."""
+    import attention_forward_fa_gb300 as fa
+
+    assert _max_abs_ds(*_large_ds_inputs("fp16")) > 65504.0
+    code, _, _ = _large_ds_run("fp16")
+    assert code == fa.FA_ERR_RANGE, fa.fa_strerror(code)
+
+
+def test_backward_bf16_large_ds_matches_oracle():
+    """The same inputs in bf16 (no range limit below fp32's): dS ~ 1e5.  They
+    are the O(1) problem V = +-1, dO = 1 with V and dO scaled by 2^8; the
+    gradients are linear in each, so dQ and dK scale by 2^16 and dV by 2^8
+    (exactly, in floating point too).  The usual bound, which is stated for
+    O(1) data, applies to the gradients scaled back."""
+    code, (q, k, v, do), g = _large_ds_run("bf16")
+    assert code == 0
+    scale = 1.0 / np.sqrt(q.shape[-1])
+    O, L = A.attention_fwd(q, k, v, scale, mask=W.MASK_CAUSAL)
+    ref = BW.attention_bwd(q, k, v, O, L, do, scale, mask=W.MASK_CAUSAL)
+    assert _max_abs_ds(q, k, v, do) > 65504.0
+    assert min(float(np.abs(r).max()) for r in ref) > 1e3
+    back = (2.0 ** -16, 2.0 ** -16, 2.0 ** -8)
+    _check([x * f for x, f in zip(g, back)], [r * f for r, f in zip(ref, back)], "large dS bf16")
 
 
 def test_backward_across_several_plane_batches():
