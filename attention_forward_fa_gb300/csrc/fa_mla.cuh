@@ -111,6 +111,12 @@ struct MlaSmem {
 // other box of a key row is an X box.
 __device__ __forceinline__ bool mla_is_v_box(int bx, int half) { return (bx >> 2) == half && bx < 8; }
 
+// Waits until at most one committed group of this thread's cp.async copies
+// is pending (the producers keep two regions in flight).
+__device__ __forceinline__ void cp_async_wait_one_pending() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+
 // One part of Q K^T for a tile: the steps over the X boxes (kV false, the
 // first steps of the product) or over the V boxes (k-step kk covers query
 // columns 16 kk .. 16 kk + 15: box kk / 4).  Query columns below 320 come from
@@ -491,51 +497,65 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   } else if (warp < kMlaMmaWarp) {
     // ============================================================ producers
     // All three warps copy every tile j into stage j % 2: warp 4 + w the row
-    // groups w, w + 3, w + 6, ... (four rows each).  First the X boxes,
-    // once Q K^T of the tile two back has read them, then the V boxes, once
-    // its P.V has.  Each lane copies 16-byte chunks (4 rows x 128 bytes per
-    // warp instruction, so every 128-byte line is read whole) to their
-    // 128-byte-swizzle positions; the warp waits for its copies, fences them
-    // for the tensor core (async proxy) and arrives on the region's full
-    // barrier.  The first use of each stage waits for the Q staging instead.
+    // groups w, w + 3, w + 6, ... (four rows each).  A tile is two regions,
+    // taken in order: its X boxes, once Q K^T of the tile two back has read
+    // them, then its V boxes, once its P.V has.  Each lane copies 16-byte
+    // chunks (4 rows x 128 bytes per warp instruction, so every 128-byte line
+    // is read whole) to their 128-byte-swizzle positions, one commit group per
+    // region.  Two regions are in flight: after issuing region r the warp
+    // waits for region r - 1's group only, fences it for the tensor core
+    // (async proxy) and arrives on its full barrier.  (Region r's empty
+    // barrier never waits on region r - 1's full one: X of tile j frees with
+    // Q K^T of tile j - 2 and V with P.V of tile j - 2, both issued before
+    // tile j is needed.)  The first use of each stage waits for the Q staging
+    // instead.
     const int w = warp - 4;
     const int sub = lane >> 3;       // row within a group of four
     const int chunk = lane & 7;      // 16-byte chunk within a 128-byte row
     bool ab = false;
+    auto full_bar = [&](int r) { return (r & 1) ? BAR_FULL_V((r >> 1) % kMlaNS) : BAR_FULL_X((r >> 1) % kMlaNS); };
+    int r = 0;
 #pragma unroll 1
-    for (int j = 0; j < nt && !ab; ++j) {
+    for (; r < 2 * nt; ++r) {
+      const int j = r >> 1, region = r & 1;
       const int s = j % kMlaNS, use = j / kMlaNS;
       const uint32_t stage = sRing + s * SM::kStageBytes;
-#pragma unroll 1
-      for (int region = 0; region < 2 && !ab; ++region) {
-        if (lane == 0) {
-          if (use == 0) {
-            ab = region == 0 && !wait_bar(BAR_QDONE, 0, wc);             // Q staging consumed
-          } else {
-            ab = !wait_bar(region ? BAR_EMPTY_V(s) : BAR_EMPTY_X(s), (use - 1) & 1, wc);
-          }
+      if (lane == 0) {
+        if (use == 0) {
+          ab = region == 0 && !wait_bar(BAR_QDONE, 0, wc);               // Q staging consumed
+        } else {
+          ab = !wait_bar(region ? BAR_EMPTY_V(s) : BAR_EMPTY_X(s), (use - 1) & 1, wc);
         }
-        ab = __shfl_sync(0xffffffffu, ab, 0);
-        if (ab) break;
+      }
+      ab = __shfl_sync(0xffffffffu, ab, 0);
+      if (ab) break;
 #pragma unroll 1
-        for (int g = w; g < kMlaN / 4; g += kMlaProducers) {
-          // positions past the last key repeat a valid row (their scores are masked)
-          const int row = 4 * g + sub;
-          const int pos = j * kMlaN + row;
-          const int key = s_idx[pos < nkeys ? pos : nkeys - 1];
-          const uint16_t* src = p.kl + ((size_t)b * p.Skv + key) * kMlaD + chunk * 8;
-          const uint32_t dst = stage + row * 128 + ((chunk ^ (row & 7)) << 4);
+      for (int g = w; g < kMlaN / 4; g += kMlaProducers) {
+        // positions past the last key repeat a valid row (their scores are masked)
+        const int row = 4 * g + sub;
+        const int pos = j * kMlaN + row;
+        const int key = s_idx[pos < nkeys ? pos : nkeys - 1];
+        const uint16_t* src = p.kl + ((size_t)b * p.Skv + key) * kMlaD + chunk * 8;
+        const uint32_t dst = stage + row * 128 + ((chunk ^ (row & 7)) << 4);
 #pragma unroll
-          for (int bx = 0; bx < kMlaBoxes; ++bx)
-            if (mla_is_v_box(bx, half) == (region == 1))
-              cp_async16(dst + bx * SM::kBoxBytes, src + bx * 64);
-        }
-        cp_async_commit();
-        cp_async_wait_all();
+        for (int bx = 0; bx < kMlaBoxes; ++bx)
+          if (mla_is_v_box(bx, half) == (region == 1))
+            cp_async16(dst + bx * SM::kBoxBytes, src + bx * 64);
+      }
+      cp_async_commit();
+      if (r > 0) {
+        cp_async_wait_one_pending();   // region r - 1 landed
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(region ? BAR_FULL_V(s) : BAR_FULL_X(s));
+        if (lane == 0) mbar_arrive(full_bar(r - 1));
       }
+    }
+    // the last region issued (or, after an abort, every copy in flight)
+    cp_async_wait_all();
+    if (!ab && r > 0) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(full_bar(r - 1));
     }
     // the Q tile's copy must land before the CTA's shared memory goes away
     if (w == 0 && lane == 0 && live) drain_bar(BAR_QFULL, 0, wc.timeout);
