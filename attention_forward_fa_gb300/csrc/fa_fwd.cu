@@ -1081,7 +1081,7 @@ const char* fa_strerror(int code) {
     case FA_ERR_THRESHOLD: return "rescale_threshold outside [0, 15]";
     case FA_ERR_CUDA: return "CUDA call failed";
     case FA_ERR_DEVICE_TIMEOUT: return "bounded on-chip wait expired";
-    case FA_ERR_RANGE: return "bf16 V value outside the fp16 range";
+    case FA_ERR_RANGE: return "value outside the fp16 range in an fp16 product (bf16 V, top-k Q or latent; fp16 backward dS)";
     case FA_ERR_SCRATCH: return "bf16 key latent larger than the fixed scratch of fa_fwd_noalloc (32 MiB fp16)";
     default: return "unknown error code";
   }

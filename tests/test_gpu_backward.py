@@ -163,8 +163,10 @@ def test_backward_bf16_large_ds_matches_oracle():
     gradients are linear in each, so dQ and dK scale by 2^16 and dV by 2^8
     (exactly, in floating point too).  The usual bound, which is stated for
     O(1) data, applies to the gradients scaled back."""
+    import attention_forward_fa_gb300 as fa
+
     code, (q, k, v, do), g = _large_ds_run("bf16")
-    assert code == 0
+    assert code == 0, fa.fa_strerror(code)
     scale = 1.0 / np.sqrt(q.shape[-1])
     O, L = A.attention_fwd(q, k, v, scale, mask=W.MASK_CAUSAL)
     ref = BW.attention_bwd(q, k, v, O, L, do, scale, mask=W.MASK_CAUSAL)
