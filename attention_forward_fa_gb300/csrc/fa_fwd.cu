@@ -767,13 +767,14 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
 
   // S and dP straight from the inputs on the tensor cores; P and dS as hi +
   // lo pairs of the inputs' type (about 16 significant bits for bf16, 22 for
-  // fp16, whose lo parts reach the subnormals below 2^-14) for dV, dQ and dK;
-  // dQ, dK, dV accumulate in fp32.  An fp16 dS beyond 65504 sets the range
-  // bit of the status word.
+  // fp16, whose lo parts reach the subnormals below 2^-14), written in place
+  // over S and dP, for dV, dQ and dK; dQ, dK, dV accumulate in fp32.  An fp16
+  // dS beyond 65504 sets the range bit of the status word.
   const cudaDataType_t t16 = fp16 ? CUDA_R_16F : CUDA_R_16BF;
 
-  // Stream-ordered scratch: d_row; fp32 dQ, dK, dV; S (then dP) of one batch
-  // of KV planes in fp32 and the hi / lo pair of P (then dS).
+  // Stream-ordered scratch: d_row; fp32 dQ; fp32 dK2 and dV2 (two rows per
+  // key: its hi and lo parts); K2 (every row of K twice); S and dP of one
+  // batch of KV planes in fp32 (then the P and dS pairs).
   const int G = Hq / Hkv;
   const int planes = B * Hkv;
   const size_t nq = (size_t)B * Hq * Sq * D, nk = (size_t)B * Hkv * Skv * D;
@@ -782,9 +783,9 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   const int chunk = (int)std::min<size_t>(
       {(size_t)planes, (size_t)65535, std::max<size_t>(1, kBwdGemmBytes / (plane_mat * 8))});
   auto al = [](size_t b) { return (b + 255) & ~size_t(255); };
-  const size_t b_row = al(rows * 4), b_q = al(nq * 4), b_k = al(nk * 4);
-  const size_t b_m = al((size_t)chunk * plane_mat * 4), b_h = al((size_t)chunk * plane_mat * 2);
-  const size_t bytes = b_row + b_q + 2 * b_k + b_m + 2 * b_h;
+  const size_t b_row = al(rows * 4), b_q = al(nq * 4), b_k2 = al(2 * nk * 4), b_kk = al(2 * nk * 2);
+  const size_t b_m = al((size_t)chunk * plane_mat * 4);
+  const size_t bytes = b_row + b_q + 2 * b_k2 + b_kk + 2 * b_m;
   uint8_t* scratch = static_cast<uint8_t*>(scratch_alloc(bytes, st));
   if (!scratch) return cuda_fail(cudaGetLastError());
   uint8_t* c = scratch;
@@ -792,13 +793,13 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   c += b_row;
   float* dq32 = reinterpret_cast<float*>(c);
   c += b_q;
-  float* dk32 = reinterpret_cast<float*>(c);
-  float* dv32 = reinterpret_cast<float*>(c + b_k);
-  c += 2 * b_k;
+  float* dk2 = reinterpret_cast<float*>(c);
+  float* dv2 = reinterpret_cast<float*>(c + b_k2);
+  c += 2 * b_k2;
+  uint16_t* k2 = reinterpret_cast<uint16_t*>(c);
+  c += b_kk;
   float* sm = reinterpret_cast<float*>(c);
-  c += b_m;
-  uint16_t* ph = reinterpret_cast<uint16_t*>(c);
-  uint16_t* pl = reinterpret_cast<uint16_t*>(c + b_h);
+  float* dpm = reinterpret_cast<float*>(c + b_m);
 
   int rc = FA_OK;
   auto launched = [&]() {
@@ -807,21 +808,36 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
     return rc == FA_OK;
   };
   // every row is a multiple of 8 elements (D = 64 or 128)
+  auto grid8 = [](size_t n8) { return (unsigned)std::min<size_t>((n8 + 255) / 256, 4096); };
   auto from32 = [&](const float* in, void* out, size_t n) {
     const size_t n8 = n / 8;
-    const unsigned blocks = (unsigned)std::min<size_t>((n8 + 255) / 256, 4096);
-    if (fp16) fa::fa_bwd_from_f32_kernel<false><<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(in), static_cast<uint4*>(out), n8);
-    else fa::fa_bwd_from_f32_kernel<true><<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(in), static_cast<uint4*>(out), n8);
+    const auto* i4 = reinterpret_cast<const float4*>(in);
+    auto* o4 = static_cast<uint4*>(out);
+    if (fp16) fa::fa_bwd_from_f32_kernel<false><<<grid8(n8), 256, 0, st>>>(i4, o4, n8);
+    else fa::fa_bwd_from_f32_kernel<true><<<grid8(n8), 256, 0, st>>>(i4, o4, n8);
+    return launched();
+  };
+  auto from32_pairs = [&](const float* in, void* out, size_t n) {   // n output elements
+    const size_t n8 = n / 8;
+    const auto* i4 = reinterpret_cast<const float4*>(in);
+    auto* o4 = static_cast<uint4*>(out);
+    if (fp16) fa::fa_bwd_from_f32_pairs_kernel<false><<<grid8(n8), 256, 0, st>>>(i4, o4, n8, D);
+    else fa::fa_bwd_from_f32_pairs_kernel<true><<<grid8(n8), 256, 0, st>>>(i4, o4, n8, D);
     return launched();
   };
   bool ok = true;
   {
-    const cudaError_t e1 = cudaMemsetAsync(dk32, 0, nk * 4, st);
-    const cudaError_t e2 = e1 == cudaSuccess ? cudaMemsetAsync(dv32, 0, nk * 4, st) : e1;
+    const cudaError_t e1 = cudaMemsetAsync(dk2, 0, 2 * nk * 4, st);
+    const cudaError_t e2 = e1 == cudaSuccess ? cudaMemsetAsync(dv2, 0, 2 * nk * 4, st) : e1;
     if (e2 != cudaSuccess) {
       rc = cuda_fail(e2);
       ok = false;
     }
+  }
+  if (ok) {
+    fa::fa_bwd_dup_rows_kernel<<<grid8(nk / 8), 256, 0, st>>>(static_cast<const uint4*>(k),
+                                                              reinterpret_cast<uint4*>(k2), nk / 8, D);
+    ok = launched();
   }
   if (ok) {
     // d_row = rowsum(dO * (O + o_lo)) from the forward's output as given
@@ -836,14 +852,18 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   // per head g of every group and batch of KV planes [p0, p0 + np): the query
   // planes are p * G + g, so Q, dO and dQ advance by G planes per KV plane
   const long long sQ = (long long)G * Sq * D, sK = (long long)Skv * D, sM = (long long)plane_mat;
+  const long long sK2 = 2 * sK, sM2 = 2 * sM;   // K2, dK2, dV2; the pairs as 16-bit matrices
   const auto* q16 = static_cast<const uint16_t*>(q);
   const auto* k16 = static_cast<const uint16_t*>(k);
   const auto* v16 = static_cast<const uint16_t*>(v);
   const auto* do16 = static_cast<const uint16_t*>(dout);
+  const auto* p2 = reinterpret_cast<const uint16_t*>(sm);    // P pairs: [Sq x 2 Skv] per plane
+  const auto* ds2 = reinterpret_cast<const uint16_t*>(dpm);  // dS pairs
   for (int g = 0; ok && g < G; ++g) {
     for (int p0 = 0; ok && p0 < planes; p0 += chunk) {
       const int np = std::min(chunk, planes - p0);
-      const long long qo = ((long long)p0 * G + g) * Sq * D, ko = (long long)p0 * Skv * D;
+      const long long qo = ((long long)p0 * G + g) * Sq * D, ko = (long long)p0 * sK;
+      const long long ko2 = 2 * ko;
       // Causal problems go in blocks of kBwdRowBlock query rows, each against
       // the keys up to its last row only (top-left: row i sees keys j <= i), so
       // that the masked half of S is neither computed nor stored.
@@ -856,46 +876,33 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
                           status};
         const dim3 eg(nr, np);
         const long long qr = qo + (long long)r0 * D;       // the block's rows of Q, dO, dQ
-        const long long mr = (long long)r0 * Skv;           // ... of S, P, dP, dS
+        const long long mr = (long long)r0 * Skv;           // ... of S, dP (fp32 elements)
         const bool vec = Skv % 8 == 0 && nc % 8 == 0;
         ok = gemm_rm16(h, t16, false, true, nr, nc, D, 1.f, q16 + qr, D, sQ, k16 + ko, D, sK, 0.f,
                        sm + mr, Skv, sM, np);                                 // S = Q K^T
-        if (ok) {                                                             // P = hi + lo
-          if (fp16) {
-            if (vec) fa::fa_bwd_p_hilo_kernel<false, 8><<<eg, 256, 0, st>>>(sm, ph, pl, r);
-            else fa::fa_bwd_p_hilo_kernel<false, 1><<<eg, 256, 0, st>>>(sm, ph, pl, r);
-          } else {
-            if (vec) fa::fa_bwd_p_hilo_kernel<true, 8><<<eg, 256, 0, st>>>(sm, ph, pl, r);
-            else fa::fa_bwd_p_hilo_kernel<true, 1><<<eg, 256, 0, st>>>(sm, ph, pl, r);
-          }
-          ok = launched();
-        }
-        for (int part = 0; ok && part < 2; ++part)                           // dV += P^T dO
-          ok = gemm_rm16(h, t16, true, false, nc, D, nr, 1.f, (part ? pl : ph) + mr, Skv, sM,
-                         do16 + qr, D, sQ, 1.f, dv32 + ko, D, sK, np);
         if (ok) ok = gemm_rm16(h, t16, false, true, nr, nc, D, 1.f, do16 + qr, D, sQ, v16 + ko, D,
-                               sK, 0.f, sm + mr, Skv, sM, np);               // dP = dO V^T
-        if (ok) {                                                             // dS = hi + lo
+                               sK, 0.f, dpm + mr, Skv, sM, np);              // dP = dO V^T
+        if (ok) {                                                             // P, dS pairs
           if (fp16) {
-            if (vec) fa::fa_bwd_ds_hilo_kernel<false, 8><<<eg, 256, 0, st>>>(ph, pl, sm, r);
-            else fa::fa_bwd_ds_hilo_kernel<false, 1><<<eg, 256, 0, st>>>(ph, pl, sm, r);
+            if (vec) fa::fa_bwd_p_ds_kernel<false, 8><<<eg, 256, 0, st>>>(sm, dpm, r);
+            else fa::fa_bwd_p_ds_kernel<false, 1><<<eg, 256, 0, st>>>(sm, dpm, r);
           } else {
-            if (vec) fa::fa_bwd_ds_hilo_kernel<true, 8><<<eg, 256, 0, st>>>(ph, pl, sm, r);
-            else fa::fa_bwd_ds_hilo_kernel<true, 1><<<eg, 256, 0, st>>>(ph, pl, sm, r);
+            if (vec) fa::fa_bwd_p_ds_kernel<true, 8><<<eg, 256, 0, st>>>(sm, dpm, r);
+            else fa::fa_bwd_p_ds_kernel<true, 1><<<eg, 256, 0, st>>>(sm, dpm, r);
           }
           ok = launched();
         }
-        for (int part = 0; ok && part < 2; ++part)                           // dQ = scale dS K
-          ok = gemm_rm16(h, t16, false, false, nr, D, nc, scale, (part ? pl : ph) + mr, Skv, sM,
-                         k16 + ko, D, sK, part ? 1.f : 0.f, dq32 + qr, D, sQ, np);
-        for (int part = 0; ok && part < 2; ++part)                           // dK += scale dS^T Q
-          ok = gemm_rm16(h, t16, true, false, nc, D, nr, scale, (part ? pl : ph) + mr, Skv, sM,
-                         q16 + qr, D, sQ, 1.f, dk32 + ko, D, sK, np);
+        if (ok) ok = gemm_rm16(h, t16, true, false, 2 * nc, D, nr, 1.f, p2 + 2 * mr, 2 * Skv, sM2,
+                               do16 + qr, D, sQ, 1.f, dv2 + ko2, D, sK2, np);  // dV2 += P2^T dO
+        if (ok) ok = gemm_rm16(h, t16, false, false, nr, D, 2 * nc, scale, ds2 + 2 * mr, 2 * Skv,
+                               sM2, k2 + ko2, D, sK2, 0.f, dq32 + qr, D, sQ, np);  // dQ = scale dS2 K2
+        if (ok) ok = gemm_rm16(h, t16, true, false, 2 * nc, D, nr, scale, ds2 + 2 * mr, 2 * Skv,
+                               sM2, q16 + qr, D, sQ, 1.f, dk2 + ko2, D, sK2, np);  // dK2 += scale dS2^T Q
       }
       if (!ok && rc == FA_OK) rc = cuda_fail(cudaErrorUnknown);
     }
   }
-  if (ok) ok = from32(dq32, dq, nq) && from32(dk32, dk, nk) && from32(dv32, dv, nk);
+  if (ok) ok = from32(dq32, dq, nq) && from32_pairs(dk2, dk, nk) && from32_pairs(dv2, dv, nk);
   cudaFreeAsync(scratch, st);
   return rc;
 }

@@ -311,8 +311,10 @@ int fa_fwd_o_lo(const void* q, const void* k, const void* v, void* o, void* o_lo
  * type).  With fp16 inputs a |dS| beyond 65504 cannot be held by the pair:
  * the gradients are then not finite and fa_check_status() reports
  * FA_ERR_RANGE.  Stream-ordered scratch (cudaMallocAsync, freed on `stream`):
- * d_row; fp32 dq, dk, dv; 8 * Sq * Skv bytes per plane of a batch, batches of
- * up to 1 GiB (at least one plane).  Calls from several host threads
+ * d_row; fp32 dq; fp32 dk and dv with two rows per key (the products of the
+ * hi and lo parts, summed at the end); k with every row twice (16-bit);
+ * 8 * Sq * Skv bytes per plane of a batch (S and dP in fp32, then the P and
+ * dS pairs in place), batches of up to 1 GiB (at least one plane).  Calls from several host threads
  * serialise their enqueueing on one lock per process.  Returns FA_OK or a
  * negative FA_ERR_* code (nothing launched on an argument error). */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* o_lo,
