@@ -416,60 +416,70 @@ def kernel_name(p):
             f"{',convert-V' if bf16 else ''}>")
 
 
-def other_workloads(args, dev, dist, world, local, peak):
-    """The same path on the other workloads (one fa_fwd call per step, threshold
-    0, the given slot order), each timed like the benchmark line with its own
-    clock record: ms per call, algorithmic TFLOP/s, fraction of the peak, and
-    the DRAM bytes per launch of the latest ncu capture of that kernel (null
-    when its sources changed since)."""
-    import torch
+def time_workload(args, dev, dist, world, local, peak, name, p, threshold=0.0, traffic=True):
+    """One workload entry: the path on problem `p` (workload `name`'s shape) at
+    `threshold`, timed like the benchmark line with its own clock record: ms
+    per call, algorithmic TFLOP/s, fraction of the peak, and the DRAM bytes
+    per launch of the latest ncu capture of that kernel (null when its sources
+    changed since, or when the capture is of another configuration)."""
     from attention_forward_fa_gb300 import workloads as W
-    out = {}
-    for name in ("c3", "c4", "c5"):
-        p = workload_problem(name)
-        flops = W.algorithmic_flops(p)
-        prep = Prepared(p, dev)
-        total_ms, kern_ms, conv_ms, clocks, graph = timed_steps(
-            prep, args.workload_steps, 5, args.workload_soak, dist, local)
-        total_ms, kern_ms = max_over_ranks(dist, [total_ms, kern_ms], dev)
-        ms = total_ms / args.workload_steps
-        achieved = flops / (kern_ms * 1e-3) / 1e12
-        e = {"config": workload_desc(p, name), "algorithmic_gflop": flops / 1e9,
-             "ms_per_call": ms, "tflops": whole_job_tflops(world, flops, ms),
-             "kernel": kernel_name(p), "kernel_ms": kern_ms,
-             "kernel_tflops": achieved, "frac": achieved / peak, "steps": args.workload_steps,
-             "timing": "CUDA graph of the steps" if graph else "eager, events around each launch",
-             "clocks": clocks, "traffic": dram_traffic(name)}
-        if e["traffic"] is not None:
-            e["dram_gbs"] = e["traffic"] / (kern_ms * 1e-3) / 1e9
-        if prep.conv_pass:
-            e["other_kernel"] = {"name": "fa_convert_v_kernel (bf16 -> fp16 copy of the key latent)",
-                                 "avg_ms": conv_ms}
-        out[name] = e
-        del prep
-        torch.cuda.empty_cache()
-    # the benchmark's workload at the lazy threshold (8 log2 units) instead of
-    # the exact running max: the cost of the exact max, which the pages put at
-    # about 4 % of the forward on this GPU
-    p = workload_problem("c2")
     flops = W.algorithmic_flops(p)
     prep = Prepared(p, dev)
-    prep.threshold = 8.0
-    total_ms, kern_ms, _, clocks, graph = timed_steps(
+    prep.threshold = threshold
+    total_ms, kern_ms, conv_ms, clocks, graph = timed_steps(
         prep, args.workload_steps, 5, args.workload_soak, dist, local)
     total_ms, kern_ms = max_over_ranks(dist, [total_ms, kern_ms], dev)
     ms = total_ms / args.workload_steps
-    cfg = workload_desc(p, "c2")
-    cfg["rescale_threshold"] = 8.0
     achieved = flops / (kern_ms * 1e-3) / 1e12
-    out["c2_threshold_8"] = {"config": cfg, "algorithmic_gflop": flops / 1e9, "ms_per_call": ms,
-                             "tflops": whole_job_tflops(world, flops, ms), "kernel": kernel_name(p),
-                             "kernel_ms": kern_ms, "kernel_tflops": achieved,
-                             "frac": achieved / peak, "steps": args.workload_steps,
-                             "timing": "CUDA graph of the steps" if graph else
-                                       "eager, events around each launch",
-                             "clocks": clocks}
-    del prep
+    cfg = workload_desc(p, name)
+    cfg["rescale_threshold"] = threshold
+    e = {"config": cfg, "algorithmic_gflop": flops / 1e9,
+         "ms_per_call": ms, "tflops": whole_job_tflops(world, flops, ms),
+         "kernel": kernel_name(p), "kernel_ms": kern_ms,
+         "kernel_tflops": achieved, "frac": achieved / peak, "steps": args.workload_steps,
+         "timing": "CUDA graph of the steps" if graph else "eager, events around each launch",
+         "clocks": clocks, "traffic": dram_traffic(name) if traffic else None}
+    if e["traffic"] is not None:
+        e["dram_gbs"] = e["traffic"] / (kern_ms * 1e-3) / 1e9
+    if prep.conv_pass:
+        e["other_kernel"] = {"name": "fa_convert_v_kernel (bf16 -> fp16 copy of the key latent)",
+                             "avg_ms": conv_ms}
+    return e
+
+
+def other_workloads(args, dev, dist, world, local, peak):
+    """The same path on the other workloads (one fa_fwd call per step, threshold
+    0, the given slot order); the top-k workload also at the lazy threshold and
+    with every token's slot order reversed (the four runs the pages measure it
+    in); and the benchmark's workload at the lazy threshold."""
+    import dataclasses
+    import numpy as np
+    import torch
+    out = {}
+    for name in ("c3", "c4", "c5"):
+        p = workload_problem(name)
+        out[name] = time_workload(args, dev, dist, world, local, peak, name, p)
+        torch.cuda.empty_cache()
+        if name == "c5":
+            # self key last, invalid slots first; the same valid pairs
+            rev = dataclasses.replace(p, name=p.name + "_reversed",
+                                      topk_idx=np.ascontiguousarray(p.topk_idx[:, :, ::-1]))
+            for key, prob, thr in (("c5_threshold_8", p, 8.0), ("c5_reversed", rev, 0.0),
+                                   ("c5_reversed_threshold_8", rev, 8.0)):
+                e = time_workload(args, dev, dist, world, local, peak, name, prob, thr,
+                                  traffic=False)
+                e["config"]["slot_order"] = "reversed" if prob is rev else "given"
+                out[key] = e
+                torch.cuda.empty_cache()
+            out["c5"]["config"]["slot_order"] = "given"
+            # the exact running max's cost on the top-k workload
+            out["c5_threshold_8"]["exact_max_cost"] = (out["c5"]["ms_per_call"] /
+                                                       out["c5_threshold_8"]["ms_per_call"] - 1)
+    # the benchmark's workload at the lazy threshold (8 log2 units) instead of
+    # the exact running max: the cost of the exact max, which the pages put at
+    # about 4 % of the forward on this GPU
+    out["c2_threshold_8"] = time_workload(args, dev, dist, world, local, peak, "c2",
+                                          workload_problem("c2"), 8.0, traffic=False)
     torch.cuda.empty_cache()
     return out
 
