@@ -53,6 +53,7 @@ constexpr int kMlaDq = 256;                  // value columns per CTA
 constexpr int kMlaSplit = kMlaDv / kMlaDq;   // CTAs per (token, head group)
 constexpr int kMlaHeads = 128;               // query heads per CTA (MMA rows)
 constexpr int kMlaNS = 2;                    // ring stages
+constexpr int kMlaRescaleChunks = 2;         // O columns per TMEM round trip of a rescale: x 32
 constexpr int kMlaProducers = 3;             // producer warps, all on every tile
 constexpr int kMlaMmaWarp = 4 + kMlaProducers;
 constexpr int kMlaThreads = 32 * (kMlaMmaWarp + 1);
@@ -412,22 +413,28 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         }
         tc_fence_after();
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // O *= alpha, kMlaRescaleChunks 32-column chunks per TMEM round trip
           const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
-          for (int cc = 0; cc < kMlaDq / 32; ++cc) {
-            uint32_t o32[32];
-            tmem_ld32(tO + 32 * cc, o32);
+          for (int cc = 0; cc < kMlaDq / 32; cc += kMlaRescaleChunks) {
+            uint32_t o32[kMlaRescaleChunks][32];
+#pragma unroll
+            for (int u = 0; u < kMlaRescaleChunks; ++u) tmem_ld32(tO + 32 * (cc + u), o32[u]);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float x0, x1;
-              f2_unpack(f2_mul(f2_pack(__uint_as_float(o32[2 * i]), __uint_as_float(o32[2 * i + 1])),
-                               a2),
-                        x0, x1);
-              o32[2 * i] = __float_as_uint(x0);
-              o32[2 * i + 1] = __float_as_uint(x1);
+            for (int u = 0; u < kMlaRescaleChunks; ++u) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float x0, x1;
+                f2_unpack(f2_mul(f2_pack(__uint_as_float(o32[u][2 * i]),
+                                         __uint_as_float(o32[u][2 * i + 1])),
+                                 a2),
+                          x0, x1);
+                o32[u][2 * i] = __float_as_uint(x0);
+                o32[u][2 * i + 1] = __float_as_uint(x1);
+              }
+              tmem_st32(tO + 32 * (cc + u), o32[u]);
             }
-            tmem_st32(tO + 32 * cc, o32);
           }
         }
         tmem_st32(tP, ph);
