@@ -124,6 +124,19 @@ __global__ void __launch_bounds__(256) fa_bwd_p_ds_kernel(float* __restrict__ s,
   bool big = false;
   for (int j0 = threadIdx.x * kV; j0 < r.ncols; j0 += blockDim.x * kV) {
     float x[kV], y[kV];
+    if (j0 >= lim) {   // every key of the group masked: zero pairs, S and dP not read
+      if constexpr (kV == 8) {
+        const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(s + base + j0) = zero;
+        *reinterpret_cast<uint4*>(s + base + j0 + 4) = zero;
+        *reinterpret_cast<uint4*>(dp + base + j0) = zero;
+        *reinterpret_cast<uint4*>(dp + base + j0 + 4) = zero;
+      } else {
+        reinterpret_cast<uint32_t*>(s)[base + j0] = 0u;
+        reinterpret_cast<uint32_t*>(dp)[base + j0] = 0u;
+      }
+      continue;
+    }
     if constexpr (kV == 8) {
       const float4 a = *reinterpret_cast<const float4*>(s + base + j0);
       const float4 c = *reinterpret_cast<const float4*>(s + base + j0 + 4);
