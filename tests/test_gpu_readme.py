@@ -1,5 +1,5 @@
-"""The usage example of the README runs as written (forward, residual output,
-backward, optional terms, status check)."""
+"""The repository's front-page usage example (its first python block) runs as
+written: forward, residual output, backward, optional terms, status check."""
 import re
 from pathlib import Path
 
@@ -11,9 +11,9 @@ pytestmark = pytest.mark.gpu
 def test_readme_usage_example_runs():
     text = (Path(__file__).resolve().parents[1] / "README.md").read_text()
     blocks = re.findall(r"```python\n(.*?)```", text, re.S)
-    assert blocks, "no python block in the README"
+    assert blocks, "no python block on the front page"
     env = {}
-    exec(compile(blocks[0], "README.md", "exec"), env)
+    exec(compile(blocks[0], "usage-example", "exec"), env)
     import torch
     torch.cuda.synchronize()
     for name in ("o", "lse", "o_lo", "dq", "dk", "dv", "o2", "lse2"):
